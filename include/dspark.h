@@ -1,0 +1,219 @@
+/*
+ * dspark.h — C ABI of the DSpark ragged-verification hot path for one GB300 (sm_103a).
+ *
+ * A decode step of confidence-driven variable-length speculative verification runs four calls,
+ * each one asynchronous on the caller's CUDA stream:
+ *
+ *   dspark_schedule  confidences c[b,j]  -> per-request verify windows w_b and K*
+ *   dspark_pack      windows, block tokens -> cu_seqlens, capture tier, packed token buffer
+ *   dspark_verify    packed target logits [M,V] (+ draft logits) -> accept lengths, committed tokens
+ *   dspark_scatter   committed tokens -> per-request output histories
+ *
+ * Source of the method: "DSpark in SGLang: Speculative Decoding with Confidence-Driven,
+ * Variable-Length Verification" (LMSYS blog, as summarised by papercache.org), sections
+ * "A2 method details" (confidence scheduler, verify modes, ragged verify over full CUDA graphs,
+ * cost-table modelling) and the quick-read summary; the min(1, p/q) accept rule as restated in
+ * the lshu.cn DSpark/SGLang article, sections 2.3 and 3.3.
+ *
+ * Conventions shared by every entry point
+ *   - Every array pointer is a DEVICE pointer owned by the caller, unless its comment says
+ *     "host". The library never allocates, frees or retains caller memory.
+ *   - Arrays are dense, row-major, with the shapes given in brackets; int32_t is little-endian
+ *     two's complement; "bf16" is IEEE bfloat16 stored in 16 bits.
+ *   - B = number of requests, gamma = block width (1 anchor + gamma-1 drafts), V = vocabulary.
+ *   - All work is enqueued on `stream` (0 = legacy default stream); nothing synchronises the host.
+ *   - Return value: DSPARK_OK, or a negative DSPARK_ERR_* code when the host-side argument check
+ *     or the kernel launch failed. On error nothing was enqueued (argument errors) or the launch
+ *     was refused (DSPARK_ERR_CUDA); dspark_last_error() then describes it.
+ *   - Data-dependent problems that only the device can see (a total beyond the largest tier,
+ *     a window outside [1,gamma], an output history that is full, ...) never fault and never
+ *     trap: the kernel ORs a DSPARK_STATUS_* bit into the caller's int32 `status` word, applies
+ *     the documented clamp and carries on. The caller zeroes `status` when it wants a fresh
+ *     report and reads it whenever convenient.
+ *   - No kernel waits on another kernel, a flag or a peer; nothing can hang.
+ */
+#ifndef DSPARK_H_
+#define DSPARK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes ---------------------------------------------------------------------- */
+#define DSPARK_OK                  0
+#define DSPARK_ERR_INVALID_ARG   (-1)  /* null pointer, bad size, bad enum, short workspace */
+#define DSPARK_ERR_UNSUPPORTED   (-2)  /* valid request beyond this build's limits           */
+#define DSPARK_ERR_CUDA          (-3)  /* the CUDA runtime refused a query or a launch       */
+
+/* ---- device status bits (OR-ed into the caller's int32 status word) -------------------- */
+#define DSPARK_STATUS_TIER_OVERFLOW  0x01 /* M above every tier: tier := M (pack)                */
+#define DSPARK_STATUS_PACK_CAPACITY  0x02 /* tier above packed_cap: rows >= packed_cap unwritten */
+#define DSPARK_STATUS_BAD_WINDOW     0x04 /* a window outside [1,gamma]: clamped into it        */
+#define DSPARK_STATUS_OUT_OVERFLOW   0x08 /* a history reached out_cap: tokens past it dropped   */
+#define DSPARK_STATUS_BAD_COST       0x10 /* no K had a finite positive T: K* := 0               */
+#define DSPARK_STATUS_BAD_ROWS       0x20 /* a request's logits rows lie outside the buffer      */
+#define DSPARK_STATUS_BAD_TOKEN      0x40 /* a draft id outside [0,V): treated as rejected       */
+#define DSPARK_STATUS_BAD_LENGTH     0x80 /* accept_len / out_len outside range: clamped         */
+
+/* ---- limits of this build ------------------------------------------------------------- */
+#define DSPARK_MAX_GAMMA        32     /* block width                                         */
+#define DSPARK_MAX_CANDIDATES   16384  /* B*(gamma-1): the scheduler sorts them in one CTA    */
+#define DSPARK_MAX_BATCH        8192   /* B for schedule and pack (single-CTA scans)          */
+#define DSPARK_MAX_TIERS        1024
+
+typedef enum { DSPARK_BF16 = 0, DSPARK_F32 = 1 } dspark_dtype;
+
+/* Verify modes ("A2 method details", verify-mode design):
+ *   STATIC     verifies the whole block every step: w_b := gamma, commits the full-block accept.
+ *   COMPACT    verifies only the scheduled window: logits hold the packed rows of cu_seqlens.
+ *   CAP_ACCEPT verifies the whole block but commits exactly what COMPACT would commit; it also
+ *              reports the accept length full verification would have given (the ceiling).  */
+typedef enum { DSPARK_STATIC = 0, DSPARK_COMPACT = 1, DSPARK_CAP_ACCEPT = 2 } dspark_mode;
+
+/* Additive step-cost model T(bs,K) = bias + alpha(bs) + theta(bs+K) ("A2 method details",
+ * cost-table profiling and modelling). Host struct; `alpha` and `theta` are DEVICE arrays of
+ * doubles indexed by bs and by M = bs+K. dspark_schedule reads alpha[B] and theta[B..B*gamma],
+ * so alpha_len >= B+1 and theta_len >= B*gamma+1. The struct itself is read during the call
+ * only and may live on the host stack. */
+typedef struct {
+    double        bias;
+    const double* alpha;
+    int32_t       alpha_len;
+    const double* theta;
+    int32_t       theta_len;
+} dspark_cost;
+
+/* ---------------------------------------------------------------------------------------
+ * dspark_schedule — confidence scheduler ("A2 method details": the confidence head's scores
+ * multiply along the block into a survival probability; the scheduler turns survivals into
+ * per-request verify budgets by trading expected accepted tokens against the cost table).
+ *
+ *   s[b,j]   = prod_{i<=j} clamp(conf[b,i], 0, 1)           fp32, sequential, j = 0..gamma-2
+ *   key[b,j] = round_to_nearest_even(s[b,j] * 2^32)         exact uint64 fixed point
+ *   order    = keys descending; ties by b ascending, then j ascending
+ *   S(K)     = sum of the first K keys in that order          (exact integer)
+ *   obj(K)   = double(B*2^32 + S(K)) / T,  T = (bias + alpha[B]) + theta[B+K]
+ *   K*       = the smallest K in [0, B*(gamma-1)] with the largest obj among K whose T is finite
+ *              and positive (none: K* = 0 and DSPARK_STATUS_BAD_COST)
+ *   w_b      = 1 + number of request b's entries among the first K* in the order
+ *
+ * conf     [B, gamma-1] fp32 (NaN counts as 0)       windows [B] int32 out    k_star [1] int32 out
+ * status   [1] int32 in/out (may be NULL: the bits are then dropped)
+ * Limits: 0 <= B <= DSPARK_MAX_BATCH, 1 <= gamma <= DSPARK_MAX_GAMMA,
+ *         B*(gamma-1) <= DSPARK_MAX_CANDIDATES. B == 0 writes k_star = 0 only.
+ * One single-CTA kernel; no workspace.
+ * ------------------------------------------------------------------------------------- */
+int dspark_schedule(const float* conf, int B, int gamma, const dspark_cost* cost,
+                    int32_t* windows, int32_t* k_star, int32_t* status, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * dspark_pack — ragged front-pack ("A2 method details", ragged verify over full CUDA graphs:
+ * variable windows are packed to the front of one compact cu_seqlens-style buffer and only the
+ * total is rounded up to the nearest captured graph tier).
+ *
+ *   w_b         = clamp(windows[b], 1, gamma)   (out of range: DSPARK_STATUS_BAD_WINDOW)
+ *   cu_seqlens  = exclusive scan of w: cu[0] = 0, cu[b+1] = cu[b] + w_b, M = cu[B]
+ *   tier        = min{ tiers[t] : tiers[t] >= M }; none: tier = M, DSPARK_STATUS_TIER_OVERFLOW
+ *   rows r < M  : packed_ids[r] = block_tokens[b, i], row_req[r] = b, row_pos[r] = i
+ *                 for the unique (b, i < w_b) with r = cu[b] + i
+ *   rows M..tier-1 (padding): packed_ids = 0, row_req = -1, row_pos = -1
+ *   rows >= packed_cap are never written (DSPARK_STATUS_PACK_CAPACITY if tier > packed_cap)
+ *   meta        = { M, tier }
+ *
+ * windows [B] int32          block_tokens [B, gamma] int32 (column 0 = anchor, 1.. = drafts)
+ * tiers [n_tiers] int32 device, any order      cu_seqlens [B+1] int32 out
+ * packed_ids, row_req, row_pos [packed_cap] int32 out (row_req/row_pos may be NULL)
+ * meta [2] int32 out          status [1] int32 in/out or NULL
+ * Limits: 0 <= B <= DSPARK_MAX_BATCH, 1 <= gamma <= DSPARK_MAX_GAMMA,
+ *         1 <= n_tiers <= DSPARK_MAX_TIERS, packed_cap >= 0.
+ * ------------------------------------------------------------------------------------- */
+int dspark_pack(const int32_t* windows, const int32_t* block_tokens, int B, int gamma,
+                const int32_t* tiers, int n_tiers, int32_t* cu_seqlens,
+                int32_t* packed_ids, int32_t* row_req, int32_t* row_pos, int packed_cap,
+                int32_t* meta, int32_t* status, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * dspark_verify — verify over the target logits and reduce to per-request accept lengths.
+ *
+ * Rows. Target row for (request b, block position i):
+ *   COMPACT              row cu_seqlens[b] + i, i < w_b         (target_logits = packed [M, V])
+ *   STATIC, CAP_ACCEPT   row b*gamma + i,       i < gamma       (target_logits = block [B*gamma, V])
+ * target row (b,i) is the target's distribution for block position i+1, which holds the draft
+ * d_{i+1} = block_tokens[b, i+1]. Draft row (b,i) of draft_logits [B, gamma-1, V] is the draft
+ * distribution that d_{i+1} was sampled from (stochastic only).
+ * Any row index outside [0, target_rows) flags DSPARK_STATUS_BAD_ROWS and the request commits
+ * nothing (accept_len 0, committed all -1).
+ *
+ * Greedy (stochastic == 0): g[b,i] = argmax_v target[row(b,i), v] (lowest v on ties; NaN
+ *   unsupported). d_{i+1} is accepted iff d_{i+1} == g[b,i]; L = 1 + number of leading accepts;
+ *   committed[b, k] = g[b, k] for k < L (the accepted drafts followed by the target's token).
+ *
+ * Stochastic (stochastic == 1; the min(1, p/q) rule of the lshu.cn article, sections 2.3/3.3):
+ *   p = softmax(target_row / temperature), q = softmax(draft_row / temperature) over all V.
+ *   Uniforms come from Philox4x64-10 (Salmon et al., SC'11) with key (seed, 0) and counter
+ *   (b, i, step, 0): word 0 gives u = (w0 >> 40) * 2^-24 for the accept test of d_{i+1},
+ *   word 1 gives u' = (w1 >> 11) * 2^-53 for a bonus drawn at position i.
+ *   d_{i+1} is accepted iff q(d) == 0 or u < float(p(d) / q(d)).
+ *   First rejection at position i: the bonus is drawn from the residual max(0, p - q) of row i
+ *   (normalised); no rejection among the w_b - 1 drafts: the bonus is drawn from p of row
+ *   w_b - 1. Drawing: the smallest v whose running sum (in v order) exceeds u' * total.
+ *   committed[b] = d_1 .. d_{L-1}, bonus.
+ *
+ * Modes: STATIC uses w_b := gamma. CAP_ACCEPT commits exactly what COMPACT commits for the same
+ *   windows (its decisions and bonus depend on rows i < w_b only) and writes
+ *   ceiling_len[b] = the accept length over all gamma-1 drafts. STATIC writes ceiling_len =
+ *   accept_len; COMPACT writes -1 (when ceiling_len != NULL).
+ *
+ * target_logits [target_rows, V] bf16 or fp32 (dtype); draft_logits [B, gamma-1, V] same dtype
+ *   (stochastic only, else NULL). cu_seqlens [B+1] (COMPACT only, else may be NULL).
+ * windows [B] int32 (COMPACT/CAP_ACCEPT; clamped to [1,gamma], DSPARK_STATUS_BAD_WINDOW)
+ * block_tokens [B, gamma] int32; ids outside [0,V) flag DSPARK_STATUS_BAD_TOKEN and reject.
+ * accept_len [B] int32 out; committed [B, gamma] int32 out (-1 after the L committed tokens);
+ * ceiling_len [B] int32 out or NULL; row_prob [target_rows, 2] fp32 out or NULL: (p(d), q(d))
+ *   of every target row that carries a stochastic accept test, (-1, -1) on the other rows of a
+ *   request (always -1 in greedy mode).
+ * workspace: device scratch of at least dspark_verify_workspace_bytes(B, gamma, V, stochastic)
+ *   bytes, 16-byte aligned, owned by the caller, fully rewritten by every call before it is
+ *   read (no clearing needed). Calls that share one workspace must not overlap on the GPU.
+ * Limits: 0 <= B, 1 <= gamma <= DSPARK_MAX_GAMMA, V >= 1, temperature > 0 (stochastic).
+ * Two kernels: a persistent streaming kernel over fixed row chunks, then one CTA per request.
+ * ------------------------------------------------------------------------------------- */
+int dspark_verify(dspark_mode mode, int stochastic,
+                  const void* target_logits, int target_rows, const void* draft_logits,
+                  dspark_dtype dtype, int V,
+                  const int32_t* cu_seqlens, const int32_t* windows, const int32_t* block_tokens,
+                  int B, int gamma, float temperature, uint64_t seed, uint64_t step,
+                  int32_t* accept_len, int32_t* committed, int32_t* ceiling_len, float* row_prob,
+                  void* workspace, size_t workspace_bytes, int32_t* status, cudaStream_t stream);
+
+/* Bytes of device workspace dspark_verify needs for these sizes (0 when B == 0); a value
+ * that depends on the sizes only. Returns 0 and sets dspark_last_error on invalid sizes. */
+size_t dspark_verify_workspace_bytes(int B, int gamma, int V, int stochastic);
+
+/* ---------------------------------------------------------------------------------------
+ * dspark_scatter — compact scatter ("A2 method details", performance: the fused kernel that
+ * writes accepted tokens back to per-request state).
+ *   L = clamp(accept_len[b], 0, gamma), n = clamp(out_len[b], 0, out_cap)
+ *   out_tokens[b, n + i] = committed[b, i] for i < L and n + i < out_cap
+ *   out_len[b] = min(out_cap, n + L)   (tokens past out_cap: DSPARK_STATUS_OUT_OVERFLOW)
+ * committed [B, gamma] int32; accept_len [B] int32; out_tokens [B, out_cap] int32 in/out;
+ * out_len [B] int32 in/out; status [1] int32 in/out or NULL. Limits: B >= 0, 1 <= gamma <= 32.
+ * ------------------------------------------------------------------------------------- */
+int dspark_scatter(const int32_t* committed, const int32_t* accept_len, int B, int gamma,
+                   int32_t* out_tokens, int32_t* out_len, int out_cap, int32_t* status,
+                   cudaStream_t stream);
+
+/* Message of the last failed call on this host thread ("" if none). Never NULL. */
+const char* dspark_last_error(void);
+
+/* ABI version: 100 * major + minor. */
+int dspark_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSPARK_H_ */
