@@ -1,0 +1,760 @@
+// verify.cu — verify over the target logits and reduction to per-request accept lengths.
+//
+// Greedy: a draft survives iff it equals the target row's argmax; the accept length ends at
+// the first divergence (lshu.cn DSpark article, 1.2). Stochastic: accept with probability
+// min(1, p(d)/q(d)) (lshu.cn article, 2.3 and 3.3) with the residual bonus sample of standard
+// speculative sampling. Modes: "DSpark in SGLang" (LMSYS blog summary), A2 verify-mode design
+// (static, compact, cap-accept: full-block verify that commits exactly what compact commits).
+//
+// Two kernels per call.
+//
+// 1. verify_stream_kernel — the HBM-bound part. Every logits row is cut into nc chunks at
+//    fixed offsets (c * C, C a multiple of 8 elements chosen from V and B*gamma only, never
+//    from M), so a row's statistics are bit-identical wherever the row sits in the buffer:
+//    compact and cap-accept see the same numbers for the same row. A persistent grid of warps
+//    walks the flat list of (row, chunk) units; each warp owns a contiguous run of units and
+//    streams each chunk with 16-byte read-only loads (eight in flight per lane), then
+//    reduces across the warp with shuffles and writes one partial per unit:
+//      greedy:     (max value, lowest index of it)
+//      stochastic: (max logit m, sum of exp2((l - m) * log2(e)/T)) — an online softmax.
+//    Stochastic calls also stream the draft rows of every tested draft (M - B rows in
+//    compact mode).
+// 2. verify_finalize_kernel — one CTA per request: combines the chunk partials of its rows in
+//    a fixed order, runs the accept tests (Philox4x64-10 uniforms), walks to the first
+//    rejection, writes accept_len / committed / ceiling, and for stochastic calls draws the
+//    bonus token with one more pass over the one or two rows it needs.
+#include <math.h>
+
+#include "common.cuh"
+
+namespace dspark {
+namespace {
+
+constexpr int kStreamThreads = 256;
+constexpr int kStreamWarps = kStreamThreads / 32;
+constexpr int kUnroll = 8;            // 16-byte loads in flight per lane
+constexpr int kFinalThreads = 256;
+constexpr int kFinalWarps = kFinalThreads / 32;
+constexpr int kTargetUnits = 8192;    // aim: about one or two units per resident warp
+constexpr int kMaxChunk = 4096;       // elements per chunk, upper bound
+constexpr int kMinChunk = 256;        // elements per chunk, lower bound
+constexpr int kMaxVocabStochastic = 1 << 20;
+
+struct __align__(8) ArgPart {
+    float v;
+    int idx;
+};
+struct __align__(16) SoftPart {
+    float m;
+    float pad;
+    double z;
+};
+
+struct Plan {
+    int nc;       // chunks per row
+    int C;        // elements per chunk (multiple of 8)
+    int64_t rows_max;
+};
+
+Plan make_plan(int V, int B, int gamma)
+{
+    Plan p;
+    p.rows_max = static_cast<int64_t>(B) * gamma;
+    const int64_t nc_min = ceil_div(V, kMaxChunk);
+    const int64_t nc_max = V / kMinChunk > 0 ? V / kMinChunk : 1;
+    const int64_t nc_want = ceil_div(kTargetUnits, p.rows_max > 0 ? p.rows_max : 1);
+    int64_t nc = nc_want < nc_max ? nc_want : nc_max;
+    if (nc < nc_min) nc = nc_min;
+    int64_t C = ceil_div(ceil_div(V, nc), 8) * 8;
+    p.C = static_cast<int>(C);
+    p.nc = static_cast<int>(ceil_div(V, C));
+    return p;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct StreamArgs {
+    const void* target;
+    const void* draft;
+    const int32_t* cu;
+    const int32_t* windows;
+    void* part_t;
+    void* part_d;
+    int32_t* status;
+    int mode, V, nc, C, vec, B, gamma, target_rows;
+    int64_t rows_max;
+    float s;   // log2(e) / temperature
+};
+
+// Rows this call verifies: compact M = cu[B] (bounded by the buffer), else B*gamma.
+__device__ __forceinline__ int64_t target_row_count(int mode, const int32_t* cu, int B, int gamma,
+                                                    int target_rows, int64_t rows_max)
+{
+    int64_t n;
+    if (mode == DSPARK_COMPACT) n = cu[B];
+    else n = static_cast<int64_t>(B) * gamma;
+    if (n < 0) n = 0;
+    if (n > target_rows) n = target_rows;
+    if (n > rows_max) n = rows_max;
+    return n;
+}
+
+__device__ __forceinline__ void arg_merge(float& v, int& i, float v2, int i2)
+{
+    if (v2 > v || (v2 == v && i2 < i)) {
+        v = v2;
+        i = i2;
+    }
+}
+
+// ---- per-element kernels of a chunk ---------------------------------------------------
+template <int DT>
+__device__ __forceinline__ void unpack8(const uint4* q, int k, float (&x)[8]);
+
+template <>
+__device__ __forceinline__ void unpack8<DSPARK_BF16>(const uint4* q, int k, float (&x)[8])
+{
+    const uint4 u = q[k];
+    x[0] = bf16_lo(u.x); x[1] = bf16_hi(u.x);
+    x[2] = bf16_lo(u.y); x[3] = bf16_hi(u.y);
+    x[4] = bf16_lo(u.z); x[5] = bf16_hi(u.z);
+    x[6] = bf16_lo(u.w); x[7] = bf16_hi(u.w);
+}
+
+template <>
+__device__ __forceinline__ void unpack8<DSPARK_F32>(const uint4* q, int k, float (&x)[8])
+{
+    const uint4 a = q[2 * k], b = q[2 * k + 1];
+    x[0] = __uint_as_float(a.x); x[1] = __uint_as_float(a.y);
+    x[2] = __uint_as_float(a.z); x[3] = __uint_as_float(a.w);
+    x[4] = __uint_as_float(b.x); x[5] = __uint_as_float(b.y);
+    x[6] = __uint_as_float(b.z); x[7] = __uint_as_float(b.w);
+}
+
+// One chunk of one row: lane partial over [v0, v1). Elements are visited by each lane in
+// increasing index order, so a strict '>' keeps the lowest index of the lane's maximum.
+template <int DT, bool STOCH>
+__device__ __forceinline__ void chunk_lane(const char* row, int v0, int v1, int vec, float s,
+                                           int lane, float& a, float& b, int& idx)
+{
+    constexpr int E = (DT == DSPARK_BF16) ? 2 : 4;
+    constexpr int Q = (DT == DSPARK_BF16) ? 1 : 2;   // uint4 per 8 elements
+    if (vec) {
+        const char* base = row + static_cast<int64_t>(v0) * E;
+        const int n8 = (v1 - v0) >> 3;               // groups of 8 elements
+        for (int g0 = lane; g0 < n8; g0 += 32 * kUnroll) {
+            uint4 buf[kUnroll * Q];
+#pragma unroll
+            for (int k = 0; k < kUnroll; ++k) {
+                const int g = g0 + k * 32;
+                if (g < n8) {
+#pragma unroll
+                    for (int h = 0; h < Q; ++h)
+                        buf[k * Q + h] = ld_stream16(base + (static_cast<int64_t>(g) * Q + h) * 16);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kUnroll; ++k) {
+                const int g = g0 + k * 32;
+                if (g < n8) {
+                    float x[8];
+                    unpack8<DT>(buf, k, x);
+                    const int vb = v0 + g * 8;
+                    if (!STOCH) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            if (x[e] > a) { a = x[e]; idx = vb + e; }
+                    } else {
+                        float vm = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])),
+                                         fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
+                        if (vm > a) {
+                            b *= ex2_approx((a - vm) * s);
+                            a = vm;
+                        }
+                        if (a != -INFINITY) {
+                            float t[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) t[e] = ex2_approx((x[e] - a) * s);
+                            b += ((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7]));
+                        }
+                    }
+                }
+            }
+        }
+    } else {
+        for (int v = v0 + lane; v < v1; v += 32) {
+            const float x = load_logit<DT>(row, v);
+            if (!STOCH) {
+                if (x > a) { a = x; idx = v; }
+            } else {
+                if (x > a) {
+                    b *= ex2_approx((a - x) * s);
+                    a = x;
+                }
+                if (a != -INFINITY) b += ex2_approx((x - a) * s);
+            }
+        }
+    }
+}
+
+template <int DT, bool STOCH>
+__global__ void __launch_bounds__(kStreamThreads)
+verify_stream_kernel(StreamArgs A)
+{
+    constexpr int E = (DT == DSPARK_BF16) ? 2 : 4;
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = static_cast<int64_t>(blockIdx.x) * kStreamWarps + (threadIdx.x >> 5);
+    const int64_t GW = static_cast<int64_t>(gridDim.x) * kStreamWarps;
+    const int L = A.gamma - 1;
+
+    const int64_t n_t = target_row_count(A.mode, A.cu, A.B, A.gamma, A.target_rows, A.rows_max);
+    int64_t n_d = 0;
+    if (STOCH) n_d = (A.mode == DSPARK_COMPACT) ? n_t : static_cast<int64_t>(A.B) * L;
+    const int64_t U = (n_t + n_d) * A.nc;
+    const int64_t u0 = gw * U / GW, u1 = (gw + 1) * U / GW;
+
+    for (int64_t u = u0; u < u1; ++u) {
+        const int64_t job = u / A.nc;
+        const int c = static_cast<int>(u - job * A.nc);
+        const char* row;
+        int64_t slot;   // partial index = (paired target row) * nc + c
+        if (job < n_t) {
+            row = static_cast<const char*>(A.target) + job * A.V * E;
+            slot = job * A.nc + c;
+        } else {
+            const int64_t k = job - n_t;
+            int b, i;
+            int64_t r;
+            if (A.mode == DSPARK_COMPACT) {
+                r = k;                                   // draft job of packed row r
+                int lo = 0, hi = A.B;                    // largest b with cu[b] <= r
+                while (hi - lo > 1) {
+                    const int mid = (lo + hi) >> 1;
+                    if (A.cu[mid] <= r) lo = mid; else hi = mid;
+                }
+                b = lo;
+                i = static_cast<int>(r - A.cu[b]);
+                int w = A.windows[b];
+                w = w < 1 ? 1 : (w > A.gamma ? A.gamma : w);
+                if (i < 0 || i >= w - 1 || i >= L) continue;   // last row of a request: no draft
+            } else {
+                b = static_cast<int>(k / L);
+                i = static_cast<int>(k - static_cast<int64_t>(b) * L);
+                r = static_cast<int64_t>(b) * A.gamma + i;
+            }
+            row = static_cast<const char*>(A.draft) + (static_cast<int64_t>(b) * L + i) * A.V * E;
+            slot = r * A.nc + c;
+        }
+        const int v0 = c * A.C;
+        const int v1 = min(A.V, v0 + A.C);
+        float a = -INFINITY, bsum = 0.0f;
+        int idx = 0x7FFFFFFF;
+        chunk_lane<DT, STOCH>(row, v0, v1, A.vec, A.s, lane, a, bsum, idx);
+        if (!STOCH) {
+            for (int off = 16; off > 0; off >>= 1) {
+                const float v2 = __shfl_xor_sync(0xffffffffu, a, off);
+                const int i2 = __shfl_xor_sync(0xffffffffu, idx, off);
+                arg_merge(a, idx, v2, i2);
+            }
+            if (lane == 0) {
+                ArgPart p;
+                p.v = a;
+                p.idx = idx;
+                static_cast<ArgPart*>(A.part_t)[slot] = p;
+            }
+        } else {
+            float m = a;
+            for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+            double z = 0.0;
+            if (a != -INFINITY) z = static_cast<double>(bsum) * static_cast<double>(ex2_approx((a - m) * A.s));
+            for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+            if (lane == 0) {
+                SoftPart p;
+                p.m = m;
+                p.pad = 0.0f;
+                p.z = z;
+                SoftPart* dst = static_cast<SoftPart*>(job < n_t ? A.part_t : A.part_d);
+                dst[slot] = p;
+            }
+        }
+    }
+}
+
+// ---- Philox4x64-10 (Salmon, Moraes, Dror, Shaw, SC'11), device side ---------------------
+__device__ __forceinline__ void philox4x64_10(uint64_t c0, uint64_t c1, uint64_t c2, uint64_t c3,
+                                              uint64_t k0, uint64_t k1, uint64_t out[4])
+{
+    const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+    const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint64_t hi0 = __umul64hi(M0, c0), lo0 = M0 * c0;
+        const uint64_t hi1 = __umul64hi(M1, c2), lo1 = M1 * c2;
+        const uint64_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
+        k0 += W0; k1 += W1;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+struct FinalArgs {
+    const void* target;
+    const void* draft;
+    const int32_t* cu;
+    const int32_t* windows;
+    const int32_t* tokens;
+    const void* part_t;
+    const void* part_d;
+    int32_t* accept_len;
+    int32_t* committed;
+    int32_t* ceiling;
+    float* row_prob;
+    int32_t* status;
+    uint64_t seed, step;
+    int mode, V, nc, vec, B, gamma, target_rows;
+    int64_t rows_max;
+    float s;        // log2(e) / temperature
+    double inv_t;   // 1 / temperature
+    double temp;    // temperature
+};
+
+// Eight consecutive logits [v0, v0+8) of a row as fp32; positions >= V read as -inf.
+template <int DT>
+__device__ __forceinline__ void load8(const char* row, int v0, int V, int vec, float (&x)[8])
+{
+    if (vec && v0 + 8 <= V) {
+        const uint4* q = reinterpret_cast<const uint4*>(row + static_cast<int64_t>(v0) * (DT == DSPARK_BF16 ? 2 : 4));
+        if (DT == DSPARK_BF16) {
+            const uint4 u = __ldg(q);
+            x[0] = bf16_lo(u.x); x[1] = bf16_hi(u.x); x[2] = bf16_lo(u.y); x[3] = bf16_hi(u.y);
+            x[4] = bf16_lo(u.z); x[5] = bf16_hi(u.z); x[6] = bf16_lo(u.w); x[7] = bf16_hi(u.w);
+        } else {
+            const uint4 a = __ldg(q), b = __ldg(q + 1);
+            x[0] = __uint_as_float(a.x); x[1] = __uint_as_float(a.y);
+            x[2] = __uint_as_float(a.z); x[3] = __uint_as_float(a.w);
+            x[4] = __uint_as_float(b.x); x[5] = __uint_as_float(b.y);
+            x[6] = __uint_as_float(b.z); x[7] = __uint_as_float(b.w);
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = (v0 + e < V) ? load_logit<DT>(row, v0 + e) : -INFINITY;
+    }
+}
+
+// Bonus weights of 8 consecutive tokens: p_v (residual == 0) or max(0, p_v - q_v).
+template <int DT>
+__device__ __forceinline__ void bonus_weights(const char* trow, const char* drow, int v0, int V,
+                                              int vec, bool residual, float mp, float izp,
+                                              float mq, float izq, float s, float (&w)[8])
+{
+    float xp[8];
+    load8<DT>(trow, v0, V, vec, xp);
+    if (residual) {
+        float xq[8];
+        load8<DT>(drow, v0, V, vec, xq);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float p = (v0 + e < V) ? ex2_approx((xp[e] - mp) * s) * izp : 0.0f;
+            const float q = (v0 + e < V) ? ex2_approx((xq[e] - mq) * s) * izq : 0.0f;
+            w[e] = fmaxf(p - q, 0.0f);
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            w[e] = (v0 + e < V) ? ex2_approx((xp[e] - mp) * s) * izp : 0.0f;
+    }
+}
+
+__device__ __forceinline__ float sum8(const float (&w)[8])
+{
+    return ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
+}
+
+// Combined softmax statistics of one row from its nc chunk partials, by one warp, in a fixed
+// order (lane-strided, then a fixed shuffle tree): deterministic for a given nc.
+__device__ __forceinline__ void combine_soft(const SoftPart* parts, int nc, float s, int lane,
+                                             float& m_out, double& z_out)
+{
+    float m = -INFINITY;
+    for (int c = lane; c < nc; c += 32) m = fmaxf(m, parts[c].m);
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    double z = 0.0;
+    if (m != -INFINITY) {
+        for (int c = lane; c < nc; c += 32) {
+            const SoftPart p = parts[c];
+            if (p.m != -INFINITY) z += p.z * exp2(static_cast<double>(p.m - m) * static_cast<double>(s));
+        }
+    }
+    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+    m_out = m;
+    z_out = z;
+}
+
+template <int DT, bool STOCH>
+__global__ void __launch_bounds__(kFinalThreads)
+verify_finalize_kernel(FinalArgs A)
+{
+    constexpr int E = (DT == DSPARK_BF16) ? 2 : 4;
+    extern __shared__ double tile_sum[];      // stochastic bonus: one entry per 256-token tile
+    __shared__ int g_s[DSPARK_MAX_GAMMA];
+    __shared__ float mp_s[DSPARK_MAX_GAMMA], mq_s[DSPARK_MAX_GAMMA];
+    __shared__ double zp_s[DSPARK_MAX_GAMMA], zq_s[DSPARK_MAX_GAMMA];
+    __shared__ double ub_s[DSPARK_MAX_GAMMA];
+    __shared__ int acc_s[DSPARK_MAX_GAMMA];
+    __shared__ int walk_s[4];                 // Lc, Lf (then: done marker), pos, rejected
+
+    const int b = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int gamma = A.gamma;
+    const int L = gamma - 1;
+    int bits = 0;
+
+    int w = gamma;
+    if (A.mode != DSPARK_STATIC) {
+        w = A.windows[b];
+        if (w < 1 || w > gamma) {
+            if (tid == 0) bits |= DSPARK_STATUS_BAD_WINDOW;
+            w = w < 1 ? 1 : gamma;
+        }
+    }
+    const int nrows = (A.mode == DSPARK_COMPACT) ? w : gamma;
+    const int64_t base = (A.mode == DSPARK_COMPACT) ? static_cast<int64_t>(A.cu[b])
+                                                    : static_cast<int64_t>(b) * gamma;
+    const int64_t n_t = target_row_count(A.mode, A.cu, A.B, gamma, A.target_rows, A.rows_max);
+    int32_t* out = A.committed + static_cast<int64_t>(b) * gamma;
+
+    if (base < 0 || base + nrows > n_t) {
+        for (int k = tid; k < gamma; k += kFinalThreads) out[k] = -1;
+        if (tid == 0) {
+            A.accept_len[b] = 0;
+            if (A.ceiling) A.ceiling[b] = (A.mode == DSPARK_COMPACT) ? -1 : 0;
+            raise_status(A.status, bits | DSPARK_STATUS_BAD_ROWS);
+        }
+        return;
+    }
+    const int ndec = nrows - 1;   // accept tests this mode runs
+
+    // 1. per-row statistics from the chunk partials; one warp per row
+    for (int i = warp; i < nrows; i += kFinalWarps) {
+        const int64_t r = base + i;
+        if (!STOCH) {
+            const ArgPart* parts = static_cast<const ArgPart*>(A.part_t) + r * A.nc;
+            float v = -INFINITY;
+            int idx = 0x7FFFFFFF;
+            for (int c = lane; c < A.nc; c += 32) {
+                const ArgPart p = parts[c];
+                arg_merge(v, idx, p.v, p.idx);
+            }
+            for (int off = 16; off > 0; off >>= 1) {
+                const float v2 = __shfl_xor_sync(0xffffffffu, v, off);
+                const int i2 = __shfl_xor_sync(0xffffffffu, idx, off);
+                arg_merge(v, idx, v2, i2);
+            }
+            if (lane == 0) g_s[i] = idx;
+        } else {
+            float m;
+            double z;
+            combine_soft(static_cast<const SoftPart*>(A.part_t) + r * A.nc, A.nc, A.s, lane, m, z);
+            if (lane == 0) { mp_s[i] = m; zp_s[i] = z; }
+            if (i < ndec) {
+                combine_soft(static_cast<const SoftPart*>(A.part_d) + r * A.nc, A.nc, A.s, lane, m, z);
+                if (lane == 0) { mq_s[i] = m; zq_s[i] = z; }
+            }
+        }
+    }
+    __syncthreads();
+
+    // 2. accept tests, one thread per tested position
+    if (tid < nrows) {
+        const int i = tid;
+        int accepted = 0;
+        const bool tested = i < ndec;
+        const int d = tested ? A.tokens[static_cast<int64_t>(b) * gamma + i + 1] : -1;
+        const bool valid = d >= 0 && d < A.V;
+        if (tested && !valid) bits |= DSPARK_STATUS_BAD_TOKEN;
+        if (!STOCH) {
+            if (tested && valid) accepted = (d == g_s[i]);
+            if (A.row_prob) {
+                A.row_prob[(base + i) * 2] = -1.0f;
+                A.row_prob[(base + i) * 2 + 1] = -1.0f;
+            }
+        } else {
+            uint64_t rnd[4];
+            philox4x64_10(static_cast<uint64_t>(b), static_cast<uint64_t>(i), A.step, 0ull, A.seed, 0ull, rnd);
+            ub_s[i] = static_cast<double>(rnd[1] >> 11) * 0x1p-53;
+            float pp = -1.0f, qq = -1.0f;
+            if (tested && valid) {
+                const char* trow = static_cast<const char*>(A.target) + (base + i) * A.V * E;
+                const char* drow = static_cast<const char*>(A.draft) + (static_cast<int64_t>(b) * L + i) * A.V * E;
+                const double lp = load_logit<DT>(trow, d);
+                const double lq = load_logit<DT>(drow, d);
+                const double p = exp((lp - static_cast<double>(mp_s[i])) / A.temp) / zp_s[i];
+                const double q = exp((lq - static_cast<double>(mq_s[i])) / A.temp) / zq_s[i];
+                const float u = static_cast<float>(rnd[0] >> 40) * 0x1p-24f;
+                if (q == 0.0) accepted = 1;
+                else accepted = u < static_cast<float>(p / q);
+                pp = static_cast<float>(p);
+                qq = static_cast<float>(q);
+            }
+            if (A.row_prob) {
+                A.row_prob[(base + i) * 2] = pp;
+                A.row_prob[(base + i) * 2 + 1] = qq;
+            }
+        }
+        acc_s[i] = tested ? accepted : 0;
+    }
+    __syncthreads();
+
+    // 3. walks: committed window (identical in compact and cap-accept) and the full block
+    if (tid == 0) {
+        int Lc = 1;
+        while (Lc - 1 < w - 1 && acc_s[Lc - 1]) ++Lc;
+        int Lf = 1;
+        while (Lf - 1 < ndec && acc_s[Lf - 1]) ++Lf;
+        walk_s[0] = Lc;
+        walk_s[1] = Lf;
+        walk_s[2] = Lc - 1;
+        walk_s[3] = (Lc - 1 < w - 1) ? 1 : 0;
+        A.accept_len[b] = Lc;
+        if (A.ceiling) A.ceiling[b] = (A.mode == DSPARK_COMPACT) ? -1 : Lf;
+    }
+    __syncthreads();
+    const int Lc = walk_s[0];
+    if (!STOCH) {
+        for (int k = tid; k < gamma; k += kFinalThreads) out[k] = (k < Lc) ? g_s[k] : -1;
+    } else {
+        for (int k = tid; k < gamma; k += kFinalThreads)
+            out[k] = (k < Lc - 1) ? A.tokens[static_cast<int64_t>(b) * gamma + k + 1] : -1;
+
+        // 4. bonus: inverse CDF over the residual of row pos (after a rejection) or over p of
+        //    row pos (after full acceptance); 256-token tiles, one warp per tile. A residual
+        //    that sums to zero (only rounding can do that) falls back to p.
+        const int pos = walk_s[2];
+        const char* trow = static_cast<const char*>(A.target) + (base + pos) * A.V * E;
+        const char* drow = static_cast<const char*>(A.draft) + (static_cast<int64_t>(b) * L + pos) * A.V * E;
+        const float mp = mp_s[pos];
+        const float izp = static_cast<float>(1.0 / zp_s[pos]);
+        const int n_tiles = (A.V + 255) / 256;
+        for (int attempt = 0; attempt < 2; ++attempt) {
+            const bool residual = walk_s[3] != 0 && attempt == 0;
+            const float mq = residual ? mq_s[pos] : 0.0f;
+            const float izq = residual ? static_cast<float>(1.0 / zq_s[pos]) : 0.0f;
+            for (int t = warp; t < n_tiles; t += kFinalWarps) {
+                float wv[8];
+                bonus_weights<DT>(trow, drow, t * 256 + lane * 8, A.V, A.vec, residual, mp, izp,
+                                  mq, izq, A.s, wv);
+                double ts = static_cast<double>(sum8(wv));
+                for (int off = 16; off > 0; off >>= 1) ts += __shfl_xor_sync(0xffffffffu, ts, off);
+                if (lane == 0) tile_sum[t] = ts;
+            }
+            __syncthreads();
+            if (warp == 0) {
+                // lane-contiguous groups of tiles, inclusive scan over lanes
+                const int per = (n_tiles + 31) / 32;
+                const int t0 = lane * per;
+                const int t1 = min(t0 + per, n_tiles);
+                double own = 0.0;
+                for (int t = t0; t < t1; ++t) own += tile_sum[t];
+                double incl = own;
+                for (int off = 1; off < 32; off <<= 1) {
+                    const double v = __shfl_up_sync(0xffffffffu, incl, off);
+                    if (lane >= off) incl += v;
+                }
+                const double R = __shfl_sync(0xffffffffu, incl, 31);
+                if (residual && !(R > 0.0)) {
+                    if (lane == 0) walk_s[3] = 0;       // retry with p
+                } else {
+                    const double thr = ub_s[pos] * R;
+                    const unsigned hit = __ballot_sync(0xffffffffu, incl > thr);
+                    int tile;
+                    double before;
+                    if (hit) {
+                        const int src = __ffs(hit) - 1;
+                        tile = -1;
+                        before = 0.0;
+                        if (lane == src) {
+                            double cum = incl - own;
+                            for (int t = t0; t < t1; ++t) {
+                                if (cum + tile_sum[t] > thr) { tile = t; break; }
+                                cum += tile_sum[t];
+                            }
+                            if (tile < 0) { tile = t1 - 1; cum -= tile_sum[tile]; }
+                            before = cum;
+                        }
+                        tile = __shfl_sync(0xffffffffu, tile, src);
+                        before = __shfl_sync(0xffffffffu, before, src);
+                    } else {
+                        tile = n_tiles - 1;          // rounding left no crossing
+                        before = R - tile_sum[tile];
+                    }
+                    // inside the tile: lane sums, inclusive scan, then the lane's 8 tokens
+                    float wv[8];
+                    bonus_weights<DT>(trow, drow, tile * 256 + lane * 8, A.V, A.vec, residual, mp,
+                                      izp, mq, izq, A.s, wv);
+                    const double own8 = static_cast<double>(sum8(wv));
+                    double inc8 = own8;
+                    for (int off = 1; off < 32; off <<= 1) {
+                        const double v = __shfl_up_sync(0xffffffffu, inc8, off);
+                        if (lane >= off) inc8 += v;
+                    }
+                    const unsigned hit8 = __ballot_sync(0xffffffffu, before + inc8 > thr);
+                    int chosen = -1;
+                    if (hit8) {
+                        const int src = __ffs(hit8) - 1;
+                        if (lane == src) {
+                            double cum = before + inc8 - own8;
+                            for (int e = 0; e < 8; ++e) {
+                                cum += static_cast<double>(wv[e]);
+                                if (cum > thr) { chosen = tile * 256 + lane * 8 + e; break; }
+                            }
+                        }
+                        chosen = __shfl_sync(0xffffffffu, chosen, src);
+                    }
+                    if (chosen < 0) {
+                        // rounding fallback: the tile's last token with positive weight
+                        int cand = -1;
+                        for (int e = 7; e >= 0; --e)
+                            if (wv[e] > 0.0f) { cand = tile * 256 + lane * 8 + e; break; }
+                        for (int off = 16; off > 0; off >>= 1)
+                            cand = max(cand, __shfl_xor_sync(0xffffffffu, cand, off));
+                        chosen = cand >= 0 ? cand : min(tile * 256, A.V - 1);
+                    }
+                    if (lane == 0) {
+                        out[Lc - 1] = chosen;
+                        walk_s[3] = 0;
+                        walk_s[1] = -1;                 // done marker
+                    }
+                }
+            }
+            __syncthreads();
+            if (walk_s[1] == -1) break;
+        }
+    }
+    // status bits of the CTA
+    const unsigned any = __ballot_sync(0xffffffffu, bits != 0);
+    if (any) {
+        int all = bits;
+        for (int off = 16; off > 0; off >>= 1) all |= __shfl_xor_sync(0xffffffffu, all, off);
+        if (lane == 0) raise_status(A.status, all);
+    }
+}
+
+template <int DT, bool STOCH>
+int run_verify(const VerifyCall& c, const Plan& plan, void* part_t, void* part_d,
+               cudaStream_t stream)
+{
+    DeviceInfo dev;
+    int rc = current_device(&dev);
+    if (rc != DSPARK_OK) return rc;
+    static thread_local int occ_device = -1;
+    static thread_local int occ = 0;
+    if (occ_device != dev.device) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, verify_stream_kernel<DT, STOCH>,
+                                                          kStreamThreads, 0) != cudaSuccess)
+            return check_launch("verify (occupancy query)");
+        if (occ < 1) occ = 1;
+        occ_device = dev.device;
+    }
+    const int L = c.gamma - 1;
+    const double inv_t = STOCH ? 1.0 / static_cast<double>(c.temperature) : 1.0;
+    const float s = static_cast<float>(1.4426950408889634 * inv_t);
+
+    StreamArgs sa;
+    sa.target = c.target;
+    sa.draft = c.draft;
+    sa.cu = c.cu;
+    sa.windows = c.windows;
+    sa.part_t = part_t;
+    sa.part_d = part_d;
+    sa.status = c.status;
+    sa.mode = c.mode;
+    sa.V = c.V;
+    sa.nc = plan.nc;
+    sa.C = plan.C;
+    const size_t esz = (DT == DSPARK_BF16) ? 2 : 4;
+    // vector path: whole 8-element groups (V % 8 == 0) starting on 16-byte boundaries
+    bool vec = c.V % 8 == 0 && (static_cast<size_t>(c.V) * esz) % 16 == 0 &&
+               reinterpret_cast<uintptr_t>(c.target) % 16 == 0;
+    if (STOCH) vec = vec && reinterpret_cast<uintptr_t>(c.draft) % 16 == 0;
+    sa.vec = vec ? 1 : 0;
+    sa.B = c.B;
+    sa.gamma = c.gamma;
+    sa.target_rows = c.target_rows;
+    sa.rows_max = plan.rows_max;
+    sa.s = s;
+
+    const int64_t max_units = (plan.rows_max + (STOCH ? static_cast<int64_t>(c.B) * L : 0)) * plan.nc;
+    int64_t grid = static_cast<int64_t>(dev.sm_count) * occ;
+    const int64_t need = ceil_div(max_units, kStreamWarps);
+    if (grid > need) grid = need;
+    if (grid < 1) grid = 1;
+    verify_stream_kernel<DT, STOCH><<<static_cast<unsigned>(grid), kStreamThreads, 0, stream>>>(sa);
+    rc = check_launch("verify (stream)");
+    if (rc != DSPARK_OK) return rc;
+
+    FinalArgs fa;
+    fa.target = c.target;
+    fa.draft = c.draft;
+    fa.cu = c.cu;
+    fa.windows = c.windows;
+    fa.tokens = c.tokens;
+    fa.part_t = part_t;
+    fa.part_d = part_d;
+    fa.accept_len = c.accept_len;
+    fa.committed = c.committed;
+    fa.ceiling = c.ceiling;
+    fa.row_prob = c.row_prob;
+    fa.status = c.status;
+    fa.seed = c.seed;
+    fa.step = c.step;
+    fa.mode = c.mode;
+    fa.V = c.V;
+    fa.nc = plan.nc;
+    fa.vec = sa.vec;
+    fa.B = c.B;
+    fa.gamma = c.gamma;
+    fa.target_rows = c.target_rows;
+    fa.rows_max = plan.rows_max;
+    fa.s = s;
+    fa.inv_t = inv_t;
+    fa.temp = static_cast<double>(c.temperature);
+    const size_t smem = STOCH ? sizeof(double) * static_cast<size_t>((c.V + 255) / 256) : 0;
+    verify_finalize_kernel<DT, STOCH><<<c.B, kFinalThreads, smem, stream>>>(fa);
+    return check_launch("verify (finalize)");
+}
+
+}  // namespace
+
+size_t verify_workspace_bytes(int B, int gamma, int V, int stochastic)
+{
+    if (B <= 0) return 0;
+    const Plan plan = make_plan(V, B, gamma);
+    const size_t per = stochastic ? sizeof(SoftPart) : sizeof(ArgPart);
+    const size_t one = align_up(static_cast<size_t>(plan.rows_max) * plan.nc * per, 256);
+    return stochastic ? 2 * one : one;
+}
+
+int launch_verify(const VerifyCall& c, cudaStream_t stream)
+{
+    if (c.stochastic && c.V > kMaxVocabStochastic)
+        return fail(DSPARK_ERR_UNSUPPORTED, "dspark_verify: stochastic verify supports V <= %d, got %d",
+                    kMaxVocabStochastic, c.V);
+    const Plan plan = make_plan(c.V, c.B, c.gamma);
+    const size_t need = verify_workspace_bytes(c.B, c.gamma, c.V, c.stochastic);
+    if (c.ws_bytes < need)
+        return fail(DSPARK_ERR_INVALID_ARG, "dspark_verify: workspace of %zu bytes, %zu needed",
+                    c.ws_bytes, need);
+    if (need > 0 && (c.ws == nullptr || reinterpret_cast<uintptr_t>(c.ws) % 16 != 0))
+        return fail(DSPARK_ERR_INVALID_ARG, "dspark_verify: workspace must be a 16-byte aligned device pointer");
+    void* part_t = c.ws;
+    void* part_d = c.stochastic ? static_cast<char*>(c.ws) + need / 2 : nullptr;
+    if (c.dtype == DSPARK_BF16)
+        return c.stochastic ? run_verify<DSPARK_BF16, true>(c, plan, part_t, part_d, stream)
+                            : run_verify<DSPARK_BF16, false>(c, plan, part_t, part_d, stream);
+    return c.stochastic ? run_verify<DSPARK_F32, true>(c, plan, part_t, part_d, stream)
+                        : run_verify<DSPARK_F32, false>(c, plan, part_t, part_d, stream);
+}
+
+}  // namespace dspark

@@ -1,0 +1,77 @@
+"""A buffer-owning runner of one DSpark decode step: schedule -> pack -> verify -> scatter.
+
+All buffers are allocated once, on the device, at construction; `run` only enqueues the four
+library calls (five kernel launches) on the current stream and never synchronises, so it can
+be timed with CUDA events or captured into a CUDA graph.
+"""
+from __future__ import annotations
+
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import _binding as bd
+
+
+class DSparkStep:
+    LAUNCHES_PER_STEP = 5   # schedule, pack, verify (stream + finalize), scatter
+
+    def __init__(self, B: int, gamma: int, V: int, tiers: Sequence[int], bias: float,
+                 alpha, theta, *, mode: str = "compact", stochastic: bool = False,
+                 out_cap: int = 4096, device="cuda"):
+        self.B, self.gamma, self.V = B, gamma, V
+        self.mode = mode
+        self.stochastic = stochastic
+        self.device = torch.device(device)
+        dev = dict(device=self.device)
+        i32 = dict(dtype=torch.int32, **dev)
+        self.cost = bd.CostTable(bias, torch.as_tensor(np.asarray(alpha, np.float64), **dev),
+                                 torch.as_tensor(np.asarray(theta, np.float64), **dev))
+        self.tiers = torch.as_tensor(np.asarray(tiers, np.int32), **dev)
+        self.packed_cap = int(max(max(tiers), B * gamma))
+        self.windows = torch.zeros(B, **i32)
+        self.k_star = torch.zeros(1, **i32)
+        self.cu = torch.zeros(B + 1, **i32)
+        self.packed_ids = torch.zeros(self.packed_cap, **i32)
+        self.row_req = torch.zeros(self.packed_cap, **i32)
+        self.row_pos = torch.zeros(self.packed_cap, **i32)
+        self.meta = torch.zeros(2, **i32)
+        self.status = torch.zeros(1, **i32)
+        self.accept_len = torch.zeros(B, **i32)
+        self.committed = torch.zeros(B, gamma, **i32)
+        self.ceiling = torch.zeros(B, **i32)
+        ws = bd.dspark_verify_workspace_bytes(B, gamma, V, stochastic)
+        self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, **dev)
+        self.out_tokens = torch.full((B, out_cap), -1, **i32)
+        self.out_len = torch.zeros(B, **i32)
+
+    def schedule(self, conf: torch.Tensor):
+        bd.dspark_schedule(conf, self.cost, self.windows, self.k_star, self.status)
+
+    def pack(self, block_tokens: torch.Tensor):
+        bd.dspark_pack(self.windows, block_tokens, self.tiers, self.cu, self.packed_ids,
+                       self.meta, self.row_req, self.row_pos, self.status)
+
+    def verify(self, target: torch.Tensor, block_tokens: torch.Tensor,
+               draft: Optional[torch.Tensor] = None, *, temperature: float = 1.0, seed: int = 0,
+               step: int = 0, row_prob: Optional[torch.Tensor] = None):
+        bd.dspark_verify(self.mode, target, block_tokens, self.accept_len, self.committed,
+                         self.workspace, stochastic=self.stochastic, draft=draft,
+                         cu_seqlens=self.cu, windows=self.windows, ceiling_len=self.ceiling,
+                         row_prob=row_prob, temperature=temperature, seed=seed, step=step,
+                         status=self.status)
+
+    def scatter(self):
+        bd.dspark_scatter(self.committed, self.accept_len, self.out_tokens, self.out_len,
+                          self.status)
+
+    def run(self, conf, block_tokens, target, draft=None, *, temperature=1.0, seed=0, step=0,
+            row_prob=None):
+        """One whole step. `target` holds the rows this mode verifies: the packed [>=M, V]
+        rows of the scheduled windows (compact) or the full block [B*gamma, V]."""
+        self.schedule(conf)
+        self.pack(block_tokens)
+        self.verify(target, block_tokens, draft, temperature=temperature, seed=seed, step=step,
+                    row_prob=row_prob)
+        self.scatter()

@@ -178,9 +178,12 @@ def _gaussian_rows(rng, rows, V, sigma, spike, dtype, block_rows=256):
     return out
 
 
-def _first_argmax(rows: torch.Tensor) -> np.ndarray:
+def _first_argmax(rows: torch.Tensor, block_rows=256) -> np.ndarray:
     # first index among equal maxima, on the values the verify sees (after dtype rounding)
-    return torch.argmax(rows.float(), dim=-1).numpy().astype(np.int64)
+    out = np.empty(rows.shape[0], np.int64)
+    for r0 in range(0, rows.shape[0], block_rows):
+        out[r0:r0 + block_rows] = torch.argmax(rows[r0:r0 + block_rows].float(), dim=-1).numpy()
+    return out
 
 
 def _gumbel_sample(rng, logits: torch.Tensor, temperature: float, block_rows=256) -> np.ndarray:

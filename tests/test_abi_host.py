@@ -1,0 +1,72 @@
+"""The C ABI without a GPU: the library builds for sm_103a, loads, exports every entry point
+include/dspark.h declares, and rejects invalid arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_ragged_gb300 import build
+    build.build()
+    from speculative_decoding_ragged_gb300 import _binding
+    return _binding.lib()
+
+
+def header_functions():
+    with open(os.path.join(ROOT, "include", "dspark.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dspark_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = header_functions()
+    assert {"dspark_schedule", "dspark_pack", "dspark_verify", "dspark_scatter"} <= set(names)
+    for name in names:
+        assert hasattr(lib, name), name
+    from speculative_decoding_ragged_gb300 import _binding
+    assert set(names) == set(_binding.SYMBOLS)
+
+
+def test_version(lib):
+    assert lib.dspark_version() == 100
+
+
+def test_argument_errors_are_reported_on_the_host(lib):
+    from speculative_decoding_ragged_gb300 import _binding as bd
+    cost = bd._Cost(1.0, None, 0, None, 0)
+    rc = lib.dspark_schedule(None, -1, 4, ctypes.byref(cost), None, None, None, None)
+    assert rc == -1 and "B = -1" in bd.last_error()
+    rc = lib.dspark_schedule(None, 4, 40, ctypes.byref(cost), None, None, None, None)
+    assert rc == -1 and "gamma" in bd.last_error()
+    rc = lib.dspark_schedule(None, 8192, 4, ctypes.byref(cost), None, None, None, None)
+    assert rc == -2 and "B*(gamma-1)" in bd.last_error()     # 24576 candidates > 16384
+    rc = lib.dspark_pack(None, None, 2, 4, None, 0, None, None, None, None, 0, None, None, None)
+    assert rc == -1 and "n_tiers" in bd.last_error()
+    rc = lib.dspark_verify(7, 0, None, 0, None, 0, 16, None, None, None, 1, 2, 1.0, 0, 0,
+                           None, None, None, None, None, 0, None, None)
+    assert rc == -1 and "mode" in bd.last_error()
+    rc = lib.dspark_verify(1, 1, None, 0, None, 0, 16, None, None, None, 1, 2, 0.0, 0, 0,
+                           None, None, None, None, None, 0, None, None)
+    assert rc == -1 and "temperature" in bd.last_error()
+    rc = lib.dspark_verify(1, 0, None, 0, None, 0, 16, None, None, None, 1, 2, 1.0, 0, 0,
+                           None, None, None, None, None, 0, None, None)
+    assert rc == -1 and "required" in bd.last_error()
+    rc = lib.dspark_scatter(None, None, 3, 33, None, None, 4, None, None)
+    assert rc == -1
+
+
+def test_workspace_size_is_a_function_of_sizes(lib):
+    from speculative_decoding_ragged_gb300 import _binding as bd
+    assert bd.dspark_verify_workspace_bytes(0, 8, 1000, False) == 0
+    g = bd.dspark_verify_workspace_bytes(256, 8, 151936, False)
+    s = bd.dspark_verify_workspace_bytes(256, 8, 151936, True)
+    assert g > 0 and s == 4 * g          # two arrays of 16-byte partials vs one of 8-byte
+    assert g % 256 == 0
+    assert bd.dspark_verify_workspace_bytes(-1, 8, 10, False) == 0
+    assert "bad sizes" in bd.last_error()

@@ -1,0 +1,104 @@
+"""GPU parity of dspark_schedule and dspark_pack against the oracle: bit-exact windows, K*,
+status bits, cu_seqlens, tiers and packed rows, from tiny to the maximum sizes."""
+import numpy as np
+import pytest
+
+from speculative_decoding_ragged_gb300 import synth
+import oracle
+
+from gpu_util import device, gpu_pack, gpu_schedule
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return device()
+
+
+def tables(rng, B, gamma, kind):
+    M = np.arange(B * gamma + 1, dtype=np.float64)
+    alpha = rng.uniform(0, 0.1) * np.arange(B + 1, dtype=np.float64)
+    if kind == 0:
+        theta = rng.uniform(0, 0.05) * M
+    elif kind == 1:
+        theta = np.ceil(M / 64) * rng.uniform(0, 0.2)
+    else:
+        theta = rng.uniform(0, 1.0, size=M.size)
+    return float(rng.uniform(0.5, 3)), alpha, theta
+
+
+SIZES = [(1, 1), (1, 2), (4, 4), (3, 32), (7, 8), (100, 5), (256, 8), (512, 8), (1000, 17),
+         (2048, 9), (8192, 2), (8192, 3), (5, 1), (1023, 2), (1025, 3)]
+
+
+@pytest.mark.parametrize("B,gamma", SIZES)
+def test_schedule_parity_random(dev, B, gamma):
+    rng = np.random.default_rng(B * 100 + gamma)
+    for trial in range(4):
+        a = rng.uniform(0.1, 0.95, size=B)
+        conf = rng.beta(8 * a[:, None], 8 * (1 - a[:, None]), size=(B, gamma - 1))
+        if trial == 1:
+            conf = np.round(conf * 8) / 8          # many equal survivals: tie rule
+        if trial == 2:
+            conf[rng.uniform(size=conf.shape) < 0.05] = np.nan
+            conf[rng.uniform(size=conf.shape) < 0.05] = 1.5
+        conf = conf.astype(np.float32)
+        bias, alpha, theta = tables(rng, B, gamma, trial % 3)
+        g = gpu_schedule(dev, conf, bias, alpha, theta)
+        r = oracle.schedule(conf, bias, alpha, theta)
+        np.testing.assert_array_equal(g["windows"], r["windows"])
+        assert g["k_star"] == r["k_star"] and g["status"] == r["status"]
+
+
+@pytest.mark.parametrize("name", list(synth.WORKLOADS))
+def test_schedule_parity_workloads(dev, name):
+    wl = synth.WORKLOADS[name]
+    thetas = synth.HIGH_LOAD_THETAS if name == "high_load" else (wl.theta_slope,)
+    small = wl.with_(V=64)                      # the schedule never reads logits
+    for seed in range(3):
+        for th in thetas:
+            bt = synth.make_batch(small, seed=seed, theta_slope=th)
+            g = gpu_schedule(dev, bt.conf, bt.bias, bt.alpha, bt.theta)
+            r = oracle.schedule(bt.conf, bt.bias, bt.alpha, bt.theta)
+            np.testing.assert_array_equal(g["windows"], r["windows"])
+            assert g["k_star"] == r["k_star"] and g["status"] == r["status"] == 0
+
+
+def test_schedule_invalid_cost_and_empty(dev):
+    conf = np.full((3, 4), 0.5, np.float32)
+    g = gpu_schedule(dev, conf, 1.0, np.zeros(4), np.full(16, -5.0))
+    assert g["status"] == 0x10 and g["k_star"] == 0 and (g["windows"] == 1).all()
+    g = gpu_schedule(dev, np.zeros((0, 4), np.float32), 1.0, np.zeros(1), np.zeros(1))
+    assert g["k_star"] == 0
+    g = gpu_schedule(dev, np.zeros((6, 0), np.float32), 1.0, np.zeros(7), np.full(7, -1.0))
+    assert g["status"] == 0x10 and (g["windows"] == 1).all()
+
+
+@pytest.mark.parametrize("B,gamma", [(0, 4), (1, 1), (2, 6), (33, 8), (1025, 4), (8192, 8),
+                                     (300, 32)])
+def test_pack_parity(dev, B, gamma):
+    rng = np.random.default_rng(B + gamma)
+    for trial in range(4):
+        windows = rng.integers(1, gamma + 1, size=B)
+        if trial == 3 and B:
+            windows[rng.uniform(size=B) < 0.1] = gamma + 3      # clamped, flagged
+            windows[rng.uniform(size=B) < 0.1] = 0
+        tokens = rng.integers(0, 150000, size=(B, gamma))
+        tiers = rng.permutation(np.arange(1, B * gamma + 9))[:int(rng.integers(1, 20))]
+        if trial == 0:
+            tiers = np.arange(1, 64) * max(1, B * gamma // 32)
+        cap = [B * gamma + 8, int(tiers.max()) + 3, max(1, B * gamma // 2), 0][trial]
+        g = gpu_pack(dev, windows, tokens, tiers, cap)
+        r = oracle.pack(windows, tokens, tiers, cap)
+        for key in ("cu", "packed_ids", "row_req", "row_pos"):
+            np.testing.assert_array_equal(g[key], r[key], err_msg=key)
+        assert (g["M"], g["tier"], g["status"]) == (r["M"], r["tier"], r["status"])
+
+
+def test_pack_page_example(dev):
+    tokens = np.array([[10, 11, 12, 13, 14, 15], [20, 21, 22, 23, 24, 25]])
+    g = gpu_pack(dev, np.array([2, 6]), tokens, np.array([16, 4, 8]), 16)
+    assert g["cu"].tolist() == [0, 2, 8] and g["M"] == 8 and g["tier"] == 8
+    assert g["packed_ids"][:8].tolist() == [10, 11, 20, 21, 22, 23, 24, 25]
+    assert (g["packed_ids"][8:] == -7).all()

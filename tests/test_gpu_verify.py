@@ -1,0 +1,159 @@
+"""GPU parity of dspark_verify against the oracle at sizes the oracle finishes in seconds:
+greedy bit-exact (argmax tokens, accept lengths, committed tokens, ceilings, status bits) in
+all three modes, both dtypes, vector and scalar paths (V % 8 != 0), ragged chunk tails, planted
+ties; stochastic decisions exact except at counted near-ties, p(d), q(d) within 1e-5 relative,
+and compact == cap-accept bit for bit on the device."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_decoding_ragged_gb300 import synth
+
+from gpu_util import (assert_greedy_equal, compare_stochastic, device, gpu_verify, ref_verify)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return device()
+
+
+def scheduled(bt):
+    s = oracle.schedule(bt.conf, bt.bias, bt.alpha, bt.theta)
+    w = s["windows"]
+    p = oracle.pack(w, bt.tokens, bt.tiers, int(max(int(bt.tiers.max()), bt.B * bt.gamma)))
+    return w, p["cu"]
+
+
+GREEDY_CASES = [
+    # B, gamma, V, dtype, sigma
+    (4, 4, 1024, "f32", 3.0),
+    (6, 5, 1001, "bf16", 2.0),      # V % 8 != 0: scalar path
+    (6, 5, 1004, "f32", 2.0),       # fp32 with V % 8 == 4: scalar path
+    (9, 8, 4104, "bf16", 0.05),     # heavy bf16 ties
+    (17, 6, 32000, "bf16", 2.0),
+    (3, 32, 777, "bf16", 2.0),
+    (1, 1, 64, "bf16", 1.0),        # no drafts at all
+    (40, 3, 129280, "bf16", 2.0),
+]
+
+
+@pytest.mark.parametrize("B,gamma,V,dtype,sigma", GREEDY_CASES)
+def test_greedy_parity_all_modes(dev, B, gamma, V, dtype, sigma):
+    wl = synth.custom(B=B, gamma=gamma, V=V, dtype=dtype, sigma=sigma, spike=6.0,
+                      accept=np.linspace(0.95, 0.2, B), tiers=(8, 64, 4096))
+    bt = synth.make_batch(wl, seed=B + V)
+    w, cu = scheduled(bt)
+    packed = synth.gather_packed(bt.target, B, gamma, w)
+    for mode, tgt, kw in [("compact", packed, dict(cu=cu, windows=w)),
+                          ("cap_accept", bt.target, dict(windows=w)),
+                          ("static", bt.target, {})]:
+        g = gpu_verify(dev, mode, tgt, bt.tokens, **kw)
+        r = ref_verify(mode, tgt, bt.tokens, **kw)
+        assert_greedy_equal(g, r)
+        assert (g["row_prob"][: tgt.shape[0]] == -1).all() or mode == "compact"
+    gc = gpu_verify(dev, "compact", packed, bt.tokens, cu=cu, windows=w)
+    ga = gpu_verify(dev, "cap_accept", bt.target, bt.tokens, windows=w)
+    np.testing.assert_array_equal(gc["committed"], ga["committed"])
+    assert (ga["ceiling_len"] >= ga["accept_len"]).all() and (gc["accept_len"] <= w).all()
+
+
+def test_greedy_planted_ties_lowest_index(dev):
+    B, gamma, V = 3, 4, 5000
+    x = torch.zeros((B * gamma, V), dtype=torch.bfloat16)
+    rng = np.random.default_rng(0)
+    for r in range(B * gamma):
+        ids = np.sort(rng.choice(V, size=3, replace=False))
+        x[r, ids] = 7.0
+    tokens = np.zeros((B, gamma), np.int32)
+    g = gpu_verify(dev, "static", x, tokens)
+    r = ref_verify("static", x, tokens)
+    assert_greedy_equal(g, r)
+
+
+def test_greedy_flags(dev):
+    x = torch.zeros((6, 16), dtype=torch.float32)
+    x[:, 3] = 1.0
+    tokens = np.array([[0, 3, 99, 3], [0, -1, 3, 3]], np.int32)
+    w = np.array([4, 9], np.int32)       # 9 is clamped to gamma = 4 (flagged)
+    g = gpu_verify(dev, "cap_accept", x, tokens, windows=w)
+    r = ref_verify("cap_accept", x, tokens, windows=w)
+    assert_greedy_equal(g, r)
+    assert g["status"] == 0x04 | 0x20 | 0x40
+
+
+def test_empty_batch(dev):
+    g = gpu_verify(dev, "static", torch.zeros((1, 8)), np.zeros((0, 4), np.int32))
+    assert g["accept_len"].size == 0
+
+
+STOCH_CASES = [
+    # B, gamma, V, dtype, T
+    (8, 5, 1000, "bf16", 1.0),
+    (8, 5, 1001, "bf16", 0.7),      # scalar path
+    (5, 4, 2048, "f32", 1.3),
+    (32, 8, 32000, "bf16", 1.0),    # the stochastic workload's shape
+    (2, 16, 129280, "bf16", 0.7),
+]
+
+
+@pytest.mark.parametrize("B,gamma,V,dtype,T", STOCH_CASES)
+def test_stochastic_parity(dev, B, gamma, V, dtype, T):
+    wl = synth.WORKLOADS["stochastic"].with_(B=B, gamma=gamma, V=V, dtype=dtype, temperature=T,
+                                             tiers=(4096,))
+    total_near = 0
+    for seed in range(2):
+        bt = synth.make_batch(wl, seed=seed)
+        w, cu = scheduled(bt)
+        packed = synth.gather_packed(bt.target, B, gamma, w)
+        M = int(cu[-1])
+        for step in range(3):
+            kw = dict(stochastic=True, draft=bt.draft, temperature=T, seed=seed * 7 + 1, step=step)
+            gc = gpu_verify(dev, "compact", packed, bt.tokens, cu=cu, windows=w, **kw)
+            rc = ref_verify("compact", packed, bt.tokens, cu=cu, windows=w, **kw)
+            near, _ = compare_stochastic(gc, rc, M)
+            total_near += near
+            ga = gpu_verify(dev, "cap_accept", bt.target, bt.tokens, windows=w, **kw)
+            ra = ref_verify("cap_accept", bt.target, bt.tokens, windows=w, **kw)
+            near, _ = compare_stochastic(ga, ra, B * gamma)
+            total_near += near
+            # on the device, compact and cap-accept commit identical tokens, bit for bit
+            np.testing.assert_array_equal(gc["committed"], ga["committed"])
+            np.testing.assert_array_equal(gc["accept_len"], ga["accept_len"])
+            assert (ga["ceiling_len"] >= ga["accept_len"]).all()
+            gs = gpu_verify(dev, "static", bt.target, bt.tokens, **kw)
+            rs = ref_verify("static", bt.target, bt.tokens, **kw)
+            near, _ = compare_stochastic(gs, rs, B * gamma)
+            total_near += near
+    print(f"near-tie requests: {total_near}")
+    assert total_near <= max(1, B // 8)
+
+
+def test_stochastic_identical_draft_accepts_all(dev):
+    B, gamma, V = 16, 6, 3000
+    wl = synth.WORKLOADS["stochastic"].with_(B=B, gamma=gamma, V=V, draft_sigma=0.0)
+    bt = synth.make_batch(wl, seed=3)
+    g = gpu_verify(dev, "static", bt.target, bt.tokens, stochastic=True, draft=bt.draft, seed=5)
+    assert (g["accept_len"] == gamma).all()
+    np.testing.assert_array_equal(g["committed"][:, :gamma - 1], bt.tokens[:, 1:])
+
+
+def test_stochastic_first_token_law(dev):
+    """Chi-square on V = 16: the device's first emitted token follows p."""
+    stats = pytest.importorskip("scipy.stats")
+    V, N, gamma = 16, 200_000, 2
+    pl = np.log(np.linspace(1.0, 3.0, V)).astype(np.float32)
+    ql = np.log(np.linspace(3.0, 1.0, V) ** 2).astype(np.float32)
+    p = np.exp(pl - pl.max()); p /= p.sum()
+    q = np.exp(ql - ql.max()); q /= q.sum()
+    rng = np.random.default_rng(0)
+    target = torch.from_numpy(np.tile(pl, (N * gamma, 1)))
+    draft = torch.from_numpy(np.tile(ql, (N, 1)))
+    tokens = np.zeros((N, gamma), np.int32)
+    tokens[:, 1] = rng.choice(V, size=N, p=q)
+    g = gpu_verify(dev, "static", target, tokens, stochastic=True, draft=draft, seed=99)
+    counts = np.bincount(g["committed"][:, 0], minlength=V)
+    chi = ((counts - N * p) ** 2 / (N * p)).sum()
+    assert stats.chi2.sf(chi, V - 1) > 1e-3
