@@ -207,6 +207,36 @@ int dspark_scatter(const int32_t* committed, const int32_t* accept_len, int B, i
                    int32_t* out_tokens, int32_t* out_len, int out_cap, int32_t* status,
                    cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------------------
+ * dspark_verify_noalloc — the pages have no counterpart to this entry point; it exists for
+ * callers that cannot hand the library scratch memory. Some hosts give a kernel library only
+ * its input and output buffers (a plugin interface with no workspace argument), and some
+ * serving loops reserve nearly all device memory for the KV cache before decoding starts and
+ * must not call cudaMalloc in the middle of a step, where the allocation can fail or
+ * synchronise the device and stall the overlapped scheduler.
+ *
+ * Same arguments, outputs and results as dspark_verify, minus the workspace: the scratch is a
+ * static device array of DSPARK_NOALLOC_SCRATCH_BYTES inside this library, which every GPU
+ * that loads the library keeps until the process exits. The call allocates nothing.
+ *   - Sizes whose dspark_verify_workspace_bytes(B, gamma, V, stochastic) exceeds
+ *     DSPARK_NOALLOC_SCRATCH_BYTES are rejected with DSPARK_ERR_UNSUPPORTED and a message.
+ *   - The first call on each device looks up the array's device address (a one-time set-up,
+ *     with that device current); make that first call before any stream capture.
+ *   - Every call on a device shares the one array and leaves its contents behind. Nothing in
+ *     it needs to start at zero (each call rewrites what it reads), but calls that overlap on
+ *     the GPU — on different streams, or from different host threads — race on it: order
+ *     them on one stream or synchronise between them.
+ * ------------------------------------------------------------------------------------- */
+#define DSPARK_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)  /* 4 MiB per device */
+int dspark_verify_noalloc(dspark_mode mode, int stochastic,
+                          const void* target_logits, int target_rows, const void* draft_logits,
+                          dspark_dtype dtype, int V,
+                          const int32_t* cu_seqlens, const int32_t* windows,
+                          const int32_t* block_tokens, int B, int gamma, float temperature,
+                          uint64_t seed, uint64_t step, int32_t* accept_len, int32_t* committed,
+                          int32_t* ceiling_len, float* row_prob, int32_t* status,
+                          cudaStream_t stream);
+
 /* Message of the last failed call on this host thread ("" if none). Never NULL. */
 const char* dspark_last_error(void);
 

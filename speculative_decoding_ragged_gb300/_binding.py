@@ -59,6 +59,8 @@ SYMBOLS = {
                        _p, _p, _p, _p, _p, ctypes.c_size_t, _p, _p], _i),
     "dspark_verify_workspace_bytes": ([_i, _i, _i, _i], ctypes.c_size_t),
     "dspark_scatter": ([_p, _p, _i, _i, _p, _p, _i, _p, _p], _i),
+    "dspark_verify_noalloc": ([_i, _i, _p, _i, _p, _i, _i, _p, _p, _p, _i, _i, ctypes.c_float,
+                               _u64, _u64, _p, _p, _p, _p, _p, _p], _i),
     "dspark_last_error": ([], ctypes.c_char_p),
     "dspark_version": ([], _i),
 }
@@ -226,3 +228,42 @@ def dspark_scatter(committed: torch.Tensor, accept_len: torch.Tensor, out_tokens
         _ptr(out_len, "out_len", torch.int32, min_numel=B, required=B > 0), cap,
         _ptr(status, "status", torch.int32, min_numel=1, required=False), _stream(stream))
     _check("dspark_scatter", rc)
+
+
+NOALLOC_SCRATCH_BYTES = 4 << 20
+
+
+def dspark_verify_noalloc(mode, target: torch.Tensor, block_tokens: torch.Tensor,
+                          accept_len: torch.Tensor, committed: torch.Tensor, *,
+                          stochastic: bool = False, draft: Optional[torch.Tensor] = None,
+                          cu_seqlens: Optional[torch.Tensor] = None,
+                          windows: Optional[torch.Tensor] = None,
+                          ceiling_len: Optional[torch.Tensor] = None,
+                          row_prob: Optional[torch.Tensor] = None, temperature: float = 1.0,
+                          seed: int = 0, step: int = 0, status: Optional[torch.Tensor] = None,
+                          stream=None):
+    """dspark_verify without a workspace argument, for callers that cannot provide scratch
+    memory: the library keeps a static 4 MiB device array per GPU and uses that instead.
+    Calls that overlap on the GPU share the array; keep them ordered on one stream."""
+    mode = MODES[mode] if isinstance(mode, str) else int(mode)
+    B, gamma = block_tokens.shape
+    rows, V = target.shape
+    dt = _dtype_code(target)
+    if draft is not None:
+        if draft.dtype != target.dtype or draft.shape[-1] != V:
+            raise ValueError("draft logits must match the target's dtype and vocabulary")
+        if draft.numel() != B * (gamma - 1) * V:
+            raise ValueError(f"draft logits must hold B*(gamma-1) = {B * (gamma - 1)} rows")
+    rc = lib().dspark_verify_noalloc(
+        mode, int(bool(stochastic)), _ptr(target, "target"), rows,
+        _ptr(draft, "draft", required=False), dt, V,
+        _ptr(cu_seqlens, "cu_seqlens", torch.int32, min_numel=B + 1, required=False),
+        _ptr(windows, "windows", torch.int32, min_numel=B, required=False),
+        _ptr(block_tokens, "block_tokens", torch.int32), B, gamma, float(temperature),
+        int(seed) & (2**64 - 1), int(step) & (2**64 - 1),
+        _ptr(accept_len, "accept_len", torch.int32, min_numel=B),
+        _ptr(committed, "committed", torch.int32, min_numel=B * gamma),
+        _ptr(ceiling_len, "ceiling_len", torch.int32, min_numel=B, required=False),
+        _ptr(row_prob, "row_prob", torch.float32, min_numel=2 * rows, required=False),
+        _ptr(status, "status", torch.int32, min_numel=1, required=False), _stream(stream))
+    _check("dspark_verify_noalloc", rc)
