@@ -53,6 +53,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batches", type=int, default=N_BATCHES)
+    ap.add_argument("--latency-steps", type=int, default=10000)
     return ap.parse_args()
 
 
@@ -221,19 +222,20 @@ def run_native(args, rank, world, local):
     batches = make_inputs(wl, seeds, dev, st)
     stream = torch.cuda.current_stream()
     nb = len(batches)
+    calls = [st.prepare(b["conf"], b["tokens"], b["packed"]) for b in batches]
 
     def step(i, ev=None):
-        b = batches[i % nb]
+        sched, pack, verify, scatter = calls[i % nb]
         if ev is not None:
             ev[0].record(stream)
-        st.schedule(b["conf"])
-        st.pack(b["tokens"])
+        sched()
+        pack()
         if ev is not None:
             ev[1].record(stream)
-        st.verify(b["packed"], b["tokens"])
+        verify()
         if ev is not None:
             ev[2].record(stream)
-        st.scatter()
+        scatter()
 
     for i in range(args.warmup):
         step(i)
@@ -298,6 +300,8 @@ def run_native(args, rank, world, local):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
     e2e_rows = sum_over_ranks(e2e_rows, world)
 
+    latency = latency_leg(dev, args.latency_steps) if args.latency_steps > 0 else None
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(batches, wl, args.cpu_seconds)
@@ -329,7 +333,60 @@ def run_native(args, rank, world, local):
                 "steps": E},
         "gpu_launches": K * st.LAUNCHES_PER_STEP,
         "clocks": clk,
+        "latency_b1": latency,
     }
+
+
+def latency_leg(dev, steps, pool=64):
+    """Per-step time of the batch-1 workload (B=1, gamma=16, V=129280 bf16, greedy compact):
+    `steps` consecutive steps cycling through `pool` seeded inputs (4 MB of logits each, the
+    pool larger than L2), launched eagerly (five kernels per step) and as one CUDA graph
+    replay per step."""
+    from speculative_decoding_ragged_gb300 import synth
+    from speculative_decoding_ragged_gb300.step import DSparkGraph, DSparkStep
+    wl = synth.WORKLOADS["latency_b1"]
+    st = DSparkStep(wl.B, wl.gamma, wl.V, wl.tiers, wl.bias, wl.alpha_slope * np.arange(2),
+                    wl.theta_slope * np.arange(wl.gamma + 1), out_cap=16, device=dev)
+    entries = []
+    for k in range(pool):
+        target, _ = synth.make_logits(wl.with_(draft_sigma=None), seed=0, pool_index=k)
+        bt = synth.make_batch(wl, seed=0, step=k, logits=(target, None))
+        # B = 1: the packed rows of any window are the block's leading rows
+        entries.append((torch.as_tensor(bt.conf, device=dev),
+                        torch.as_tensor(bt.tokens, device=dev), bt.target.to(dev)))
+    calls = [st.prepare(*e) for e in entries]
+    graphs = [DSparkGraph(st, *e) for e in entries]
+    # the whole pool cycle (one step per entry) in one graph: the GPU-side step time
+    cycle = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(cycle):
+        for e in entries:
+            for c in st.prepare(*e):
+                c()
+    stream = torch.cuda.current_stream()
+    out = {"steps": steps, "pool_blocks": pool,
+           "pool_mb": round(pool * wl.gamma * wl.V * 2 / 1e6, 1)}
+    for mode in ("eager", "graph", "graph_cycle"):
+        def one(i):
+            if mode == "eager":
+                for c in calls[i % pool]:
+                    c()
+            elif mode == "graph":
+                graphs[i % pool].replay()
+            elif i % pool == 0:
+                cycle.replay()
+        n = steps - steps % pool
+        for i in range(2 * pool):
+            one(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n):
+            one(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out[f"step_us_{mode}"] = e0.elapsed_time(e1) * 1e3 / n
+    out["launches_per_step"] = st.LAUNCHES_PER_STEP
+    return out
 
 
 def oracle_inputs(bt, n_req, packed_bits=None):

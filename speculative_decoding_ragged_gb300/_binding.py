@@ -119,6 +119,30 @@ def _ptr(t: Optional[torch.Tensor], name: str, dtype=None, numel=None, min_numel
     return ctypes.c_void_p(t.data_ptr())
 
 
+class Prepared:
+    """One checked, marshalled call: calling it re-issues the same C call (same pointers,
+    sizes and stream) with no Python-side checks, for tight step loops."""
+
+    __slots__ = ("name", "fn", "args")
+
+    def __init__(self, name, args):
+        self.name = name
+        self.fn = getattr(lib(), name)
+        self.args = args
+
+    def __call__(self):
+        rc = self.fn(*self.args)
+        if rc != 0:
+            raise DSparkError(self.name, rc, last_error())
+
+
+def _call(name: str, args, prepare: bool):
+    if prepare:
+        return Prepared(name, args)
+    _check(name, getattr(lib(), name)(*args))
+    return None
+
+
 def version() -> int:
     return lib().dspark_version()
 
@@ -139,25 +163,25 @@ class CostTable:
 
 
 def dspark_schedule(conf: torch.Tensor, cost: CostTable, windows: torch.Tensor,
-                    k_star: torch.Tensor, status: Optional[torch.Tensor] = None, stream=None):
+                    k_star: torch.Tensor, status: Optional[torch.Tensor] = None, stream=None,
+                    prepare: bool = False):
     B = windows.numel()
     L = conf.shape[-1] if conf.dim() == 2 else 0
     gamma = L + 1
-    rc = lib().dspark_schedule(
-        _ptr(conf, "conf", torch.float32, numel=B * L, required=L > 0 and B > 0), B, gamma,
-        ctypes.byref(cost.c), _ptr(windows, "windows", torch.int32),
-        _ptr(k_star, "k_star", torch.int32, min_numel=1),
-        _ptr(status, "status", torch.int32, min_numel=1, required=False), _stream(stream))
-    _check("dspark_schedule", rc)
+    args = (_ptr(conf, "conf", torch.float32, numel=B * L, required=L > 0 and B > 0), B, gamma,
+            ctypes.byref(cost.c), _ptr(windows, "windows", torch.int32),
+            _ptr(k_star, "k_star", torch.int32, min_numel=1),
+            _ptr(status, "status", torch.int32, min_numel=1, required=False), _stream(stream))
+    return _call("dspark_schedule", args, prepare)
 
 
 def dspark_pack(windows: torch.Tensor, block_tokens: torch.Tensor, tiers: torch.Tensor,
                 cu_seqlens: torch.Tensor, packed_ids: torch.Tensor, meta: torch.Tensor,
                 row_req: Optional[torch.Tensor] = None, row_pos: Optional[torch.Tensor] = None,
-                status: Optional[torch.Tensor] = None, stream=None):
+                status: Optional[torch.Tensor] = None, stream=None, prepare: bool = False):
     B, gamma = block_tokens.shape
     cap = packed_ids.numel()
-    rc = lib().dspark_pack(
+    args = (
         _ptr(windows, "windows", torch.int32, numel=B, required=B > 0),
         _ptr(block_tokens, "block_tokens", torch.int32, required=B > 0), B, gamma,
         _ptr(tiers, "tiers", torch.int32), tiers.numel(),
@@ -167,7 +191,7 @@ def dspark_pack(windows: torch.Tensor, block_tokens: torch.Tensor, tiers: torch.
         _ptr(row_pos, "row_pos", torch.int32, min_numel=cap, required=False), cap,
         _ptr(meta, "meta", torch.int32, min_numel=2),
         _ptr(status, "status", torch.int32, min_numel=1, required=False), _stream(stream))
-    _check("dspark_pack", rc)
+    return _call("dspark_pack", args, prepare)
 
 
 def dspark_verify_workspace_bytes(B: int, gamma: int, V: int, stochastic: bool) -> int:
@@ -190,7 +214,7 @@ def dspark_verify(mode, target: torch.Tensor, block_tokens: torch.Tensor,
                   ceiling_len: Optional[torch.Tensor] = None,
                   row_prob: Optional[torch.Tensor] = None, temperature: float = 1.0,
                   seed: int = 0, step: int = 0, status: Optional[torch.Tensor] = None,
-                  stream=None):
+                  stream=None, prepare: bool = False):
     mode = MODES[mode] if isinstance(mode, str) else int(mode)
     B, gamma = block_tokens.shape
     rows, V = target.shape
@@ -200,7 +224,7 @@ def dspark_verify(mode, target: torch.Tensor, block_tokens: torch.Tensor,
             raise ValueError("draft logits must match the target's dtype and vocabulary")
         if draft.numel() != B * (gamma - 1) * V:
             raise ValueError(f"draft logits must hold B*(gamma-1) = {B * (gamma - 1)} rows")
-    rc = lib().dspark_verify(
+    args = (
         mode, int(bool(stochastic)), _ptr(target, "target"), rows,
         _ptr(draft, "draft", required=False), dt, V,
         _ptr(cu_seqlens, "cu_seqlens", torch.int32, min_numel=B + 1, required=False),
@@ -214,20 +238,21 @@ def dspark_verify(mode, target: torch.Tensor, block_tokens: torch.Tensor,
         _ptr(workspace, "workspace", required=False),
         workspace.numel() * workspace.element_size() if workspace is not None else 0,
         _ptr(status, "status", torch.int32, min_numel=1, required=False), _stream(stream))
-    _check("dspark_verify", rc)
+    return _call("dspark_verify", args, prepare)
 
 
 def dspark_scatter(committed: torch.Tensor, accept_len: torch.Tensor, out_tokens: torch.Tensor,
-                   out_len: torch.Tensor, status: Optional[torch.Tensor] = None, stream=None):
+                   out_len: torch.Tensor, status: Optional[torch.Tensor] = None, stream=None,
+                   prepare: bool = False):
     B, gamma = committed.shape
     cap = out_tokens.shape[1] if out_tokens.dim() == 2 else 0
-    rc = lib().dspark_scatter(
+    args = (
         _ptr(committed, "committed", torch.int32, required=B > 0),
         _ptr(accept_len, "accept_len", torch.int32, min_numel=B, required=B > 0), B, gamma,
         _ptr(out_tokens, "out_tokens", torch.int32, min_numel=B * cap, required=B * cap > 0),
         _ptr(out_len, "out_len", torch.int32, min_numel=B, required=B > 0), cap,
         _ptr(status, "status", torch.int32, min_numel=1, required=False), _stream(stream))
-    _check("dspark_scatter", rc)
+    return _call("dspark_scatter", args, prepare)
 
 
 NOALLOC_SCRATCH_BYTES = 4 << 20

@@ -52,6 +52,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    # optional compile-time tuning (e.g. -DDSPARK_STREAM_STAGES=3); build() must then be forced
+    extra += os.environ.get("DSPARK_NVCC_FLAGS", "").split()
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src) + ".o")

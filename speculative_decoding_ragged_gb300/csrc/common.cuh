@@ -61,7 +61,42 @@ int launch_scatter(const int32_t* committed, const int32_t* accept_len, int B, i
                    int32_t* out_tokens, int32_t* out_len, int out_cap, int32_t* status,
                    cudaStream_t stream);
 
+// Launch with programmatic dependent launch allowed: the grid may start while the previous
+// kernel on the stream finishes; every kernel of this library begins with pdl_wait(), which
+// returns once the previous grid has completed and its memory is visible, so nothing is read
+// early. Without a preceding kernel (or one that never triggers) this is a plain launch.
+template <typename... Params, typename... Args>
+int launch_pdl(const char* what, void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+               cudaStream_t stream, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(DSPARK_ERR_CUDA, "dspark %s: %s (%s)", what, cudaGetErrorString(e),
+                    cudaGetErrorName(e));
+    }
+    return check_launch(what);
+}
+
 // ---- device side ------------------------------------------------------------------------
+// Programmatic dependent launch: wait for the previous grid (a no-op when launched plainly),
+// then let the next kernel on the stream begin launching.
+__device__ __forceinline__ void pdl_wait_and_trigger()
+{
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 __device__ __forceinline__ void raise_status(int32_t* status, int bits)
 {
     if (status != nullptr && bits != 0) atomicOr(status, bits);

@@ -5,10 +5,12 @@
 // total is rounded up to the nearest captured graph tier, so a smaller budget replays a truly
 // smaller graph; padding rows up to the tier are waste (figure 2).
 //
-//   1. windows clamped to [1, gamma]; block-wide exclusive scan -> cu_seqlens (in smem too);
-//   2. tier = min over tiers >= M (block min; tiers need not be sorted);
-//   3. one thread per packed row: binary search of cu_seqlens gives (b, i); write the token
-//      and the row's (request, position); padding rows up to the tier get 0 / -1 / -1.
+//   1. every load is issued up front: each thread's windows and its requests' block tokens,
+//      and one tier per thread (n_tiers <= 1024), so the kernel pays one memory round trip;
+//   2. windows clamped to [1, gamma]; block-wide exclusive scan -> cu_seqlens;
+//   3. tier = min over tiers >= M (tiers need not be sorted);
+//   4. each thread writes its requests' rows (token, request, position); padding rows up to
+//      the tier get 0 / -1 / -1.
 #include "common.cuh"
 
 namespace dspark {
@@ -24,23 +26,34 @@ pack_kernel(const int32_t* __restrict__ windows, const int32_t* __restrict__ tok
             int32_t* __restrict__ row_req, int32_t* __restrict__ row_pos, int packed_cap,
             int32_t* __restrict__ meta, int32_t* __restrict__ status)
 {
-    extern __shared__ int cu[];   // [B + 1]
     __shared__ int warp_total[kWarps];
     __shared__ int tier_s;
+    pdl_wait_and_trigger();
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
 
-    if (tid == 0) tier_s = INT_MAX;
-    // 1. exclusive scan; thread t owns requests [t*items, (t+1)*items)
+    // 1. loads
+    const int tier_v = tid < n_tiers ? __ldg(tiers + tid) : INT_MAX;
     const int items = (B + kThreads - 1) / kThreads;
     const int b0 = tid * items;
+    int tok[DSPARK_MAX_GAMMA];
+    int w_first = 1;
+    if (items == 1 && b0 < B) {
+        w_first = __ldg(windows + b0);
+#pragma unroll
+        for (int i = 0; i < DSPARK_MAX_GAMMA; ++i)
+            if (i < gamma) tok[i] = __ldg(tokens + static_cast<int64_t>(b0) * gamma + i);
+    }
+    if (tid == 0) tier_s = INT_MAX;
+
+    // 2. exclusive scan of the clamped windows
     int bad = 0;
     int run = 0;
     for (int it = 0; it < items; ++it) {
         const int b = b0 + it;
         if (b >= B) break;
-        int w = windows[b];
+        int w = items == 1 ? w_first : __ldg(windows + b);
         if (w < 1 || w > gamma) {
             bad = DSPARK_STATUS_BAD_WINDOW;
             w = w < 1 ? 1 : gamma;
@@ -63,27 +76,11 @@ pack_kernel(const int32_t* __restrict__ windows, const int32_t* __restrict__ tok
         warp_total[lane] = t;
     }
     __syncthreads();
-    int acc = incl - run + (warp > 0 ? warp_total[warp - 1] : 0);
-    for (int it = 0; it < items; ++it) {
-        const int b = b0 + it;
-        if (b >= B) break;
-        int w = windows[b];
-        w = w < 1 ? 1 : (w > gamma ? gamma : w);
-        cu[b] = acc;
-        cu_out[b] = acc;
-        acc += w;
-    }
     const int M = warp_total[kWarps - 1];
-    if (tid == 0) {
-        cu[B] = M;
-        cu_out[B] = M;
-    }
-    // 2. tier
-    int best = INT_MAX;
-    for (int t = tid; t < n_tiers; t += kThreads) {
-        const int v = tiers[t];
-        if (v >= M && v < best) best = v;
-    }
+    const int excl = incl - run + (warp > 0 ? warp_total[warp - 1] : 0);
+
+    // 3. tier
+    int best = tier_v >= M ? tier_v : INT_MAX;
     for (int off = 16; off > 0; off >>= 1) best = min(best, __shfl_xor_sync(0xffffffffu, best, off));
     if (lane == 0 && best != INT_MAX) atomicMin(&tier_s, best);
     __syncthreads();
@@ -94,19 +91,36 @@ pack_kernel(const int32_t* __restrict__ windows, const int32_t* __restrict__ tok
     }
     if (tier > packed_cap) bad |= DSPARK_STATUS_PACK_CAPACITY;
 
-    // 3. packed rows
-    const int rows_real = min(M, packed_cap);
-    for (int r = tid; r < rows_real; r += kThreads) {
-        int lo = 0, hi = B;   // largest b with cu[b] <= r
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (cu[mid] <= r) lo = mid; else hi = mid;
+    // 4. rows of this thread's requests, then padding
+    int acc = excl;
+    for (int it = 0; it < items; ++it) {
+        const int b = b0 + it;
+        if (b >= B) break;
+        int w = items == 1 ? w_first : __ldg(windows + b);
+        w = w < 1 ? 1 : (w > gamma ? gamma : w);
+        cu_out[b] = acc;
+        if (items == 1) {
+#pragma unroll
+            for (int i = 0; i < DSPARK_MAX_GAMMA; ++i) {
+                const int r = acc + i;
+                if (i < w && r < packed_cap) {
+                    packed_ids[r] = tok[i];
+                    if (row_req) row_req[r] = b;
+                    if (row_pos) row_pos[r] = i;
+                }
+            }
+        } else {
+            for (int i = 0; i < w; ++i) {
+                const int r = acc + i;
+                if (r >= packed_cap) break;
+                packed_ids[r] = __ldg(tokens + static_cast<int64_t>(b) * gamma + i);
+                if (row_req) row_req[r] = b;
+                if (row_pos) row_pos[r] = i;
+            }
         }
-        const int i = r - cu[lo];
-        packed_ids[r] = tokens[static_cast<int64_t>(lo) * gamma + i];
-        if (row_req) row_req[r] = lo;
-        if (row_pos) row_pos[r] = i;
+        acc += w;
     }
+    if (tid == 0) cu_out[B] = M;
     const int rows_pad = min(tier, packed_cap);
     for (int r = M + tid; r < rows_pad; r += kThreads) {
         packed_ids[r] = 0;
@@ -133,11 +147,9 @@ int launch_pack(const int32_t* windows, const int32_t* tokens, int B, int gamma,
                 int32_t* row_req, int32_t* row_pos, int packed_cap, int32_t* meta,
                 int32_t* status, cudaStream_t stream)
 {
-    const size_t smem = sizeof(int) * static_cast<size_t>(B + 1);
-    pack_kernel<<<1, kThreads, smem, stream>>>(windows, tokens, B, gamma, tiers, n_tiers, cu,
-                                               packed_ids, row_req, row_pos, packed_cap, meta,
-                                               status);
-    return check_launch("pack");
+    return launch_pdl("pack", pack_kernel, dim3(1), dim3(kThreads), 0, stream, windows, tokens, B,
+                      gamma, tiers, n_tiers, cu, packed_ids, row_req, row_pos, packed_cap, meta,
+                      status);
 }
 
 }  // namespace dspark

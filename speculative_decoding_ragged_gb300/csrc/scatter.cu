@@ -16,6 +16,7 @@ scatter_kernel(const int32_t* __restrict__ committed, const int32_t* __restrict_
                int B, int gamma, int32_t* __restrict__ out_tokens, int32_t* __restrict__ out_len,
                int out_cap, int32_t* __restrict__ status)
 {
+    pdl_wait_and_trigger();
     const int64_t b = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (b >= B) return;   // whole warps leave together
@@ -43,9 +44,9 @@ int launch_scatter(const int32_t* committed, const int32_t* accept_len, int B, i
                    cudaStream_t stream)
 {
     const int64_t blocks = ceil_div(static_cast<int64_t>(B) * 32, kThreads);
-    scatter_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
-        committed, accept_len, B, gamma, out_tokens, out_len, out_cap, status);
-    return check_launch("scatter");
+    return launch_pdl("scatter", scatter_kernel, dim3(static_cast<unsigned>(blocks)),
+                      dim3(kThreads), 0, stream, committed, accept_len, B, gamma, out_tokens,
+                      out_len, out_cap, status);
 }
 
 }  // namespace dspark

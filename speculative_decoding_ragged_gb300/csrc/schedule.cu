@@ -7,13 +7,23 @@
 // expected committed tokens per unit of step time, which yields a window per request.
 //
 // Work: n = B*(gamma-1) <= 16384 candidates, all in shared memory of one CTA.
-//   1. survivals -> fixed-point keys, packed with their index into unique 64-bit sort words
-//      word = key << 31 | (2^31 - 1 - index), so descending words = keys descending, then
-//      index ascending (index = b*(gamma-1) + j orders requests, then positions);
-//   2. bitonic sort of the padded power-of-two array, descending;
+//   1. survivals -> fixed-point keys; request b's keys already descend along j (survivals
+//      never grow), so the array starts as B sorted runs in (request, position) order. The
+//      theta entries this thread will need are fetched in the same round trip;
+//   2. n <= 4096: stable merge-path merging of the runs, log2(B) rounds. Keys are 32-bit
+//      (2^32 itself, a survival of exactly 1, is stored as 2^32 - 1, which no other key can
+//      be), indices travel in a parallel array, and on equal keys the lower run goes first,
+//      so the result is ordered by key descending, then request, then position. Each thread
+//      finds the co-rank of its first output with one binary search and merges its outputs
+//      sequentially. Larger n: a bitonic sort of 64-bit words key << 31 | (2^31 - 1 - index);
 //   3. block-wide inclusive scan of the keys (exact uint64 sums S(K));
-//   4. obj(K) = double(B*2^32 + S(K)) / T(K) and a block argmax (smallest K on ties);
-//   5. windows w_b = 1 + count of request b among the first K* words.
+//   4. obj(K) = double(B*2^32 + S(K)) / T(K). FP64 throughput is scarce on this part, so an
+//      fp32 screen (theta read from its bits with integer operations, error < 1e-6 relative)
+//      finds the K within 1e-5 of the best and only those, plus any K the screen cannot
+//      judge (negative or extreme T), get the exact fp64 evaluation; the block argmax compares
+//      the objectives' bit patterns as integers (they are positive) and takes the smallest K
+//      among equal objectives;
+//   5. windows w_b = 1 + count of request b among the first K* candidates.
 // Latency-bound (microseconds); the grid is one CTA by construction of the problem.
 #include "common.cuh"
 
@@ -22,13 +32,99 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
+constexpr int kMergeMax = 4096;          // ping-pong merge buffers up to this many words
+constexpr int kMergeItems = kMergeMax / kThreads;
+constexpr int kBuckets = 1056;           // key 0, then 32 buckets per power of two of the key
+constexpr int kBucketMax = 64;           // larger buckets (many equal keys): merge instead
+constexpr float kScreen = 1.0f - 1e-5f;  // fp32 screen: candidates within 1e-5 of the best
+constexpr float kTmin = 1e-20f, kTmax = 1e20f;   // T range the fp32 screen judges
 
-__device__ __forceinline__ bool better(double o1, int k1, double o2, int k2)
+// Objectives are positive doubles (or "none" = 0), whose bit patterns order like the values:
+// compare them as integers, the larger objective first, then the smaller K.
+__device__ __forceinline__ bool better(uint64_t o1, int k1, uint64_t o2, int k2)
 {
-    // larger objective; on equal objectives the smaller K (k = -1 means "none": loses ties)
     return o1 > o2 || (o1 == o2 && static_cast<unsigned>(k1) < static_cast<unsigned>(k2));
 }
 
+// A non-negative finite double as fp32 by truncating its fields (relative error < 2^-23),
+// with integer operations only. ok = false for negative, infinite, NaN or too-large values.
+__device__ __forceinline__ float nonneg_double_to_float(uint64_t bits, bool& ok)
+{
+    const uint32_t hi = static_cast<uint32_t>(bits >> 32);
+    const int ex = static_cast<int>((hi >> 20) & 0x7FF);
+    if ((hi >> 31) != 0 && (bits << 1) != 0) { ok = false; return 0.0f; }   // negative
+    if (ex == 0x7FF) { ok = false; return 0.0f; }                            // inf, NaN
+    const int ef = ex - 1023 + 127;
+    if (ef >= 255) { ok = false; return 0.0f; }
+    if (ef <= 0) return 0.0f;                                                 // below fp32 range
+    const uint32_t mant = static_cast<uint32_t>(bits >> 29) & 0x7FFFFFu;
+    return __uint_as_float((static_cast<uint32_t>(ef) << 23) | mant);
+}
+
+// fp32 approximation of an exact objective numerator E < 2^53 (two rounded halves).
+__device__ __forceinline__ float e_to_float(uint64_t E)
+{
+    return fmaf(__uint2float_rn(static_cast<uint32_t>(E >> 32)), 4294967296.0f,
+                __uint2float_rn(static_cast<uint32_t>(E)));
+}
+
+// The screen for one K: returns true if K must be evaluated exactly regardless of the
+// screen (the screen cannot judge T), else writes the approximate objective to f.
+__device__ __forceinline__ bool screen(uint64_t E, float t0f, bool t0_ok, uint64_t theta_bits,
+                                       float& f)
+{
+    bool ok = t0_ok;
+    const float th = nonneg_double_to_float(theta_bits, ok);
+    const float T = t0f + th;
+    if (!ok || !(T >= kTmin && T <= kTmax)) return true;
+    f = __fdividef(e_to_float(E), T);
+    return false;
+}
+
+// The sorted run of request b: fixed-point survival keys. MERGE: 32-bit keys and indices in
+// parallel arrays; else 64-bit words key << 31 | (2^31 - 1 - index).
+template <bool MERGE>
+__device__ __forceinline__ void write_run(const float* __restrict__ conf, int b, int L,
+                                          uint64_t* word, uint32_t* key32, int* index)
+{
+    float c[DSPARK_MAX_GAMMA - 1];
+#pragma unroll
+    for (int j = 0; j < DSPARK_MAX_GAMMA - 1; ++j)
+        if (j < L) c[j] = __ldg(conf + static_cast<int64_t>(b) * L + j);
+    float s = 1.0f;
+#pragma unroll
+    for (int j = 0; j < DSPARK_MAX_GAMMA - 1; ++j) {
+        if (j < L) {
+            s = __fmul_rn(s, fminf(fmaxf(c[j], 0.0f), 1.0f));   // NaN -> 0
+            const int idx = b * L + j;
+            // s < 1 gives at most 2^32 - 256; s == 1 gives 2^32, kept as 2^32 - 1 in 32 bits
+            const uint32_t k32 = s >= 1.0f ? 0xFFFFFFFFu : __float2uint_rn(__fmul_rn(s, 4294967296.0f));
+            if (MERGE) {
+                key32[idx] = k32;
+                index[idx] = idx;
+            } else {
+                const uint64_t key = s >= 1.0f ? (1ull << 32) : static_cast<uint64_t>(k32);
+                word[idx] = (key << 31) | static_cast<uint64_t>(0x7FFFFFFF - idx);
+            }
+        }
+    }
+}
+
+// Order-preserving bucket of a 32-bit key (equal keys share a bucket): the fp32 exponent and
+// top five mantissa bits of the key truncated to fp32, so a bucket spans about 3 % of its keys.
+__device__ __forceinline__ int key_bucket(uint32_t k32)
+{
+    if (k32 == 0) return 0;
+    const uint32_t f = __float_as_uint(__uint2float_rz(k32));
+    return static_cast<int>((f >> 18) - (127u << 5)) + 1;
+}
+
+__device__ __forceinline__ uint64_t key_value(uint32_t k32)
+{
+    return k32 == 0xFFFFFFFFu ? (1ull << 32) : static_cast<uint64_t>(k32);
+}
+
+template <bool MERGE>
 __global__ void __launch_bounds__(kThreads, 1)
 schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, double bias,
                 const double* __restrict__ alpha, const double* __restrict__ theta,
@@ -36,56 +132,185 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
                 int32_t* __restrict__ status)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    uint64_t* word = reinterpret_cast<uint64_t*>(smem_raw);   // [n_pad]
-    int* count = reinterpret_cast<int*>(word + n_pad);          // [B]
+    // MERGE: keys [2][n] (u32) and indices [2][n]; else words [n_pad] (u64). Then count [B].
+    uint64_t* word = reinterpret_cast<uint64_t*>(smem_raw);
+    uint32_t* ksrc = reinterpret_cast<uint32_t*>(smem_raw);
+    uint32_t* kdst = ksrc + n;
+    int* isrc = reinterpret_cast<int*>(kdst + n);
+    int* idst = isrc + n;
+    int* count = MERGE ? (idst + n) : reinterpret_cast<int*>(word + n_pad);
     __shared__ uint64_t warp_total[kWarps];
-    __shared__ double red_obj[kWarps];
+    __shared__ uint64_t red_obj[kWarps];
     __shared__ int red_k[kWarps];
+    __shared__ float red_f[kWarps];
     __shared__ int k_best;
+    __shared__ float f_best;
+    __shared__ double t0_s;
+    __shared__ int bucket_cnt[MERGE ? kBuckets : 1];
+    __shared__ int bucket_start[MERGE ? kBuckets : 1];
+    __shared__ int bucket_fill[MERGE ? kBuckets : 1];
+    __shared__ int warp_int[kWarps];
 
+    pdl_wait_and_trigger();
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
+    constexpr int kMaxItems = MERGE ? kMergeItems : DSPARK_MAX_CANDIDATES / kThreads;
+    const int items = (n + kThreads - 1) / kThreads;   // positions per thread, contiguous
+    const int p0 = tid * items;
+    const uint64_t* theta_bits = reinterpret_cast<const uint64_t*>(theta);
 
-    // 1. survival keys, one request per thread (the product is sequential along j)
+    // 1. sorted runs, and this thread's theta entries (K = p + 1 for owned positions p)
+    uint64_t th[kMergeItems];
+    if (MERGE) {
+#pragma unroll
+        for (int it = 0; it < kMergeItems; ++it)
+            if (it < items && p0 + it < n) th[it] = __ldg(theta_bits + B + p0 + it + 1);
+    }
+    uint64_t th0 = 0;
+    if (tid == 0) {
+        th0 = __ldg(theta_bits + B);
+        t0_s = bias + __ldg(alpha + B);
+    }
     for (int b = tid; b < B; b += kThreads) {
-        float s = 1.0f;
-        for (int j = 0; j < L; ++j) {
-            const int idx = b * L + j;
-            const float c = fminf(fmaxf(conf[idx], 0.0f), 1.0f);   // NaN -> 0
-            s = __fmul_rn(s, c);
-            const uint64_t key = __float2ull_rn(__fmul_rn(s, 4294967296.0f));
-            word[idx] = (key << 31) | static_cast<uint64_t>(0x7FFFFFFF - idx);
-        }
+        write_run<MERGE>(conf, b, L, word, ksrc, isrc);
         count[b] = 0;
     }
-    for (int i = n + tid; i < n_pad; i += kThreads) word[i] = 0;   // sorts after every real word
+    if (MERGE)
+        for (int j = tid; j < kBuckets; j += kThreads) {
+            bucket_cnt[j] = 0;
+            bucket_fill[j] = 0;
+        }
+    if (!MERGE)
+        for (int i = n + tid; i < n_pad; i += kThreads) word[i] = 0;   // sorts after all words
     __syncthreads();
 
-    // 2. bitonic sort, descending
-    for (int k = 2; k <= n_pad; k <<= 1) {
-        for (int j = k >> 1; j > 0; j >>= 1) {
-            for (int i = tid; i < (n_pad >> 1); i += kThreads) {
-                const int a = ((i & ~(j - 1)) << 1) | (i & (j - 1));
-                const int c = a + j;
-                const uint64_t x = word[a], y = word[c];
-                const bool descending = (a & k) == 0;
-                if (descending ? (x < y) : (x > y)) {
-                    word[a] = y;
-                    word[c] = x;
+    // 2. sort descending
+    bool sorted = false;
+    if (MERGE) {
+        // 2a. counting sort by key bucket, when every bucket is small
+        for (int p = tid; p < n; p += kThreads) atomicAdd(&bucket_cnt[key_bucket(ksrc[p])], 1);
+        __syncthreads();
+        int big = 0;
+        for (int j = tid; j < kBuckets; j += kThreads) big |= bucket_cnt[j] > kBucketMax;
+        if (!__syncthreads_or(big)) {
+            // bucket starts in descending bucket order; thread t owns reversed buckets 2t, 2t+1
+            const int j0 = kBuckets - 1 - 2 * tid, j1 = j0 - 1;
+            const int a0 = j0 >= 0 ? bucket_cnt[j0] : 0;
+            const int a1 = j1 >= 0 ? bucket_cnt[j1] : 0;
+            int incl_b = a0 + a1;
+            for (int off = 1; off < 32; off <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl_b, off);
+                if (lane >= off) incl_b += v;
+            }
+            if (lane == 31) warp_int[warp] = incl_b;
+            __syncthreads();
+            if (warp == 0) {
+                int t = warp_int[lane];
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, t, off);
+                    if (lane >= off) t += v;
+                }
+                warp_int[lane] = t;
+            }
+            __syncthreads();
+            const int ex = incl_b - (a0 + a1) + (warp > 0 ? warp_int[warp - 1] : 0);
+            if (j0 >= 0) bucket_start[j0] = ex;
+            if (j1 >= 0) bucket_start[j1] = ex + a0;
+            __syncthreads();
+            // scatter into the bucket ranges (any order inside a bucket)
+            for (int p = tid; p < n; p += kThreads) {
+                const uint32_t k = ksrc[p];
+                const int j = key_bucket(k);
+                const int q = bucket_start[j] + atomicAdd(&bucket_fill[j], 1);
+                kdst[q] = k;
+                idst[q] = p;                      // runs start in index order
+            }
+            __syncthreads();
+            // exact place inside the bucket: key descending, then index ascending
+            for (int q = tid; q < n; q += kThreads) {
+                const uint32_t x = kdst[q];
+                const int xi = idst[q];
+                const int j = key_bucket(x);
+                const int s0 = bucket_start[j], c = bucket_cnt[j];
+                int r = 0;
+                for (int t = s0; t < s0 + c; ++t) {
+                    const uint32_t y = kdst[t];
+                    r += (y > x) || (y == x && idst[t] < xi);
+                }
+                ksrc[s0 + r] = x;
+                isrc[s0 + r] = xi;
+            }
+            __syncthreads();
+            sorted = true;
+        }
+    }
+    if (MERGE && !sorted) {
+        // 2b. stable merge of the per-request runs
+        for (int R = L; R < n; R <<= 1) {          // run length: one request, two, four, ...
+            int o = p0;
+            const int o_end = min(p0 + items, n);
+            while (o < o_end) {
+                const int aS = o / (2 * R) * (2 * R);
+                const int aE = min(aS + R, n), bE = min(aS + 2 * R, n);
+                const int lenA = aE - aS, lenB = bE - aE;
+                const uint32_t* A = ksrc + aS;
+                const uint32_t* Bk = ksrc + aE;
+                // co-rank: how many of the first d merged outputs come from run A
+                const int d = o - aS;
+                int lo = max(0, d - lenB), hi = min(d, lenA);
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (A[mid] >= Bk[d - mid - 1]) lo = mid + 1; else hi = mid;
+                }
+                int i = lo, j = d - lo;
+                for (; o < o_end && o < bE; ++o) {
+                    const bool takeA = i < lenA && (j >= lenB || A[i] >= Bk[j]);
+                    if (takeA) {
+                        kdst[o] = A[i];
+                        idst[o] = isrc[aS + i];
+                        ++i;
+                    } else {
+                        kdst[o] = Bk[j];
+                        idst[o] = isrc[aE + j];
+                        ++j;
+                    }
                 }
             }
             __syncthreads();
+            uint32_t* tk = ksrc; ksrc = kdst; kdst = tk;
+            int* ti = isrc; isrc = idst; idst = ti;
+        }
+    } else if (!MERGE) {
+        for (int k = 2; k <= n_pad; k <<= 1) {
+            for (int j = k >> 1; j > 0; j >>= 1) {
+                for (int i = tid; i < (n_pad >> 1); i += kThreads) {
+                    const int a = ((i & ~(j - 1)) << 1) | (i & (j - 1));
+                    const int c = a + j;
+                    const uint64_t x = word[a], y = word[c];
+                    const bool descending = (a & k) == 0;
+                    if (descending ? (x < y) : (x > y)) {
+                        word[a] = y;
+                        word[c] = x;
+                    }
+                }
+                __syncthreads();
+            }
         }
     }
+    auto key_at = [&](int p) -> uint64_t {
+        return MERGE ? key_value(ksrc[p]) : (word[p] >> 31);
+    };
+    auto index_at = [&](int p) -> int {
+        return MERGE ? isrc[p] : 0x7FFFFFFF - static_cast<int>(word[p] & 0x7FFFFFFFull);
+    };
 
-    // 3. inclusive scan of keys; thread t owns positions [t*items, (t+1)*items)
-    const int items = (n_pad + kThreads - 1) / kThreads;
-    const int p0 = tid * items;
+    // 3. inclusive scan of keys over each thread's contiguous positions
     uint64_t run = 0;
-    for (int it = 0; it < items; ++it) {
+#pragma unroll
+    for (int it = 0; it < kMaxItems; ++it) {
         const int p = p0 + it;
-        if (p < n) run += word[p] >> 31;
+        if (it < items && p < n) run += key_at(p);
     }
     uint64_t incl = run;
     for (int off = 1; off < 32; off <<= 1) {
@@ -103,36 +328,77 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
         warp_total[lane] = t;   // inclusive over warps
     }
     __syncthreads();
-    uint64_t S = incl - run + (warp > 0 ? warp_total[warp - 1] : 0);   // exclusive prefix
-
-    // 4. objective and argmax; K = p + 1 for owned position p, K = 0 by thread 0
-    const double t0 = bias + alpha[B];
+    const uint64_t S_excl = incl - run + (warp > 0 ? warp_total[warp - 1] : 0);
     const uint64_t base_E = static_cast<uint64_t>(B) << 32;
-    double best_obj = -INFINITY;
-    int best_k = -1;
+    const double t0 = t0_s;
+    bool t0_ok = true;
+    const float t0f = nonneg_double_to_float(__double_as_longlong(t0), t0_ok);
+
+    // 4a. fp32 screen over the K this thread owns
+    float fb = -INFINITY;
     if (tid == 0) {
-        const double T = t0 + theta[B];
-        if (T > 0.0 && T < INFINITY) {
-            best_obj = static_cast<double>(base_E) / T;
-            best_k = 0;
+        float f;
+        if (!screen(base_E, t0f, t0_ok, th0, f)) fb = f;
+    }
+    {
+        uint64_t S = S_excl;
+#pragma unroll
+        for (int it = 0; it < kMaxItems; ++it) {
+            const int p = p0 + it;
+            if (it >= items || p >= n) break;
+            S += key_at(p);
+            const uint64_t tb = MERGE ? th[it % kMergeItems] : __ldg(theta_bits + B + p + 1);
+            float f;
+            if (!screen(base_E + S, t0f, t0_ok, tb, f)) fb = fmaxf(fb, f);
         }
     }
-    for (int it = 0; it < items; ++it) {
-        const int p = p0 + it;
-        if (p >= n) break;
-        S += word[p] >> 31;
-        const int K = p + 1;
-        const double T = t0 + theta[B + K];
-        if (T > 0.0 && T < INFINITY) {
-            const double obj = static_cast<double>(base_E + S) / T;
-            if (better(obj, K, best_obj, best_k)) {
-                best_obj = obj;
-                best_k = K;
+    for (int off = 16; off > 0; off >>= 1) fb = fmaxf(fb, __shfl_xor_sync(0xffffffffu, fb, off));
+    if (lane == 0) red_f[warp] = fb;
+    __syncthreads();
+    if (warp == 0) {
+        float v = red_f[lane];
+        for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+        if (lane == 0) f_best = v;
+    }
+    __syncthreads();
+    const float thr = f_best * kScreen;
+
+    // 4b. exact objective for the candidates: near the screen's best, or not screenable
+    uint64_t best_obj = 0;        // bit pattern of a positive double; 0 = none
+    int best_k = -1;
+    if (tid == 0) {
+        float f = 0.0f;
+        if (screen(base_E, t0f, t0_ok, th0, f) || f >= thr) {
+            const double T = t0 + __longlong_as_double(th0);
+            if (T > 0.0 && T < INFINITY) {
+                best_obj = __double_as_longlong(static_cast<double>(base_E) / T);
+                best_k = 0;
+            }
+        }
+    }
+    {
+        uint64_t S = S_excl;
+#pragma unroll
+        for (int it = 0; it < kMaxItems; ++it) {
+            const int p = p0 + it;
+            if (it >= items || p >= n) break;
+            S += key_at(p);
+            const uint64_t tb = MERGE ? th[it % kMergeItems] : __ldg(theta_bits + B + p + 1);
+            float f = 0.0f;
+            if (screen(base_E + S, t0f, t0_ok, tb, f) || f >= thr) {
+                const double T = t0 + __longlong_as_double(tb);
+                if (T > 0.0 && T < INFINITY) {
+                    const uint64_t obj = __double_as_longlong(static_cast<double>(base_E + S) / T);
+                    if (better(obj, p + 1, best_obj, best_k)) {
+                        best_obj = obj;
+                        best_k = p + 1;
+                    }
+                }
             }
         }
     }
     for (int off = 16; off > 0; off >>= 1) {
-        const double o = __shfl_xor_sync(0xffffffffu, best_obj, off);
+        const uint64_t o = __shfl_xor_sync(0xffffffffu, best_obj, off);
         const int kk = __shfl_xor_sync(0xffffffffu, best_k, off);
         if (better(o, kk, best_obj, best_k)) {
             best_obj = o;
@@ -148,7 +414,7 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
         best_obj = red_obj[lane];
         best_k = red_k[lane];
         for (int off = 16; off > 0; off >>= 1) {
-            const double o = __shfl_xor_sync(0xffffffffu, best_obj, off);
+            const uint64_t o = __shfl_xor_sync(0xffffffffu, best_obj, off);
             const int kk = __shfl_xor_sync(0xffffffffu, best_k, off);
             if (better(o, kk, best_obj, best_k)) {
                 best_obj = o;
@@ -168,10 +434,7 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
 
     // 5. windows
     const int K_star = k_best;
-    for (int p = tid; p < K_star; p += kThreads) {
-        const int idx = 0x7FFFFFFF - static_cast<int>(word[p] & 0x7FFFFFFFull);
-        atomicAdd(&count[idx / L], 1);
-    }
+    for (int p = tid; p < K_star; p += kThreads) atomicAdd(&count[index_at(p) / L], 1);
     __syncthreads();
     for (int b = tid; b < B; b += kThreads) windows[b] = 1 + count[b];
 }
@@ -182,6 +445,7 @@ __global__ void schedule_trivial_kernel(int B, double bias, const double* __rest
                                         int32_t* __restrict__ k_star, int32_t* __restrict__ status)
 {
     // gamma == 1: no drafts, K* = 0, every window is the anchor row alone
+    pdl_wait_and_trigger();
     const int tid = threadIdx.x;
     for (int b = tid; b < B; b += blockDim.x) windows[b] = 1;
     if (tid == 0) {
@@ -199,36 +463,44 @@ int launch_schedule(const float* conf, int B, int gamma, const dspark_cost* cost
     const int L = gamma - 1;
     const int n = B * L;
     if (n == 0) {
-        schedule_trivial_kernel<<<1, 256, 0, stream>>>(B, cost->bias, cost->alpha, cost->theta,
-                                                        windows, k_star, status);
-        return check_launch("schedule");
+        return launch_pdl("schedule", schedule_trivial_kernel, dim3(1), dim3(256), 0, stream, B,
+                          cost->bias, cost->alpha, cost->theta, windows, k_star, status);
     }
     int n_pad = 1;
     while (n_pad < n) n_pad <<= 1;
-    const size_t smem = sizeof(uint64_t) * static_cast<size_t>(n_pad) +
+    const bool merge = n <= kMergeMax;
+    const size_t smem = (merge ? 16 * static_cast<size_t>(n) : 8 * static_cast<size_t>(n_pad)) +
                         sizeof(int) * static_cast<size_t>(B);
     DeviceInfo dev;
     int rc = current_device(&dev);
     if (rc != DSPARK_OK) return rc;
     // the opt-in limit covers static plus dynamic shared memory
     static thread_local int configured_device = -1;
-    static thread_local size_t max_dynamic = 0;
+    static thread_local size_t max_dynamic[2] = {0, 0};
     if (configured_device != dev.device) {
-        cudaFuncAttributes attr;
-        if (cudaFuncGetAttributes(&attr, schedule_kernel) != cudaSuccess)
-            return check_launch("schedule (attributes)");
-        max_dynamic = static_cast<size_t>(dev.smem_optin) - attr.sharedSizeBytes;
-        if (cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(max_dynamic)) != cudaSuccess)
-            return check_launch("schedule (shared-memory opt-in)");
+        const void* fns[2] = {reinterpret_cast<const void*>(schedule_kernel<false>),
+                              reinterpret_cast<const void*>(schedule_kernel<true>)};
+        for (int v = 0; v < 2; ++v) {
+            cudaFuncAttributes attr;
+            if (cudaFuncGetAttributes(&attr, fns[v]) != cudaSuccess)
+                return check_launch("schedule (attributes)");
+            max_dynamic[v] = static_cast<size_t>(dev.smem_optin) - attr.sharedSizeBytes;
+            if (cudaFuncSetAttribute(fns[v], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(max_dynamic[v])) != cudaSuccess)
+                return check_launch("schedule (shared-memory opt-in)");
+        }
         configured_device = dev.device;
     }
-    if (smem > max_dynamic)
+    if (smem > max_dynamic[merge ? 1 : 0])
         return fail(DSPARK_ERR_UNSUPPORTED, "dspark_schedule: %zu bytes of shared memory needed, "
-                    "the device allows %zu", smem, max_dynamic);
-    schedule_kernel<<<1, kThreads, smem, stream>>>(conf, B, L, n, n_pad, cost->bias, cost->alpha,
-                                                   cost->theta, windows, k_star, status);
-    return check_launch("schedule");
+                    "the device allows %zu", smem, max_dynamic[merge ? 1 : 0]);
+    if (merge)
+        return launch_pdl("schedule", schedule_kernel<true>, dim3(1), dim3(kThreads), smem, stream,
+                          conf, B, L, n, n_pad, cost->bias, cost->alpha, cost->theta, windows,
+                          k_star, status);
+    return launch_pdl("schedule", schedule_kernel<false>, dim3(1), dim3(kThreads), smem, stream,
+                      conf, B, L, n, n_pad, cost->bias, cost->alpha, cost->theta, windows, k_star,
+                      status);
 }
 
 }  // namespace dspark

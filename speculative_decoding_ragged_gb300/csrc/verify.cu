@@ -36,7 +36,10 @@ constexpr int kUnroll = 8;            // 16-byte loads in flight per lane
 constexpr int kFinalThreads = 256;
 constexpr int kFinalWarps = kFinalThreads / 32;
 constexpr int kTargetUnits = 8192;    // aim: about one or two units per resident warp
-constexpr int kMaxChunk = 4096;       // elements per chunk, upper bound
+#ifndef DSPARK_MAX_CHUNK
+#define DSPARK_MAX_CHUNK 4096
+#endif
+constexpr int kMaxChunk = DSPARK_MAX_CHUNK;   // elements per chunk, upper bound
 constexpr int kMinChunk = 256;        // elements per chunk, lower bound
 constexpr int kMaxVocabStochastic = 1 << 20;
 
@@ -133,12 +136,36 @@ __device__ __forceinline__ void unpack8<DSPARK_F32>(const uint4* q, int k, float
 
 // One chunk of one row: lane partial over [v0, v1). Elements are visited by each lane in
 // increasing index order, so a strict '>' keeps the lowest index of the lane's maximum.
+// Exact maximum of the 8 bf16 logits of a 16-byte vector, widened to fp32 (max.bf16x2 does not
+// round; NaN inputs are unsupported).
+__device__ __forceinline__ float bf16x2_max_of(const uint4 u)
+{
+    uint32_t m01, m23, m;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(m01) : "r"(u.x), "r"(u.y));
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(m23) : "r"(u.z), "r"(u.w));
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(m01), "r"(m23));
+    return fmaxf(bf16_lo(m), bf16_hi(m));
+}
+
+// Index of the first of the 8 bf16 logits of `u` equal to `a`, the vector's maximum.
+__device__ __forceinline__ int bf16_first_equal(const uint4 u, float a)
+{
+    const float x[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
+                        bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
+    int e = 0;
+#pragma unroll
+    for (int k = 7; k >= 0; --k)
+        if (x[k] == a) e = k;
+    return e;
+}
+
 template <int DT, bool STOCH>
 __device__ __forceinline__ void chunk_lane(const char* row, int v0, int v1, int vec, float s,
                                            int lane, float& a, float& b, int& idx)
 {
     constexpr int E = (DT == DSPARK_BF16) ? 2 : 4;
     constexpr int Q = (DT == DSPARK_BF16) ? 1 : 2;   // uint4 per 8 elements
+    uint4 best = make_uint4(0, 0, 0, 0);             // bf16 greedy: vector holding the maximum
     if (vec) {
         const char* base = row + static_cast<int64_t>(v0) * E;
         const int n8 = (v1 - v0) >> 3;               // groups of 8 elements
@@ -161,9 +188,17 @@ __device__ __forceinline__ void chunk_lane(const char* row, int v0, int v1, int 
                     unpack8<DT>(buf, k, x);
                     const int vb = v0 + g * 8;
                     if (!STOCH) {
+                        if (DT == DSPARK_BF16) {
+                            // exact packed max of the 8 bf16 values; the index is resolved once
+                            // per chunk from the first vector holding the lane's maximum
+                            const uint4 u = buf[k];
+                            const float vm = bf16x2_max_of(u);
+                            if (vm > a) { a = vm; best = u; idx = vb; }
+                        } else {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            if (x[e] > a) { a = x[e]; idx = vb + e; }
+                            for (int e = 0; e < 8; ++e)
+                                if (x[e] > a) { a = x[e]; idx = vb + e; }
+                        }
                     } else {
                         float vm = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])),
                                          fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
@@ -181,6 +216,7 @@ __device__ __forceinline__ void chunk_lane(const char* row, int v0, int v1, int 
                 }
             }
         }
+        if (!STOCH && DT == DSPARK_BF16 && idx != 0x7FFFFFFF) idx += bf16_first_equal(best, a);
     } else {
         for (int v = v0 + lane; v < v1; v += 32) {
             const float x = load_logit<DT>(row, v);
@@ -197,86 +233,127 @@ __device__ __forceinline__ void chunk_lane(const char* row, int v0, int v1, int 
     }
 }
 
+// Where unit u = (job row, chunk c) reads from and where its partial goes. Draft jobs of the
+// last row of a compact request have no draft (skip).
+struct UnitSrc {
+    const char* row;
+    int64_t slot;   // partial index = (paired target row) * nc + c
+    int c;
+    bool draft;
+    bool skip;
+};
+
+template <int E>
+__device__ __forceinline__ UnitSrc unit_source(const StreamArgs& A, int64_t u, int64_t n_t)
+{
+    UnitSrc s;
+    const int64_t job = u / A.nc;
+    s.c = static_cast<int>(u - job * A.nc);
+    s.skip = false;
+    s.draft = job >= n_t;
+    if (!s.draft) {
+        s.row = static_cast<const char*>(A.target) + job * A.V * E;
+        s.slot = job * A.nc + s.c;
+        return s;
+    }
+    const int L = A.gamma - 1;
+    const int64_t k = job - n_t;
+    int b, i;
+    int64_t r;
+    if (A.mode == DSPARK_COMPACT) {
+        r = k;                                   // draft job of packed row r
+        int lo = 0, hi = A.B;                    // largest b with cu[b] <= r
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (A.cu[mid] <= r) lo = mid; else hi = mid;
+        }
+        b = lo;
+        i = static_cast<int>(r - A.cu[b]);
+        int w = A.windows[b];
+        w = w < 1 ? 1 : (w > A.gamma ? A.gamma : w);
+        if (i < 0 || i >= w - 1 || i >= L) {     // last row of a request: no draft
+            s.skip = true;
+            s.row = nullptr;
+            s.slot = 0;
+            return s;
+        }
+    } else {
+        b = static_cast<int>(k / L);
+        i = static_cast<int>(k - static_cast<int64_t>(b) * L);
+        r = static_cast<int64_t>(b) * A.gamma + i;
+    }
+    s.row = static_cast<const char*>(A.draft) + (static_cast<int64_t>(b) * L + i) * A.V * E;
+    s.slot = r * A.nc + s.c;
+    return s;
+}
+
+// Units this call streams: target rows, then (stochastic) the draft jobs.
+template <bool STOCH>
+__device__ __forceinline__ int64_t unit_count(const StreamArgs& A, int64_t& n_t)
+{
+    n_t = target_row_count(A.mode, A.cu, A.B, A.gamma, A.target_rows, A.rows_max);
+    int64_t n_d = 0;
+    if (STOCH) n_d = (A.mode == DSPARK_COMPACT) ? n_t : static_cast<int64_t>(A.B) * (A.gamma - 1);
+    return (n_t + n_d) * A.nc;
+}
+
+// Warp-level end of a unit: reduce the lanes' running values and write the unit's partial.
+template <bool STOCH>
+__device__ __forceinline__ void write_partial(const StreamArgs& A, const UnitSrc& src, int lane,
+                                              float a, float bsum, int idx)
+{
+    if (!STOCH) {
+        for (int off = 16; off > 0; off >>= 1) {
+            const float v2 = __shfl_xor_sync(0xffffffffu, a, off);
+            const int i2 = __shfl_xor_sync(0xffffffffu, idx, off);
+            arg_merge(a, idx, v2, i2);
+        }
+        if (lane == 0) {
+            ArgPart p;
+            p.v = a;
+            p.idx = idx;
+            static_cast<ArgPart*>(A.part_t)[src.slot] = p;
+        }
+    } else {
+        float m = a;
+        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        double z = 0.0;
+        if (a != -INFINITY) z = static_cast<double>(bsum) * static_cast<double>(ex2_approx((a - m) * A.s));
+        for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+        if (lane == 0) {
+            SoftPart p;
+            p.m = m;
+            p.pad = 0.0f;
+            p.z = z;
+            static_cast<SoftPart*>(src.draft ? A.part_d : A.part_t)[src.slot] = p;
+        }
+    }
+}
+
+// Register-streaming variant: any alignment (scalar loads when the rows are not 16-byte
+// aligned or V % 8 != 0).
 template <int DT, bool STOCH>
 __global__ void __launch_bounds__(kStreamThreads)
 verify_stream_kernel(StreamArgs A)
 {
     constexpr int E = (DT == DSPARK_BF16) ? 2 : 4;
+    pdl_wait_and_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t gw = static_cast<int64_t>(blockIdx.x) * kStreamWarps + (threadIdx.x >> 5);
     const int64_t GW = static_cast<int64_t>(gridDim.x) * kStreamWarps;
-    const int L = A.gamma - 1;
-
-    const int64_t n_t = target_row_count(A.mode, A.cu, A.B, A.gamma, A.target_rows, A.rows_max);
-    int64_t n_d = 0;
-    if (STOCH) n_d = (A.mode == DSPARK_COMPACT) ? n_t : static_cast<int64_t>(A.B) * L;
-    const int64_t U = (n_t + n_d) * A.nc;
+    int64_t n_t;
+    const int64_t U = unit_count<STOCH>(A, n_t);
     const int64_t u0 = gw * U / GW, u1 = (gw + 1) * U / GW;
 
     for (int64_t u = u0; u < u1; ++u) {
-        const int64_t job = u / A.nc;
-        const int c = static_cast<int>(u - job * A.nc);
-        const char* row;
-        int64_t slot;   // partial index = (paired target row) * nc + c
-        if (job < n_t) {
-            row = static_cast<const char*>(A.target) + job * A.V * E;
-            slot = job * A.nc + c;
-        } else {
-            const int64_t k = job - n_t;
-            int b, i;
-            int64_t r;
-            if (A.mode == DSPARK_COMPACT) {
-                r = k;                                   // draft job of packed row r
-                int lo = 0, hi = A.B;                    // largest b with cu[b] <= r
-                while (hi - lo > 1) {
-                    const int mid = (lo + hi) >> 1;
-                    if (A.cu[mid] <= r) lo = mid; else hi = mid;
-                }
-                b = lo;
-                i = static_cast<int>(r - A.cu[b]);
-                int w = A.windows[b];
-                w = w < 1 ? 1 : (w > A.gamma ? A.gamma : w);
-                if (i < 0 || i >= w - 1 || i >= L) continue;   // last row of a request: no draft
-            } else {
-                b = static_cast<int>(k / L);
-                i = static_cast<int>(k - static_cast<int64_t>(b) * L);
-                r = static_cast<int64_t>(b) * A.gamma + i;
-            }
-            row = static_cast<const char*>(A.draft) + (static_cast<int64_t>(b) * L + i) * A.V * E;
-            slot = r * A.nc + c;
-        }
-        const int v0 = c * A.C;
+        const UnitSrc src = unit_source<E>(A, u, n_t);
+        if (src.skip) continue;
+        const int v0 = src.c * A.C;
         const int v1 = min(A.V, v0 + A.C);
         float a = -INFINITY, bsum = 0.0f;
         int idx = 0x7FFFFFFF;
-        chunk_lane<DT, STOCH>(row, v0, v1, A.vec, A.s, lane, a, bsum, idx);
-        if (!STOCH) {
-            for (int off = 16; off > 0; off >>= 1) {
-                const float v2 = __shfl_xor_sync(0xffffffffu, a, off);
-                const int i2 = __shfl_xor_sync(0xffffffffu, idx, off);
-                arg_merge(a, idx, v2, i2);
-            }
-            if (lane == 0) {
-                ArgPart p;
-                p.v = a;
-                p.idx = idx;
-                static_cast<ArgPart*>(A.part_t)[slot] = p;
-            }
-        } else {
-            float m = a;
-            for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-            double z = 0.0;
-            if (a != -INFINITY) z = static_cast<double>(bsum) * static_cast<double>(ex2_approx((a - m) * A.s));
-            for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-            if (lane == 0) {
-                SoftPart p;
-                p.m = m;
-                p.pad = 0.0f;
-                p.z = z;
-                SoftPart* dst = static_cast<SoftPart*>(job < n_t ? A.part_t : A.part_d);
-                dst[slot] = p;
-            }
-        }
+        chunk_lane<DT, STOCH>(src.row, v0, v1, A.vec, A.s, lane, a, bsum, idx);
+        write_partial<STOCH>(A, src, lane, a, bsum, idx);
     }
 }
 
@@ -403,6 +480,7 @@ verify_finalize_kernel(FinalArgs A)
     __shared__ int acc_s[DSPARK_MAX_GAMMA];
     __shared__ int walk_s[4];                 // Lc, Lf (then: done marker), pos, rejected
 
+    pdl_wait_and_trigger();
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -410,6 +488,8 @@ verify_finalize_kernel(FinalArgs A)
     const int gamma = A.gamma;
     const int L = gamma - 1;
     int bits = 0;
+    // the draft this thread may test, fetched before anything else is known
+    const int d_mine = tid < L ? __ldg(A.tokens + static_cast<int64_t>(b) * gamma + tid + 1) : -1;
 
     int w = gamma;
     if (A.mode != DSPARK_STATIC) {
@@ -452,7 +532,7 @@ verify_finalize_kernel(FinalArgs A)
                 const int i2 = __shfl_xor_sync(0xffffffffu, idx, off);
                 arg_merge(v, idx, v2, i2);
             }
-            if (lane == 0) g_s[i] = idx;
+            if (lane == 0) g_s[i] = idx == 0x7FFFFFFF ? 0 : idx;   // all -inf: index 0
         } else {
             float m;
             double z;
@@ -471,7 +551,7 @@ verify_finalize_kernel(FinalArgs A)
         const int i = tid;
         int accepted = 0;
         const bool tested = i < ndec;
-        const int d = tested ? A.tokens[static_cast<int64_t>(b) * gamma + i + 1] : -1;
+        const int d = tested ? d_mine : -1;
         const bool valid = d >= 0 && d < A.V;
         if (tested && !valid) bits |= DSPARK_STATUS_BAD_TOKEN;
         if (!STOCH) {
@@ -507,24 +587,27 @@ verify_finalize_kernel(FinalArgs A)
     }
     __syncthreads();
 
-    // 3. walks: committed window (identical in compact and cap-accept) and the full block
-    if (tid == 0) {
-        int Lc = 1;
-        while (Lc - 1 < w - 1 && acc_s[Lc - 1]) ++Lc;
-        int Lf = 1;
-        while (Lf - 1 < ndec && acc_s[Lf - 1]) ++Lf;
-        walk_s[0] = Lc;
-        walk_s[1] = Lf;
-        walk_s[2] = Lc - 1;
-        walk_s[3] = (Lc - 1 < w - 1) ? 1 : 0;
-        A.accept_len[b] = Lc;
-        if (A.ceiling) A.ceiling[b] = (A.mode == DSPARK_COMPACT) ? -1 : Lf;
+    // 3. walks (warp 0): the window's accept length (identical in compact and cap-accept) and
+    //    the full block's; positions past the tested ones count as rejections
+    if (warp == 0) {
+        const bool acc = lane < ndec && acc_s[lane] != 0;
+        const unsigned rej = __ballot_sync(0xffffffffu, !acc);   // ndec <= 31: never zero
+        const int lead = __ffs(rej) - 1;                          // leading accepted drafts
+        const int Lc = 1 + min(lead, w - 1);
+        const int Lf = 1 + lead;
+        if (lane == 0) {
+            walk_s[0] = Lc;
+            walk_s[1] = Lf;
+            walk_s[2] = Lc - 1;
+            walk_s[3] = (Lc - 1 < w - 1) ? 1 : 0;
+            A.accept_len[b] = Lc;
+            if (A.ceiling) A.ceiling[b] = (A.mode == DSPARK_COMPACT) ? -1 : Lf;
+        }
+        if (!STOCH && lane < gamma) out[lane] = (lane < Lc) ? g_s[lane] : -1;
     }
     __syncthreads();
     const int Lc = walk_s[0];
-    if (!STOCH) {
-        for (int k = tid; k < gamma; k += kFinalThreads) out[k] = (k < Lc) ? g_s[k] : -1;
-    } else {
+    if (STOCH) {
         for (int k = tid; k < gamma; k += kFinalThreads)
             out[k] = (k < Lc - 1) ? A.tokens[static_cast<int64_t>(b) * gamma + k + 1] : -1;
 
@@ -690,8 +773,8 @@ int run_verify(const VerifyCall& c, const Plan& plan, void* part_t, void* part_d
     const int64_t need = ceil_div(max_units, kStreamWarps);
     if (grid > need) grid = need;
     if (grid < 1) grid = 1;
-    verify_stream_kernel<DT, STOCH><<<static_cast<unsigned>(grid), kStreamThreads, 0, stream>>>(sa);
-    rc = check_launch("verify (stream)");
+    rc = launch_pdl("verify (stream)", verify_stream_kernel<DT, STOCH>,
+                    dim3(static_cast<unsigned>(grid)), dim3(kStreamThreads), 0, stream, sa);
     if (rc != DSPARK_OK) return rc;
 
     FinalArgs fa;
@@ -721,8 +804,8 @@ int run_verify(const VerifyCall& c, const Plan& plan, void* part_t, void* part_d
     fa.inv_t = inv_t;
     fa.temp = static_cast<double>(c.temperature);
     const size_t smem = STOCH ? sizeof(double) * static_cast<size_t>((c.V + 255) / 256) : 0;
-    verify_finalize_kernel<DT, STOCH><<<c.B, kFinalThreads, smem, stream>>>(fa);
-    return check_launch("verify (finalize)");
+    return launch_pdl("verify (finalize)", verify_finalize_kernel<DT, STOCH>, dim3(c.B),
+                      dim3(kFinalThreads), smem, stream, fa);
 }
 
 }  // namespace

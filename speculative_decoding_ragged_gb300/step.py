@@ -66,6 +66,25 @@ class DSparkStep:
         bd.dspark_scatter(self.committed, self.accept_len, self.out_tokens, self.out_len,
                           self.status)
 
+    def prepare(self, conf, block_tokens, target, draft=None, *, temperature=1.0, seed=0,
+                step=0, row_prob=None):
+        """The step's four calls, checked and marshalled once for these input tensors (which
+        must stay alive and in place): returns [schedule, pack, verify, scatter], each a
+        callable that re-issues its C call on the current stream without Python-side checks."""
+        return [
+            bd.dspark_schedule(conf, self.cost, self.windows, self.k_star, self.status,
+                               prepare=True),
+            bd.dspark_pack(self.windows, block_tokens, self.tiers, self.cu, self.packed_ids,
+                           self.meta, self.row_req, self.row_pos, self.status, prepare=True),
+            bd.dspark_verify(self.mode, target, block_tokens, self.accept_len, self.committed,
+                             self.workspace, stochastic=self.stochastic, draft=draft,
+                             cu_seqlens=self.cu, windows=self.windows, ceiling_len=self.ceiling,
+                             row_prob=row_prob, temperature=temperature, seed=seed, step=step,
+                             status=self.status, prepare=True),
+            bd.dspark_scatter(self.committed, self.accept_len, self.out_tokens, self.out_len,
+                              self.status, prepare=True),
+        ]
+
     def run(self, conf, block_tokens, target, draft=None, *, temperature=1.0, seed=0, step=0,
             row_prob=None):
         """One whole step. `target` holds the rows this mode verifies: the packed [>=M, V]
@@ -75,3 +94,32 @@ class DSparkStep:
         self.verify(target, block_tokens, draft, temperature=temperature, seed=seed, step=step,
                     row_prob=row_prob)
         self.scatter()
+
+
+class DSparkGraph:
+    """One decode step captured as a CUDA graph over fixed input buffers.
+
+    Every kernel sizes itself on the device (verify reads M from cu_seqlens), so a single
+    graph serves every window allocation and every tier: replay() launches the whole step —
+    schedule, pack, verify, scatter — with one call. New inputs are written into the same
+    tensors (conf, block_tokens, target, draft) before a replay. The step's status word keeps
+    accumulating across replays until the caller zeroes it.
+    """
+
+    def __init__(self, step: DSparkStep, conf, block_tokens, target, draft=None, *,
+                 temperature=1.0, seed=0, step_index=0, row_prob=None):
+        self.step = step
+        kw = dict(temperature=temperature, seed=seed, step=step_index, row_prob=row_prob)
+        # one eager run first: per-device set-up of the library happens outside the capture
+        for call in step.prepare(conf, block_tokens, target, draft, **kw):
+            call()
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            calls = step.prepare(conf, block_tokens, target, draft, **kw)
+            for call in calls:
+                call()
+        self._calls = calls
+
+    def replay(self):
+        self.graph.replay()

@@ -19,13 +19,19 @@ def dev():
 def tables(rng, B, gamma, kind):
     M = np.arange(B * gamma + 1, dtype=np.float64)
     alpha = rng.uniform(0, 0.1) * np.arange(B + 1, dtype=np.float64)
+    bias = float(rng.uniform(0.5, 3))
     if kind == 0:
         theta = rng.uniform(0, 0.05) * M
     elif kind == 1:
         theta = np.ceil(M / 64) * rng.uniform(0, 0.2)
-    else:
+    elif kind == 2:
         theta = rng.uniform(0, 1.0, size=M.size)
-    return float(rng.uniform(0.5, 3)), alpha, theta
+    elif kind == 3:     # negative bias and an offset theta: T > 0 only through cancellation
+        bias = -5.0
+        theta = 6.0 + rng.uniform(0, 0.05) * M
+    else:               # a mix of negative, zero, tiny and huge entries
+        theta = rng.choice([-1.0, 0.0, 1e-30, 1e25, 0.5], size=M.size) * rng.uniform(0.5, 1.5, M.size)
+    return bias, alpha, theta
 
 
 SIZES = [(1, 1), (1, 2), (4, 4), (3, 32), (7, 8), (100, 5), (256, 8), (512, 8), (1000, 17),
@@ -35,7 +41,7 @@ SIZES = [(1, 1), (1, 2), (4, 4), (3, 32), (7, 8), (100, 5), (256, 8), (512, 8), 
 @pytest.mark.parametrize("B,gamma", SIZES)
 def test_schedule_parity_random(dev, B, gamma):
     rng = np.random.default_rng(B * 100 + gamma)
-    for trial in range(4):
+    for trial in range(6):
         a = rng.uniform(0.1, 0.95, size=B)
         conf = rng.beta(8 * a[:, None], 8 * (1 - a[:, None]), size=(B, gamma - 1))
         if trial == 1:
@@ -44,7 +50,7 @@ def test_schedule_parity_random(dev, B, gamma):
             conf[rng.uniform(size=conf.shape) < 0.05] = np.nan
             conf[rng.uniform(size=conf.shape) < 0.05] = 1.5
         conf = conf.astype(np.float32)
-        bias, alpha, theta = tables(rng, B, gamma, trial % 3)
+        bias, alpha, theta = tables(rng, B, gamma, trial % 5)
         g = gpu_schedule(dev, conf, bias, alpha, theta)
         r = oracle.schedule(conf, bias, alpha, theta)
         np.testing.assert_array_equal(g["windows"], r["windows"])
