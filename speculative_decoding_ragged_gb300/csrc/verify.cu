@@ -32,7 +32,10 @@ namespace {
 
 constexpr int kStreamThreads = 256;
 constexpr int kStreamWarps = kStreamThreads / 32;
-constexpr int kUnroll = 8;            // 16-byte loads in flight per lane
+#ifndef DSPARK_UNROLL
+#define DSPARK_UNROLL 8
+#endif
+constexpr int kUnroll = DSPARK_UNROLL;  // 16-byte loads in flight per lane
 constexpr int kFinalThreads = 256;
 constexpr int kFinalWarps = kFinalThreads / 32;
 constexpr int kTargetUnits = 8192;    // aim: about one or two units per resident warp
@@ -317,14 +320,14 @@ __device__ __forceinline__ void write_partial(const StreamArgs& A, const UnitSrc
     } else {
         float m = a;
         for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-        double z = 0.0;
-        if (a != -INFINITY) z = static_cast<double>(bsum) * static_cast<double>(ex2_approx((a - m) * A.s));
+        // fp32 tree over the 32 lanes (FP64 throughput is scarce on this part)
+        float z = a != -INFINITY ? bsum * ex2_approx((a - m) * A.s) : 0.0f;
         for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
         if (lane == 0) {
             SoftPart p;
             p.m = m;
             p.pad = 0.0f;
-            p.z = z;
+            p.z = static_cast<double>(z);
             static_cast<SoftPart*>(src.draft ? A.part_d : A.part_t)[src.slot] = p;
         }
     }
@@ -459,7 +462,7 @@ __device__ __forceinline__ void combine_soft(const SoftPart* parts, int nc, floa
     if (m != -INFINITY) {
         for (int c = lane; c < nc; c += 32) {
             const SoftPart p = parts[c];
-            if (p.m != -INFINITY) z += p.z * exp2(static_cast<double>(p.m - m) * static_cast<double>(s));
+            if (p.m != -INFINITY) z += p.z * static_cast<double>(ex2_approx((p.m - m) * s));
         }
     }
     for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
@@ -480,7 +483,6 @@ verify_finalize_kernel(FinalArgs A)
     __shared__ int acc_s[DSPARK_MAX_GAMMA];
     __shared__ int walk_s[4];                 // Lc, Lf (then: done marker), pos, rejected
 
-    pdl_wait_and_trigger();
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -488,21 +490,22 @@ verify_finalize_kernel(FinalArgs A)
     const int gamma = A.gamma;
     const int L = gamma - 1;
     int bits = 0;
-    // the draft this thread may test, fetched before anything else is known
+    // Inputs that no kernel of this call writes (drafts, windows, cu_seqlens) are fetched before
+    // waiting for the streaming kernel: they were complete before that kernel started.
     const int d_mine = tid < L ? __ldg(A.tokens + static_cast<int64_t>(b) * gamma + tid + 1) : -1;
-
     int w = gamma;
     if (A.mode != DSPARK_STATIC) {
-        w = A.windows[b];
+        w = __ldg(A.windows + b);
         if (w < 1 || w > gamma) {
             if (tid == 0) bits |= DSPARK_STATUS_BAD_WINDOW;
             w = w < 1 ? 1 : gamma;
         }
     }
     const int nrows = (A.mode == DSPARK_COMPACT) ? w : gamma;
-    const int64_t base = (A.mode == DSPARK_COMPACT) ? static_cast<int64_t>(A.cu[b])
+    const int64_t base = (A.mode == DSPARK_COMPACT) ? static_cast<int64_t>(__ldg(A.cu + b))
                                                     : static_cast<int64_t>(b) * gamma;
     const int64_t n_t = target_row_count(A.mode, A.cu, A.B, gamma, A.target_rows, A.rows_max);
+    pdl_wait_and_trigger();
     int32_t* out = A.committed + static_cast<int64_t>(b) * gamma;
 
     if (base < 0 || base + nrows > n_t) {
@@ -628,9 +631,9 @@ verify_finalize_kernel(FinalArgs A)
                 float wv[8];
                 bonus_weights<DT>(trow, drow, t * 256 + lane * 8, A.V, A.vec, residual, mp, izp,
                                   mq, izq, A.s, wv);
-                double ts = static_cast<double>(sum8(wv));
+                float ts = sum8(wv);
                 for (int off = 16; off > 0; off >>= 1) ts += __shfl_xor_sync(0xffffffffu, ts, off);
-                if (lane == 0) tile_sum[t] = ts;
+                if (lane == 0) tile_sum[t] = static_cast<double>(ts);
             }
             __syncthreads();
             if (warp == 0) {
