@@ -106,7 +106,8 @@ def measured_peak():
 
 
 def profile_traffic():
-    """ncu DRAM bytes per verify-stream launch recorded in profiles/, if still current."""
+    """DRAM bytes over algorithmic bytes of the captured verify-stream launch recorded in
+    profiles/, if verify.cu still hashes to the value recorded with it."""
     try:
         with open(PROFILE) as f:
             text = f.read()
@@ -123,7 +124,7 @@ def profile_traffic():
     if rec.get("verify_cu_sha256_16") != digest:
         return None
     try:
-        return float(rec["traffic_bytes_per_launch_full_size"])
+        return float(rec["traffic_over_algorithmic"])
     except (KeyError, ValueError):
         return None
 
@@ -266,7 +267,8 @@ def run_native(args, rank, world, local):
     verify_bytes = [batches[i % nb]["M"] * wl.V * 2 for i in range(K)]
     ach_gbs = sum(verify_bytes) / (sum(verify_us) * 1e-6) / 1e9
     peak, peak_kind = measured_peak()
-    traffic = profile_traffic()
+    ratio = profile_traffic()     # DRAM bytes / algorithmic bytes of a captured launch
+    traffic = None if ratio is None else ratio * statistics.mean(verify_bytes)
     value = rows / (ms * 1e-3)
 
     # end to end through the C ABI with host buffers: H2D of the step's inputs from pinned
