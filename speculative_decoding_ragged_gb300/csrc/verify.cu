@@ -36,8 +36,9 @@ constexpr int kStreamWarps = kStreamThreads / 32;
 #define DSPARK_UNROLL 8
 #endif
 constexpr int kUnroll = DSPARK_UNROLL;  // 16-byte loads in flight per lane
-constexpr int kFinalThreads = 256;
-constexpr int kFinalWarps = kFinalThreads / 32;
+constexpr int kFinalThreadsGreedy = 256;
+constexpr int kFinalThreadsStoch = 512;   // the bonus pass streams one or two rows per request
+constexpr int kBonusGroup = 4;            // tiles a warp loads before reducing them
 constexpr int kTargetUnits = 8192;    // aim: about one or two units per resident warp
 #ifndef DSPARK_MAX_CHUNK
 #define DSPARK_MAX_CHUNK 4096
@@ -421,17 +422,14 @@ __device__ __forceinline__ void load8(const char* row, int v0, int V, int vec, f
     }
 }
 
-// Bonus weights of 8 consecutive tokens: p_v (residual == 0) or max(0, p_v - q_v).
+// Bonus weights of 8 consecutive tokens from their logits: p_v (residual == 0) or
+// max(0, p_v - q_v); tokens at or past V weigh 0.
 template <int DT>
-__device__ __forceinline__ void bonus_weights(const char* trow, const char* drow, int v0, int V,
-                                              int vec, bool residual, float mp, float izp,
-                                              float mq, float izq, float s, float (&w)[8])
+__device__ __forceinline__ void bonus_weights_of(const float (&xp)[8], const float (&xq)[8], int v0,
+                                                 int V, bool residual, float mp, float izp,
+                                                 float mq, float izq, float s, float (&w)[8])
 {
-    float xp[8];
-    load8<DT>(trow, v0, V, vec, xp);
     if (residual) {
-        float xq[8];
-        load8<DT>(drow, v0, V, vec, xq);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const float p = (v0 + e < V) ? ex2_approx((xp[e] - mp) * s) * izp : 0.0f;
@@ -443,6 +441,18 @@ __device__ __forceinline__ void bonus_weights(const char* trow, const char* drow
         for (int e = 0; e < 8; ++e)
             w[e] = (v0 + e < V) ? ex2_approx((xp[e] - mp) * s) * izp : 0.0f;
     }
+}
+
+// The same weights, loading the logits first.
+template <int DT>
+__device__ __forceinline__ void bonus_weights(const char* trow, const char* drow, int v0, int V,
+                                              int vec, bool residual, float mp, float izp,
+                                              float mq, float izq, float s, float (&w)[8])
+{
+    float xp[8], xq[8];
+    load8<DT>(trow, v0, V, vec, xp);
+    if (residual) load8<DT>(drow, v0, V, vec, xq);
+    bonus_weights_of<DT>(xp, xq, v0, V, residual, mp, izp, mq, izq, s, w);
 }
 
 __device__ __forceinline__ float sum8(const float (&w)[8])
@@ -471,9 +481,11 @@ __device__ __forceinline__ void combine_soft(const SoftPart* parts, int nc, floa
 }
 
 template <int DT, bool STOCH>
-__global__ void __launch_bounds__(kFinalThreads)
+__global__ void __launch_bounds__(STOCH ? kFinalThreadsStoch : kFinalThreadsGreedy)
 verify_finalize_kernel(FinalArgs A)
 {
+    constexpr int kFinalThreads = STOCH ? kFinalThreadsStoch : kFinalThreadsGreedy;
+    constexpr int kFinalWarps = kFinalThreads / 32;
     constexpr int E = (DT == DSPARK_BF16) ? 2 : 4;
     extern __shared__ double tile_sum[];      // stochastic bonus: one entry per 256-token tile
     __shared__ int g_s[DSPARK_MAX_GAMMA];
@@ -627,13 +639,26 @@ verify_finalize_kernel(FinalArgs A)
             const bool residual = walk_s[3] != 0 && attempt == 0;
             const float mq = residual ? mq_s[pos] : 0.0f;
             const float izq = residual ? static_cast<float>(1.0 / zq_s[pos]) : 0.0f;
-            for (int t = warp; t < n_tiles; t += kFinalWarps) {
-                float wv[8];
-                bonus_weights<DT>(trow, drow, t * 256 + lane * 8, A.V, A.vec, residual, mp, izp,
-                                  mq, izq, A.s, wv);
-                float ts = sum8(wv);
-                for (int off = 16; off > 0; off >>= 1) ts += __shfl_xor_sync(0xffffffffu, ts, off);
-                if (lane == 0) tile_sum[t] = static_cast<double>(ts);
+            // each warp loads kBonusGroup tiles, then weighs and sums them: a few global
+            // round trips per row instead of one per tile
+            for (int t0 = warp; t0 < n_tiles; t0 += kBonusGroup * kFinalWarps) {
+                float xp[kBonusGroup][8], xq[kBonusGroup][8];
+#pragma unroll
+                for (int g = 0; g < kBonusGroup; ++g) {
+                    const int v0 = (t0 + g * kFinalWarps) * 256 + lane * 8;
+                    load8<DT>(trow, v0, A.V, A.vec, xp[g]);
+                    if (residual) load8<DT>(drow, v0, A.V, A.vec, xq[g]);
+                }
+#pragma unroll
+                for (int g = 0; g < kBonusGroup; ++g) {
+                    const int t = t0 + g * kFinalWarps;
+                    float wv[8];
+                    bonus_weights_of<DT>(xp[g], xq[g], t * 256 + lane * 8, A.V, residual, mp, izp,
+                                         mq, izq, A.s, wv);
+                    float ts = sum8(wv);
+                    for (int off = 16; off > 0; off >>= 1) ts += __shfl_xor_sync(0xffffffffu, ts, off);
+                    if (lane == 0 && t < n_tiles) tile_sum[t] = static_cast<double>(ts);
+                }
             }
             __syncthreads();
             if (warp == 0) {
@@ -808,7 +833,7 @@ int run_verify(const VerifyCall& c, const Plan& plan, void* part_t, void* part_d
     fa.temp = static_cast<double>(c.temperature);
     const size_t smem = STOCH ? sizeof(double) * static_cast<size_t>((c.V + 255) / 256) : 0;
     return launch_pdl("verify (finalize)", verify_finalize_kernel<DT, STOCH>, dim3(c.B),
-                      dim3(kFinalThreads), smem, stream, fa);
+                      dim3(STOCH ? kFinalThreadsStoch : kFinalThreadsGreedy), smem, stream, fa);
 }
 
 }  // namespace
