@@ -39,7 +39,7 @@ constexpr int kUnroll = DSPARK_UNROLL;  // 16-byte loads in flight per lane
 constexpr int kFinalThreadsGreedy = 256;
 constexpr int kFinalThreadsStoch = 512;   // the bonus pass streams one or two rows per request
 constexpr int kBonusGroup = 4;            // tiles a warp loads before reducing them
-constexpr int kTargetUnits = 8192;    // aim: about one or two units per resident warp
+constexpr int kTargetUnits = 4096;    // aim: about one unit per resident warp
 #ifndef DSPARK_MAX_CHUNK
 #define DSPARK_MAX_CHUNK 4096
 #endif
@@ -51,10 +51,9 @@ struct __align__(8) ArgPart {
     float v;
     int idx;
 };
-struct __align__(16) SoftPart {
-    float m;
-    float pad;
-    double z;
+struct __align__(8) SoftPart {
+    float m;   // chunk maximum of the raw logits
+    float z;   // sum over the chunk of exp2((l - m) * log2(e) / T)
 };
 
 struct Plan {
@@ -327,8 +326,7 @@ __device__ __forceinline__ void write_partial(const StreamArgs& A, const UnitSrc
         if (lane == 0) {
             SoftPart p;
             p.m = m;
-            p.pad = 0.0f;
-            p.z = static_cast<double>(z);
+            p.z = z;
             static_cast<SoftPart*>(src.draft ? A.part_d : A.part_t)[src.slot] = p;
         }
     }
@@ -463,16 +461,16 @@ __device__ __forceinline__ float sum8(const float (&w)[8])
 // Combined softmax statistics of one row from its nc chunk partials, by one warp, in a fixed
 // order (lane-strided, then a fixed shuffle tree): deterministic for a given nc.
 __device__ __forceinline__ void combine_soft(const SoftPart* parts, int nc, float s, int lane,
-                                             float& m_out, double& z_out)
+                                             float& m_out, float& z_out)
 {
     float m = -INFINITY;
     for (int c = lane; c < nc; c += 32) m = fmaxf(m, parts[c].m);
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    double z = 0.0;
+    float z = 0.0f;
     if (m != -INFINITY) {
         for (int c = lane; c < nc; c += 32) {
             const SoftPart p = parts[c];
-            if (p.m != -INFINITY) z += p.z * static_cast<double>(ex2_approx((p.m - m) * s));
+            if (p.m != -INFINITY) z += p.z * ex2_approx((p.m - m) * s);
         }
     }
     for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
@@ -490,7 +488,7 @@ verify_finalize_kernel(FinalArgs A)
     extern __shared__ double tile_sum[];      // stochastic bonus: one entry per 256-token tile
     __shared__ int g_s[DSPARK_MAX_GAMMA];
     __shared__ float mp_s[DSPARK_MAX_GAMMA], mq_s[DSPARK_MAX_GAMMA];
-    __shared__ double zp_s[DSPARK_MAX_GAMMA], zq_s[DSPARK_MAX_GAMMA];
+    __shared__ float zp_s[DSPARK_MAX_GAMMA], zq_s[DSPARK_MAX_GAMMA];
     __shared__ double ub_s[DSPARK_MAX_GAMMA];
     __shared__ int acc_s[DSPARK_MAX_GAMMA];
     __shared__ int walk_s[4];                 // Lc, Lf (then: done marker), pos, rejected
@@ -549,8 +547,7 @@ verify_finalize_kernel(FinalArgs A)
             }
             if (lane == 0) g_s[i] = idx == 0x7FFFFFFF ? 0 : idx;   // all -inf: index 0
         } else {
-            float m;
-            double z;
+            float m, z;
             combine_soft(static_cast<const SoftPart*>(A.part_t) + r * A.nc, A.nc, A.s, lane, m, z);
             if (lane == 0) { mp_s[i] = m; zp_s[i] = z; }
             if (i < ndec) {
@@ -583,15 +580,21 @@ verify_finalize_kernel(FinalArgs A)
             if (tested && valid) {
                 const char* trow = static_cast<const char*>(A.target) + (base + i) * A.V * E;
                 const char* drow = static_cast<const char*>(A.draft) + (static_cast<int64_t>(b) * L + i) * A.V * E;
-                const double lp = load_logit<DT>(trow, d);
-                const double lq = load_logit<DT>(drow, d);
-                const double p = exp((lp - static_cast<double>(mp_s[i])) / A.temp) / zp_s[i];
-                const double q = exp((lq - static_cast<double>(mq_s[i])) / A.temp) / zq_s[i];
+                const float lp = load_logit<DT>(trow, d);
+                const float lq = load_logit<DT>(drow, d);
+                // fp32 (FP64 is scarce here): exponents relative to each row's maximum, and the
+                // ratio as one exp2 of their difference, so p/q neither under- nor overflows
+                const float ep = (lp - mp_s[i]) * A.s;
+                const float eq = (lq - mq_s[i]) * A.s;
                 const float u = static_cast<float>(rnd[0] >> 40) * 0x1p-24f;
-                if (q == 0.0) accepted = 1;
-                else accepted = u < static_cast<float>(p / q);
-                pp = static_cast<float>(p);
-                qq = static_cast<float>(q);
+                if (lq == -INFINITY) {
+                    accepted = 1;                          // q(d) = 0
+                } else {
+                    const float ratio = exp2f(ep - eq) * (zq_s[i] / zp_s[i]);
+                    accepted = u < ratio;
+                }
+                pp = exp2f(ep) / zp_s[i];
+                qq = exp2f(eq) / zq_s[i];
             }
             if (A.row_prob) {
                 A.row_prob[(base + i) * 2] = pp;
@@ -633,12 +636,12 @@ verify_finalize_kernel(FinalArgs A)
         const char* trow = static_cast<const char*>(A.target) + (base + pos) * A.V * E;
         const char* drow = static_cast<const char*>(A.draft) + (static_cast<int64_t>(b) * L + pos) * A.V * E;
         const float mp = mp_s[pos];
-        const float izp = static_cast<float>(1.0 / zp_s[pos]);
+        const float izp = 1.0f / zp_s[pos];
         const int n_tiles = (A.V + 255) / 256;
         for (int attempt = 0; attempt < 2; ++attempt) {
             const bool residual = walk_s[3] != 0 && attempt == 0;
             const float mq = residual ? mq_s[pos] : 0.0f;
-            const float izq = residual ? static_cast<float>(1.0 / zq_s[pos]) : 0.0f;
+            const float izq = residual ? 1.0f / zq_s[pos] : 0.0f;
             // each warp loads kBonusGroup tiles, then weighs and sums them: a few global
             // round trips per row instead of one per tile
             for (int t0 = warp; t0 < n_tiles; t0 += kBonusGroup * kFinalWarps) {

@@ -66,7 +66,7 @@ def test_workspace_size_is_a_function_of_sizes(lib):
     assert bd.dspark_verify_workspace_bytes(0, 8, 1000, False) == 0
     g = bd.dspark_verify_workspace_bytes(256, 8, 151936, False)
     s = bd.dspark_verify_workspace_bytes(256, 8, 151936, True)
-    assert g > 0 and s == 4 * g          # two arrays of 16-byte partials vs one of 8-byte
+    assert g > 0 and s == 2 * g          # target and draft partials vs target only (8 B each)
     assert g % 256 == 0
     assert bd.dspark_verify_workspace_bytes(-1, 8, 10, False) == 0
     assert "bad sizes" in bd.last_error()

@@ -83,13 +83,12 @@ def test_noalloc_matches_workspace_verify_on_two_calls(dev, name):
 
 
 def test_noalloc_refuses_sizes_beyond_its_array(dev):
-    B, gamma, V = 512, 8, 151936          # stochastic partials need about 5 MB
+    B, gamma, V = 1024, 16, 151936        # stochastic partials need about 10 MB
     assert bd.dspark_verify_workspace_bytes(B, gamma, V, True) > bd.NOALLOC_SCRATCH_BYTES
     i32 = dict(dtype=torch.int32, device=dev)
-    target = torch.zeros((B * gamma, V), dtype=torch.bfloat16, device=dev)
-    draft = torch.zeros((B * (gamma - 1), V), dtype=torch.bfloat16, device=dev)
+    target = torch.zeros((1, V), dtype=torch.bfloat16, device=dev)   # refused before any read
     with pytest.raises(bd.DSparkError) as err:
         bd.dspark_verify_noalloc("static", target, torch.zeros((B, gamma), **i32),
                                  torch.zeros(B, **i32), torch.zeros((B, gamma), **i32),
-                                 stochastic=True, draft=draft)
+                                 stochastic=True)
     assert err.value.code == -2 and "static array holds" in str(err.value)
