@@ -54,6 +54,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batches", type=int, default=N_BATCHES)
     ap.add_argument("--latency-steps", type=int, default=10000)
+    ap.add_argument("--event-every", type=int, default=8,
+                    help="record the per-kernel events on every n-th timed step only: an event "
+                         "between two kernels stops the second from launching early")
     return ap.parse_args()
 
 
@@ -245,7 +248,8 @@ def run_native(args, rank, world, local):
 
     # device-resident timed region: K steps, events around sched+pack and verify each step
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampled = [i for i in range(K) if i % max(1, args.event_every) == 0]
+    evs = {i: [torch.cuda.Event(enable_timing=True) for _ in range(3)] for i in sampled}
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     barrier(world)
@@ -253,7 +257,7 @@ def run_native(args, rank, world, local):
     clocks.start()
     t_start.record(stream)
     for i in range(K):
-        step(i, evs[i])
+        step(i, evs.get(i))
     t_end.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
@@ -262,9 +266,9 @@ def run_native(args, rank, world, local):
     ms = max_over_ranks(ms, world)
     rows = sum(batches[i % nb]["M"] for i in range(K))
     rows = sum_over_ranks(rows, world)
-    sched_us = [evs[i][0].elapsed_time(evs[i][1]) * 1e3 for i in range(K)]
-    verify_us = [evs[i][1].elapsed_time(evs[i][2]) * 1e3 for i in range(K)]
-    verify_bytes = [batches[i % nb]["M"] * wl.V * 2 for i in range(K)]
+    sched_us = [evs[i][0].elapsed_time(evs[i][1]) * 1e3 for i in sampled]
+    verify_us = [evs[i][1].elapsed_time(evs[i][2]) * 1e3 for i in sampled]
+    verify_bytes = [batches[i % nb]["M"] * wl.V * 2 for i in sampled]
     ach_gbs = sum(verify_bytes) / (sum(verify_us) * 1e-6) / 1e9
     peak, peak_kind = measured_peak()
     ratio = profile_traffic()     # DRAM bytes / algorithmic bytes of a captured launch
@@ -324,6 +328,7 @@ def run_native(args, rank, world, local):
         "sched_pack_us": statistics.median(sched_us),
         "verify_us": statistics.median(verify_us),
         "step_us": ms / K * 1e3,
+        "events_sampled_steps": len(sampled),
         "roofline": {"bound": "hbm", "kernel": "dspark_verify (stream + finalize)",
                      "achieved": ach_gbs, "peak": peak, "peak_source": peak_kind,
                      "unit": "GB/s", "frac": ach_gbs / peak, "traffic": traffic,
@@ -340,54 +345,60 @@ def run_native(args, rank, world, local):
 
 
 def latency_leg(dev, steps, pool=64):
-    """Per-step time of the batch-1 workload (B=1, gamma=16, V=129280 bf16, greedy compact):
-    `steps` consecutive steps cycling through `pool` seeded inputs (4 MB of logits each, the
-    pool larger than L2), launched eagerly (five kernels per step) and as one CUDA graph
-    replay per step."""
+    """Per-step time of the batch-1 workload (B=1, gamma=16, V=129280 bf16, compact), greedy
+    and stochastic (T = 0.7): `steps` consecutive steps cycling through `pool` seeded inputs
+    (the pool's logits exceed L2), launched eagerly (five kernels per step), as one CUDA graph
+    replay per step, and as one graph holding a whole pool cycle (the GPU-side step time)."""
     from speculative_decoding_ragged_gb300 import synth
     from speculative_decoding_ragged_gb300.step import DSparkGraph, DSparkStep
     wl = synth.WORKLOADS["latency_b1"]
-    st = DSparkStep(wl.B, wl.gamma, wl.V, wl.tiers, wl.bias, wl.alpha_slope * np.arange(2),
-                    wl.theta_slope * np.arange(wl.gamma + 1), out_cap=16, device=dev)
-    entries = []
-    for k in range(pool):
-        target, _ = synth.make_logits(wl.with_(draft_sigma=None), seed=0, pool_index=k)
-        bt = synth.make_batch(wl, seed=0, step=k, logits=(target, None))
-        # B = 1: the packed rows of any window are the block's leading rows
-        entries.append((torch.as_tensor(bt.conf, device=dev),
-                        torch.as_tensor(bt.tokens, device=dev), bt.target.to(dev)))
-    calls = [st.prepare(*e) for e in entries]
-    graphs = [DSparkGraph(st, *e) for e in entries]
-    # the whole pool cycle (one step per entry) in one graph: the GPU-side step time
-    cycle = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(cycle):
-        for e in entries:
-            for c in st.prepare(*e):
-                c()
-    stream = torch.cuda.current_stream()
-    out = {"steps": steps, "pool_blocks": pool,
-           "pool_mb": round(pool * wl.gamma * wl.V * 2 / 1e6, 1)}
-    for mode in ("eager", "graph", "graph_cycle"):
-        def one(i):
-            if mode == "eager":
-                for c in calls[i % pool]:
+    out = {"steps": steps, "pool_blocks": pool, "launches_per_step": DSparkStep.LAUNCHES_PER_STEP}
+    for stochastic in (False, True):
+        st = DSparkStep(wl.B, wl.gamma, wl.V, wl.tiers, wl.bias, wl.alpha_slope * np.arange(2),
+                        wl.theta_slope * np.arange(wl.gamma + 1), out_cap=16,
+                        stochastic=stochastic, device=dev)
+        entries = []
+        for k in range(pool):
+            target, draft = synth.make_logits(wl, seed=0, pool_index=k)
+            bt = synth.make_batch(wl, seed=0, step=k, stochastic=stochastic,
+                                  logits=(target, draft))
+            # B = 1: the packed rows of any window are the block's leading rows
+            entries.append((torch.as_tensor(bt.conf, device=dev),
+                            torch.as_tensor(bt.tokens, device=dev), bt.target.to(dev),
+                            bt.draft.to(dev) if stochastic else None))
+        kw = dict(temperature=wl.temperature, seed=7)
+        calls = [st.prepare(*e, step=k, **kw) for k, e in enumerate(entries)]
+        graphs = [DSparkGraph(st, *e, step_index=k, **kw) for k, e in enumerate(entries)]
+        cycle = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cycle):
+            for k, e in enumerate(entries):
+                for c in st.prepare(*e, step=k, **kw):
                     c()
-            elif mode == "graph":
-                graphs[i % pool].replay()
-            elif i % pool == 0:
-                cycle.replay()
-        n = steps - steps % pool
-        for i in range(2 * pool):
-            one(i)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(n):
-            one(i)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        out[f"step_us_{mode}"] = e0.elapsed_time(e1) * 1e3 / n
-    out["launches_per_step"] = st.LAUNCHES_PER_STEP
+        stream = torch.cuda.current_stream()
+        name = "stochastic" if stochastic else "greedy"
+        for mode in ("eager", "graph", "graph_cycle"):
+            def one(i):
+                if mode == "eager":
+                    for c in calls[i % pool]:
+                        c()
+                elif mode == "graph":
+                    graphs[i % pool].replay()
+                elif i % pool == 0:
+                    cycle.replay()
+            n = steps - steps % pool
+            for i in range(2 * pool):
+                one(i)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(n):
+                one(i)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            out[f"{name}_step_us_{mode}"] = e0.elapsed_time(e1) * 1e3 / n
+        out["pool_mb"] = round(sum(sum(t.numel() * t.element_size() for t in e[2:] if t is not None)
+                                   for e in entries) / 1e6, 1)
+        del graphs, cycle, calls, entries
     return out
 
 
