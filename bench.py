@@ -338,7 +338,7 @@ def run_native(args, rank, world, local):
         "e2e": {"value": e2e_rows / (e2e_ms * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d // max(E, 1), "d2h_bytes_per_step": d2h // max(E, 1),
                 "steps": E},
-        "gpu_launches": K * st.LAUNCHES_PER_STEP,
+        "gpu_launches": K * st.launches_per_step,
         "clocks": clk,
         "latency_b1": latency,
     }
@@ -352,7 +352,7 @@ def latency_leg(dev, steps, pool=64):
     from speculative_decoding_ragged_gb300 import synth
     from speculative_decoding_ragged_gb300.step import DSparkGraph, DSparkStep
     wl = synth.WORKLOADS["latency_b1"]
-    out = {"steps": steps, "pool_blocks": pool, "launches_per_step": DSparkStep.LAUNCHES_PER_STEP}
+    out = {"steps": steps, "pool_blocks": pool}
     for stochastic in (False, True):
         st = DSparkStep(wl.B, wl.gamma, wl.V, wl.tiers, wl.bias, wl.alpha_slope * np.arange(2),
                         wl.theta_slope * np.arange(wl.gamma + 1), out_cap=16,
@@ -376,6 +376,7 @@ def latency_leg(dev, steps, pool=64):
                     c()
         stream = torch.cuda.current_stream()
         name = "stochastic" if stochastic else "greedy"
+        out[f"{name}_launches_per_step"] = st.launches_per_step
         for mode in ("eager", "graph", "graph_cycle"):
             def one(i):
                 if mode == "eager":

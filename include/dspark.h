@@ -208,6 +208,31 @@ int dspark_scatter(const int32_t* committed, const int32_t* accept_len, int B, i
                    cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * dspark_observe — calibration and utilisation counters ("A2 method details", observability:
+ * per-request confidence and calibration metrics such as ECE; cap-accept recovers the
+ * acceptance ceiling that truncation hides, and utilisation is committed over ceiling).
+ *
+ * c_b = clamp(ceiling_len[b], 1, gamma) is request b's accept length over the full block (the
+ * ceiling_len of a CAP_ACCEPT or STATIC verify). Draft j (0-based: the draft d_{j+1} scored by
+ * conf[b, j]) is observed when j <= c_b - 1 and j <= gamma - 2: accepted (1) if j < c_b - 1,
+ * rejected (0) if j == c_b - 1; later drafts are censored. Each observed draft, with
+ * x = clamp(conf[b, j], 0, 1) (NaN counts as 0), adds to bin k = min(n_bins - 1, floor(x * n_bins))
+ *   hist[3k] += 1,  hist[3k + 1] += round_to_nearest_even(x * 2^32),  hist[3k + 2] += outcome
+ * and util[0] += clamp(accept_len[b], 0, gamma), util[1] += c_b. All counters are uint64 and
+ * exact, so the result does not depend on the order of the atomic additions. Expected
+ * calibration error = sum_k (hist[3k]/N) |hist[3k+2]/hist[3k] - hist[3k+1]/(2^32 hist[3k])|,
+ * utilisation = util[0] / util[1]. Counters accumulate across calls; the caller zeroes them.
+ * Out-of-range ceiling_len / accept_len are clamped and flag DSPARK_STATUS_BAD_LENGTH.
+ *
+ * conf [B, gamma-1] fp32; accept_len, ceiling_len [B] int32; hist [3 * n_bins] uint64 in/out;
+ * util [2] uint64 in/out; status [1] int32 in/out or NULL.
+ * Limits: B >= 0, 1 <= gamma <= DSPARK_MAX_GAMMA, 1 <= n_bins <= 1024.
+ * ------------------------------------------------------------------------------------- */
+int dspark_observe(const float* conf, const int32_t* accept_len, const int32_t* ceiling_len,
+                   int B, int gamma, int n_bins, uint64_t* hist, uint64_t* util,
+                   int32_t* status, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------------
  * dspark_verify_noalloc — the pages have no counterpart to this entry point; it exists for
  * callers that cannot hand the library scratch memory. Some hosts give a kernel library only
  * its input and output buffers (a plugin interface with no workspace argument), and some

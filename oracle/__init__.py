@@ -70,6 +70,8 @@ def _lib():
             lib.oracle_verify.restype = ctypes.c_int
             lib.oracle_scatter.argtypes = [_p, _p, _i32, _i32, _p, _p, _i32, _p]
             lib.oracle_scatter.restype = ctypes.c_int
+            lib.oracle_observe.argtypes = [_p, _p, _p, _i32, _i32, _i32, _p, _p, _p]
+            lib.oracle_observe.restype = ctypes.c_int
             _LIB = lib
     return _LIB
 
@@ -212,3 +214,20 @@ def scatter(committed, accept_len, out_tokens, out_len) -> dict:
     if rc != 0:
         raise ValueError("oracle_scatter: invalid arguments")
     return dict(out_tokens=out_tokens, out_len=out_len, status=int(status[0]))
+
+
+def observe(conf, accept_len, ceiling_len, n_bins, hist=None, util=None) -> dict:
+    """Calibration histogram [n_bins, 3] and utilisation counters [2], accumulated."""
+    conf = _c(conf, np.float32)
+    accept_len = _c(accept_len, np.int32)
+    ceiling_len = _c(ceiling_len, np.int32)
+    B = accept_len.size
+    gamma = (conf.shape[1] + 1) if conf.ndim == 2 else 1
+    hist = np.zeros((n_bins, 3), np.uint64) if hist is None else _c(hist, np.uint64).copy()
+    util = np.zeros(2, np.uint64) if util is None else _c(util, np.uint64).copy()
+    status = np.zeros(1, np.int32)
+    rc = _lib().oracle_observe(_ptr(conf), _ptr(accept_len), _ptr(ceiling_len), B, gamma,
+                               int(n_bins), _ptr(hist), _ptr(util), _ptr(status))
+    if rc != 0:
+        raise ValueError("oracle_observe: invalid arguments")
+    return dict(hist=hist, util=util, status=int(status[0]))

@@ -495,3 +495,39 @@ int oracle_scatter(const int32_t* committed, const int32_t* accept_len, int B, i
     if (status) *status |= st;
     return 0;
 }
+
+/* ------------------------------------------------------------------------------------------
+ * Observability counters. "DSpark in SGLang", A2 observability: per-request confidence and
+ * calibration metrics (ECE) are reported for post-hoc analysis, and cap-accept exposes the
+ * acceptance ceiling that truncation hides (utilisation = committed over ceiling).
+ * READING: a draft's outcome is observed up to and including the first rejection of the full
+ * block (the ceiling); later drafts are censored. Confidence sums are kept in 2^-32 fixed point
+ * so every counter is an exact integer.
+ * hist [n_bins][3] = (count, sum of rint(x * 2^32), accepted); util [2] = (committed, ceiling).
+ * ---------------------------------------------------------------------------------------- */
+int oracle_observe(const float* conf, const int32_t* accept_len, const int32_t* ceiling_len,
+                   int B, int gamma, int n_bins, uint64_t* hist, uint64_t* util, int32_t* status)
+{
+    if (B < 0 || gamma < 1 || n_bins < 1) return -1;
+    const int L = gamma - 1;
+    int32_t st = 0;
+    for (int b = 0; b < B; ++b) {
+        int c = ceiling_len[b];
+        if (c < 1 || c > gamma) { st |= OR_BAD_LENGTH; c = c < 1 ? 1 : gamma; }
+        int a = accept_len[b];
+        if (a < 0 || a > gamma) { st |= OR_BAD_LENGTH; a = a < 0 ? 0 : gamma; }
+        util[0] += (uint64_t)a;
+        util[1] += (uint64_t)c;
+        for (int j = 0; j < L && j <= c - 1; ++j) {
+            const float x = clamp_conf(conf[(size_t)b * L + j]);
+            int k = (int)(x * (float)n_bins);
+            if (k > n_bins - 1) k = n_bins - 1;
+            const uint64_t fx = x >= 1.0f ? (1ULL << 32) : (uint64_t)llrintf(x * 4294967296.0f);
+            hist[3 * k + 0] += 1;
+            hist[3 * k + 1] += fx;
+            if (j < c - 1) hist[3 * k + 2] += 1;
+        }
+    }
+    if (status) *status |= st;
+    return 0;
+}

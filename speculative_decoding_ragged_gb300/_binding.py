@@ -61,6 +61,7 @@ SYMBOLS = {
     "dspark_scatter": ([_p, _p, _i, _i, _p, _p, _i, _p, _p], _i),
     "dspark_verify_noalloc": ([_i, _i, _p, _i, _p, _i, _i, _p, _p, _p, _i, _i, ctypes.c_float,
                                _u64, _u64, _p, _p, _p, _p, _p, _p], _i),
+    "dspark_observe": ([_p, _p, _p, _i, _i, _i, _p, _p, _p, _p], _i),
     "dspark_last_error": ([], ctypes.c_char_p),
     "dspark_version": ([], _i),
 }
@@ -253,6 +254,44 @@ def dspark_scatter(committed: torch.Tensor, accept_len: torch.Tensor, out_tokens
         _ptr(out_len, "out_len", torch.int32, min_numel=B, required=B > 0), cap,
         _ptr(status, "status", torch.int32, min_numel=1, required=False), _stream(stream))
     return _call("dspark_scatter", args, prepare)
+
+
+def dspark_observe(conf: torch.Tensor, accept_len: torch.Tensor, ceiling_len: torch.Tensor,
+                   hist: torch.Tensor, util: torch.Tensor, status: Optional[torch.Tensor] = None,
+                   stream=None, prepare: bool = False):
+    """Accumulate calibration counters (hist: int64 [n_bins, 3]) and utilisation counters
+    (util: int64 [2]) on the device; see ece() and utilisation() for the derived metrics."""
+    B = accept_len.numel()
+    L = conf.shape[-1] if conf.dim() == 2 else 0
+    n_bins = hist.numel() // 3
+    if hist.numel() != 3 * n_bins or n_bins < 1:
+        raise ValueError("hist must hold 3 counters per bin")
+    args = (_ptr(conf, "conf", torch.float32, numel=B * L, required=B > 0 and L > 0),
+            _ptr(accept_len, "accept_len", torch.int32, required=B > 0),
+            _ptr(ceiling_len, "ceiling_len", torch.int32, numel=B, required=B > 0), B, L + 1,
+            n_bins, _ptr(hist, "hist", torch.int64), _ptr(util, "util", torch.int64, numel=2),
+            _ptr(status, "status", torch.int32, min_numel=1, required=False), _stream(stream))
+    return _call("dspark_observe", args, prepare)
+
+
+def ece(hist) -> float:
+    """Expected calibration error from dspark_observe's counters (n_bins x 3, host array)."""
+    import numpy as np
+    h = np.asarray(hist, dtype=np.float64).reshape(-1, 3)
+    n = h[:, 0]
+    N = n.sum()
+    if N == 0:
+        return 0.0
+    nz = n > 0
+    conf = h[nz, 1] / 4294967296.0 / n[nz]
+    acc = h[nz, 2] / n[nz]
+    return float((n[nz] / N * np.abs(acc - conf)).sum())
+
+
+def utilisation(util) -> float:
+    """Committed tokens over the acceptance ceiling, from dspark_observe's counters."""
+    c, ceil = int(util[0]), int(util[1])
+    return c / ceil if ceil else 0.0
 
 
 NOALLOC_SCRATCH_BYTES = 4 << 20

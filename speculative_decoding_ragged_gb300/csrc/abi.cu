@@ -213,6 +213,23 @@ int dspark_scatter(const int32_t* committed, const int32_t* accept_len, int B, i
                                   status, stream);
 }
 
+int dspark_observe(const float* conf, const int32_t* accept_len, const int32_t* ceiling_len,
+                   int B, int gamma, int n_bins, uint64_t* hist, uint64_t* util,
+                   int32_t* status, cudaStream_t stream)
+{
+    if (B < 0 || gamma < 1 || gamma > DSPARK_MAX_GAMMA || n_bins < 1 || n_bins > 1024)
+        return fail(DSPARK_ERR_INVALID_ARG, "dspark_observe: bad sizes B=%d gamma=%d n_bins=%d",
+                    B, gamma, n_bins);
+    if (B == 0) return DSPARK_OK;
+    if ((conf == nullptr && gamma > 1) || accept_len == nullptr || ceiling_len == nullptr ||
+        hist == nullptr || util == nullptr ||
+        (reinterpret_cast<uintptr_t>(hist) & 7u) != 0 || (reinterpret_cast<uintptr_t>(util) & 7u) != 0)
+        return fail(DSPARK_ERR_INVALID_ARG,
+                    "dspark_observe: conf, lengths and 8-byte aligned counters are required");
+    return dspark::launch_observe(conf, accept_len, ceiling_len, B, gamma, n_bins, hist, util,
+                                  status, stream);
+}
+
 const char* dspark_last_error(void) { return dspark::last_error(); }
 
 int dspark_version(void) { return 100; }

@@ -60,6 +60,9 @@ int launch_verify(const VerifyCall& c, cudaStream_t stream);
 int launch_scatter(const int32_t* committed, const int32_t* accept_len, int B, int gamma,
                    int32_t* out_tokens, int32_t* out_len, int out_cap, int32_t* status,
                    cudaStream_t stream);
+int launch_observe(const float* conf, const int32_t* accept_len, const int32_t* ceiling_len,
+                   int B, int gamma, int n_bins, uint64_t* hist, uint64_t* util, int32_t* status,
+                   cudaStream_t stream);
 
 // Launch with programmatic dependent launch allowed: the grid may start while the previous
 // kernel on the stream finishes; every kernel of this library begins with pdl_wait(), which

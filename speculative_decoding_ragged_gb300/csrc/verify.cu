@@ -36,9 +36,12 @@ constexpr int kStreamWarps = kStreamThreads / 32;
 #define DSPARK_UNROLL 8
 #endif
 constexpr int kUnroll = DSPARK_UNROLL;  // 16-byte loads in flight per lane
-constexpr int kFinalThreadsGreedy = 256;
-constexpr int kFinalThreadsStoch = 512;   // the bonus pass streams one or two rows per request
+constexpr int kFinalThreads = 256;
+constexpr int kFinalWarps = kFinalThreads / 32;
 constexpr int kBonusGroup = 4;            // tiles a warp loads before reducing them
+constexpr int kTileThreads = 256;
+constexpr int kTilesPerCta = (kTileThreads / 32) * kBonusGroup;
+constexpr int kPickThreads = 256;
 constexpr int kTargetUnits = 4096;    // aim: about one unit per resident warp
 #ifndef DSPARK_MAX_CHUNK
 #define DSPARK_MAX_CHUNK 4096
@@ -376,6 +379,17 @@ __device__ __forceinline__ void philox4x64_10(uint64_t c0, uint64_t c1, uint64_t
     out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
 }
 
+// The bonus draw of one request, decided by the finaliser and carried out by the tile and
+// pick kernels (stochastic verify).
+struct BonusJob {
+    int64_t trow;   // target row of the bonus position
+    int64_t drow;   // draft row of a residual draw; -1 for a draw from p
+    float mp, izp;  // target row maximum and 1/Z
+    float mq, izq;  // draft row maximum and 1/Z (residual draws)
+    double u;       // the position's bonus uniform u'
+    int64_t slot;   // committed[] index that receives the bonus; -1: no draw
+};
+
 struct FinalArgs {
     const void* target;
     const void* draft;
@@ -389,12 +403,12 @@ struct FinalArgs {
     int32_t* ceiling;
     float* row_prob;
     int32_t* status;
+    BonusJob* jobs;   // [B] (stochastic)
+    float* tiles;     // [B][n_tiles][2]: residual and p weight sums per 256-token tile
     uint64_t seed, step;
-    int mode, V, nc, vec, B, gamma, target_rows;
+    int mode, V, nc, vec, B, gamma, target_rows, n_tiles;
     int64_t rows_max;
-    float s;        // log2(e) / temperature
-    double inv_t;   // 1 / temperature
-    double temp;    // temperature
+    float s;          // log2(e) / temperature
 };
 
 // Eight consecutive logits [v0, v0+8) of a row as fp32; positions >= V read as -inf.
@@ -460,38 +474,74 @@ __device__ __forceinline__ float sum8(const float (&w)[8])
 
 // Combined softmax statistics of one row from its nc chunk partials, by one warp, in a fixed
 // order (lane-strided, then a fixed shuffle tree): deterministic for a given nc.
+// Combined softmax statistics of one row from its nc chunk partials, by one warp: each lane
+// folds chunks lane, lane+32, ... in order (eight loads in flight at a time) with an online
+// rescale, then the lanes combine over a fixed shuffle tree — deterministic for a given nc.
 __device__ __forceinline__ void combine_soft(const SoftPart* parts, int nc, float s, int lane,
                                              float& m_out, float& z_out)
 {
-    float m = -INFINITY;
-    for (int c = lane; c < nc; c += 32) m = fmaxf(m, parts[c].m);
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    float z = 0.0f;
-    if (m != -INFINITY) {
-        for (int c = lane; c < nc; c += 32) {
-            const SoftPart p = parts[c];
-            if (p.m != -INFINITY) z += p.z * ex2_approx((p.m - m) * s);
+    float m = -INFINITY, z = 0.0f;
+    for (int c0 = lane; c0 < nc; c0 += 32 * 8) {
+        SoftPart p[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int c = c0 + 32 * k;
+            if (c < nc) p[k] = parts[c];
+            else { p[k].m = -INFINITY; p[k].z = 0.0f; }
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            if (p[k].m == -INFINITY) continue;
+            if (p[k].m > m) {
+                z *= ex2_approx((m - p[k].m) * s);
+                m = p[k].m;
+            }
+            z += p[k].z * ex2_approx((p[k].m - m) * s);
         }
     }
-    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-    m_out = m;
-    z_out = z;
+    float M = m;
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float zz = m != -INFINITY ? z * ex2_approx((m - M) * s) : 0.0f;
+    for (int off = 16; off > 0; off >>= 1) zz += __shfl_xor_sync(0xffffffffu, zz, off);
+    m_out = M;
+    z_out = zz;
+}
+
+// Combined argmax of one row from its nc chunk partials (exact; eight loads in flight).
+__device__ __forceinline__ int combine_arg(const ArgPart* parts, int nc, int lane)
+{
+    float v = -INFINITY;
+    int idx = 0x7FFFFFFF;
+    for (int c0 = lane; c0 < nc; c0 += 32 * 8) {
+        ArgPart p[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int c = c0 + 32 * k;
+            if (c < nc) p[k] = parts[c];
+            else { p[k].v = -INFINITY; p[k].idx = 0x7FFFFFFF; }
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) arg_merge(v, idx, p[k].v, p[k].idx);
+    }
+    for (int off = 16; off > 0; off >>= 1) {
+        const float v2 = __shfl_xor_sync(0xffffffffu, v, off);
+        const int i2 = __shfl_xor_sync(0xffffffffu, idx, off);
+        arg_merge(v, idx, v2, i2);
+    }
+    return idx == 0x7FFFFFFF ? 0 : idx;   // a row of -inf only: index 0
 }
 
 template <int DT, bool STOCH>
-__global__ void __launch_bounds__(STOCH ? kFinalThreadsStoch : kFinalThreadsGreedy)
+__global__ void __launch_bounds__(kFinalThreads)
 verify_finalize_kernel(FinalArgs A)
 {
-    constexpr int kFinalThreads = STOCH ? kFinalThreadsStoch : kFinalThreadsGreedy;
-    constexpr int kFinalWarps = kFinalThreads / 32;
     constexpr int E = (DT == DSPARK_BF16) ? 2 : 4;
-    extern __shared__ double tile_sum[];      // stochastic bonus: one entry per 256-token tile
     __shared__ int g_s[DSPARK_MAX_GAMMA];
     __shared__ float mp_s[DSPARK_MAX_GAMMA], mq_s[DSPARK_MAX_GAMMA];
     __shared__ float zp_s[DSPARK_MAX_GAMMA], zq_s[DSPARK_MAX_GAMMA];
     __shared__ double ub_s[DSPARK_MAX_GAMMA];
     __shared__ int acc_s[DSPARK_MAX_GAMMA];
-    __shared__ int walk_s[4];                 // Lc, Lf (then: done marker), pos, rejected
+    __shared__ int walk_s[4];                 // Lc, Lf, pos, rejected
 
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
@@ -524,6 +574,11 @@ verify_finalize_kernel(FinalArgs A)
             A.accept_len[b] = 0;
             if (A.ceiling) A.ceiling[b] = (A.mode == DSPARK_COMPACT) ? -1 : 0;
             raise_status(A.status, bits | DSPARK_STATUS_BAD_ROWS);
+            if (STOCH) {
+                BonusJob job = {};
+                job.slot = -1;
+                A.jobs[b] = job;
+            }
         }
         return;
     }
@@ -533,19 +588,8 @@ verify_finalize_kernel(FinalArgs A)
     for (int i = warp; i < nrows; i += kFinalWarps) {
         const int64_t r = base + i;
         if (!STOCH) {
-            const ArgPart* parts = static_cast<const ArgPart*>(A.part_t) + r * A.nc;
-            float v = -INFINITY;
-            int idx = 0x7FFFFFFF;
-            for (int c = lane; c < A.nc; c += 32) {
-                const ArgPart p = parts[c];
-                arg_merge(v, idx, p.v, p.idx);
-            }
-            for (int off = 16; off > 0; off >>= 1) {
-                const float v2 = __shfl_xor_sync(0xffffffffu, v, off);
-                const int i2 = __shfl_xor_sync(0xffffffffu, idx, off);
-                arg_merge(v, idx, v2, i2);
-            }
-            if (lane == 0) g_s[i] = idx == 0x7FFFFFFF ? 0 : idx;   // all -inf: index 0
+            const int g = combine_arg(static_cast<const ArgPart*>(A.part_t) + r * A.nc, A.nc, lane);
+            if (lane == 0) g_s[i] = g;
         } else {
             float m, z;
             combine_soft(static_cast<const SoftPart*>(A.part_t) + r * A.nc, A.nc, A.s, lane, m, z);
@@ -628,122 +672,21 @@ verify_finalize_kernel(FinalArgs A)
     if (STOCH) {
         for (int k = tid; k < gamma; k += kFinalThreads)
             out[k] = (k < Lc - 1) ? A.tokens[static_cast<int64_t>(b) * gamma + k + 1] : -1;
-
-        // 4. bonus: inverse CDF over the residual of row pos (after a rejection) or over p of
-        //    row pos (after full acceptance); 256-token tiles, one warp per tile. A residual
-        //    that sums to zero (only rounding can do that) falls back to p.
-        const int pos = walk_s[2];
-        const char* trow = static_cast<const char*>(A.target) + (base + pos) * A.V * E;
-        const char* drow = static_cast<const char*>(A.draft) + (static_cast<int64_t>(b) * L + pos) * A.V * E;
-        const float mp = mp_s[pos];
-        const float izp = 1.0f / zp_s[pos];
-        const int n_tiles = (A.V + 255) / 256;
-        for (int attempt = 0; attempt < 2; ++attempt) {
-            const bool residual = walk_s[3] != 0 && attempt == 0;
-            const float mq = residual ? mq_s[pos] : 0.0f;
-            const float izq = residual ? 1.0f / zq_s[pos] : 0.0f;
-            // each warp loads kBonusGroup tiles, then weighs and sums them: a few global
-            // round trips per row instead of one per tile
-            for (int t0 = warp; t0 < n_tiles; t0 += kBonusGroup * kFinalWarps) {
-                float xp[kBonusGroup][8], xq[kBonusGroup][8];
-#pragma unroll
-                for (int g = 0; g < kBonusGroup; ++g) {
-                    const int v0 = (t0 + g * kFinalWarps) * 256 + lane * 8;
-                    load8<DT>(trow, v0, A.V, A.vec, xp[g]);
-                    if (residual) load8<DT>(drow, v0, A.V, A.vec, xq[g]);
-                }
-#pragma unroll
-                for (int g = 0; g < kBonusGroup; ++g) {
-                    const int t = t0 + g * kFinalWarps;
-                    float wv[8];
-                    bonus_weights_of<DT>(xp[g], xq[g], t * 256 + lane * 8, A.V, residual, mp, izp,
-                                         mq, izq, A.s, wv);
-                    float ts = sum8(wv);
-                    for (int off = 16; off > 0; off >>= 1) ts += __shfl_xor_sync(0xffffffffu, ts, off);
-                    if (lane == 0 && t < n_tiles) tile_sum[t] = static_cast<double>(ts);
-                }
-            }
-            __syncthreads();
-            if (warp == 0) {
-                // lane-contiguous groups of tiles, inclusive scan over lanes
-                const int per = (n_tiles + 31) / 32;
-                const int t0 = lane * per;
-                const int t1 = min(t0 + per, n_tiles);
-                double own = 0.0;
-                for (int t = t0; t < t1; ++t) own += tile_sum[t];
-                double incl = own;
-                for (int off = 1; off < 32; off <<= 1) {
-                    const double v = __shfl_up_sync(0xffffffffu, incl, off);
-                    if (lane >= off) incl += v;
-                }
-                const double R = __shfl_sync(0xffffffffu, incl, 31);
-                if (residual && !(R > 0.0)) {
-                    if (lane == 0) walk_s[3] = 0;       // retry with p
-                } else {
-                    const double thr = ub_s[pos] * R;
-                    const unsigned hit = __ballot_sync(0xffffffffu, incl > thr);
-                    int tile;
-                    double before;
-                    if (hit) {
-                        const int src = __ffs(hit) - 1;
-                        tile = -1;
-                        before = 0.0;
-                        if (lane == src) {
-                            double cum = incl - own;
-                            for (int t = t0; t < t1; ++t) {
-                                if (cum + tile_sum[t] > thr) { tile = t; break; }
-                                cum += tile_sum[t];
-                            }
-                            if (tile < 0) { tile = t1 - 1; cum -= tile_sum[tile]; }
-                            before = cum;
-                        }
-                        tile = __shfl_sync(0xffffffffu, tile, src);
-                        before = __shfl_sync(0xffffffffu, before, src);
-                    } else {
-                        tile = n_tiles - 1;          // rounding left no crossing
-                        before = R - tile_sum[tile];
-                    }
-                    // inside the tile: lane sums, inclusive scan, then the lane's 8 tokens
-                    float wv[8];
-                    bonus_weights<DT>(trow, drow, tile * 256 + lane * 8, A.V, A.vec, residual, mp,
-                                      izp, mq, izq, A.s, wv);
-                    const double own8 = static_cast<double>(sum8(wv));
-                    double inc8 = own8;
-                    for (int off = 1; off < 32; off <<= 1) {
-                        const double v = __shfl_up_sync(0xffffffffu, inc8, off);
-                        if (lane >= off) inc8 += v;
-                    }
-                    const unsigned hit8 = __ballot_sync(0xffffffffu, before + inc8 > thr);
-                    int chosen = -1;
-                    if (hit8) {
-                        const int src = __ffs(hit8) - 1;
-                        if (lane == src) {
-                            double cum = before + inc8 - own8;
-                            for (int e = 0; e < 8; ++e) {
-                                cum += static_cast<double>(wv[e]);
-                                if (cum > thr) { chosen = tile * 256 + lane * 8 + e; break; }
-                            }
-                        }
-                        chosen = __shfl_sync(0xffffffffu, chosen, src);
-                    }
-                    if (chosen < 0) {
-                        // rounding fallback: the tile's last token with positive weight
-                        int cand = -1;
-                        for (int e = 7; e >= 0; --e)
-                            if (wv[e] > 0.0f) { cand = tile * 256 + lane * 8 + e; break; }
-                        for (int off = 16; off > 0; off >>= 1)
-                            cand = max(cand, __shfl_xor_sync(0xffffffffu, cand, off));
-                        chosen = cand >= 0 ? cand : min(tile * 256, A.V - 1);
-                    }
-                    if (lane == 0) {
-                        out[Lc - 1] = chosen;
-                        walk_s[3] = 0;
-                        walk_s[1] = -1;                 // done marker
-                    }
-                }
-            }
-            __syncthreads();
-            if (walk_s[1] == -1) break;
+        // 4. the bonus draw: the residual of the rejecting position, or p of the last verified
+        //    position after full acceptance; carried out by the tile and pick kernels
+        if (tid == 0) {
+            const int pos = Lc - 1;
+            const bool residual = pos < w - 1;
+            BonusJob job;
+            job.trow = base + pos;
+            job.drow = residual ? static_cast<int64_t>(b) * L + pos : -1;
+            job.mp = mp_s[pos];
+            job.izp = 1.0f / zp_s[pos];
+            job.mq = residual ? mq_s[pos] : 0.0f;
+            job.izq = residual ? 1.0f / zq_s[pos] : 0.0f;
+            job.u = ub_s[pos];
+            job.slot = static_cast<int64_t>(b) * gamma + Lc - 1;
+            A.jobs[b] = job;
         }
     }
     // status bits of the CTA
@@ -755,9 +698,172 @@ verify_finalize_kernel(FinalArgs A)
     }
 }
 
+// Stochastic bonus, step 1: weight sums of every 256-token tile of each request's bonus row(s),
+// spread over the whole grid (kTilesPerCta tiles per CTA, kBonusGroup per warp, all loads of a
+// warp issued before its exponentials). A residual draw also records p's sums, for the rare
+// fallback to p when rounding leaves a residual of zero.
+template <int DT>
+__global__ void __launch_bounds__(kTileThreads)
+bonus_tiles_kernel(FinalArgs A, int ctas_per_request)
+{
+    constexpr int E = (DT == DSPARK_BF16) ? 2 : 4;
+    pdl_wait_and_trigger();
+    const int b = blockIdx.x / ctas_per_request;
+    const int cta = blockIdx.x - b * ctas_per_request;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const BonusJob job = A.jobs[b];
+    if (job.slot < 0) return;
+    const bool residual = job.drow >= 0;
+    const char* trow = static_cast<const char*>(A.target) + job.trow * A.V * E;
+    const char* drow = static_cast<const char*>(A.draft) + (residual ? job.drow : 0) * A.V * E;
+    const int t0 = cta * kTilesPerCta + warp * kBonusGroup;
+    float xp[kBonusGroup][8], xq[kBonusGroup][8];
+#pragma unroll
+    for (int g = 0; g < kBonusGroup; ++g) {
+        const int v0 = (t0 + g) * 256 + lane * 8;
+        load8<DT>(trow, v0, A.V, A.vec, xp[g]);
+        if (residual) load8<DT>(drow, v0, A.V, A.vec, xq[g]);
+    }
+    float* out = A.tiles + static_cast<int64_t>(b) * A.n_tiles * 2;
+#pragma unroll
+    for (int g = 0; g < kBonusGroup; ++g) {
+        const int t = t0 + g;
+        const int v0 = t * 256 + lane * 8;
+        float wr[8], wp[8];
+        bonus_weights_of<DT>(xp[g], xq[g], v0, A.V, false, job.mp, job.izp, 0.0f, 0.0f, A.s, wp);
+        float sp = sum8(wp);
+        float sr = sp;
+        if (residual) {
+            bonus_weights_of<DT>(xp[g], xq[g], v0, A.V, true, job.mp, job.izp, job.mq, job.izq,
+                                 A.s, wr);
+            sr = sum8(wr);
+        }
+        for (int off = 16; off > 0; off >>= 1) {
+            sp += __shfl_xor_sync(0xffffffffu, sp, off);
+            sr += __shfl_xor_sync(0xffffffffu, sr, off);
+        }
+        if (lane == 0 && t < A.n_tiles) {
+            out[2 * t] = sr;
+            out[2 * t + 1] = sp;
+        }
+    }
+}
+
+// Stochastic bonus, step 2, one CTA per request: a block scan of the tile sums (fp64 running
+// sums) finds the tile where the running sum first exceeds u' * R; one warp then walks that
+// tile's tokens in order. The token is the smallest v whose running weight sum exceeds u' * R;
+// a residual summing to zero falls back to p; rounding that leaves no crossing takes the last
+// token with positive weight in the last candidate tile.
+template <int DT>
+__global__ void __launch_bounds__(kPickThreads)
+bonus_pick_kernel(FinalArgs A)
+{
+    constexpr int E = (DT == DSPARK_BF16) ? 2 : 4;
+    constexpr int kWarps = kPickThreads / 32;
+    __shared__ double warp_incl[kWarps];
+    __shared__ int first_s;
+    __shared__ int tile_s;
+    __shared__ double before_s;
+    pdl_wait_and_trigger();
+    const int b = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const BonusJob job = A.jobs[b];
+    if (job.slot < 0) return;
+    const float* sums = A.tiles + static_cast<int64_t>(b) * A.n_tiles * 2;
+    const int n = A.n_tiles;
+    const int per = (n + kPickThreads - 1) / kPickThreads;
+    const int t0 = tid * per, t1 = min(t0 + per, n);
+    int col = job.drow >= 0 ? 0 : 1;                  // residual sums, or p sums
+    double own = 0.0, incl = 0.0, R = 0.0;
+    for (int attempt = 0; attempt < 2; ++attempt) {
+        own = 0.0;
+        for (int t = t0; t < t1; ++t) own += static_cast<double>(sums[2 * t + col]);
+        incl = own;
+        for (int off = 1; off < 32; off <<= 1) {
+            const double v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        if (lane == 31) warp_incl[warp] = incl;
+        __syncthreads();
+        double offset = 0.0;
+        R = 0.0;
+        for (int k = 0; k < kWarps; ++k) {
+            if (k < warp) offset += warp_incl[k];
+            R += warp_incl[k];
+        }
+        incl += offset;
+        __syncthreads();
+        if (col == 1 || R > 0.0) break;
+        col = 1;                                      // the residual vanished: draw from p
+    }
+    const double thr = job.u * R;
+    if (tid == 0) first_s = kPickThreads;
+    __syncthreads();
+    if (incl > thr && t0 < t1) atomicMin(&first_s, tid);
+    __syncthreads();
+    if (tid == first_s) {
+        double cum = incl - own;
+        int tile = -1;
+        for (int t = t0; t < t1; ++t) {
+            const double v = static_cast<double>(sums[2 * t + col]);
+            if (cum + v > thr) { tile = t; break; }
+            cum += v;
+        }
+        if (tile < 0) { tile = t1 - 1; cum -= static_cast<double>(sums[2 * tile + col]); }
+        tile_s = tile;
+        before_s = cum;
+    }
+    if (tid == 0 && first_s == kPickThreads) {       // rounding left no crossing
+        tile_s = n - 1;
+        before_s = R - static_cast<double>(sums[2 * (n - 1) + col]);
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    const int tile = tile_s;
+    const double before = before_s;
+    const bool residual = col == 0;
+    const char* trow = static_cast<const char*>(A.target) + job.trow * A.V * E;
+    const char* drow = static_cast<const char*>(A.draft) + (job.drow >= 0 ? job.drow : 0) * A.V * E;
+    float xp[8], xq[8], wv[8];
+    const int v0 = tile * 256 + lane * 8;
+    load8<DT>(trow, v0, A.V, A.vec, xp);
+    if (residual) load8<DT>(drow, v0, A.V, A.vec, xq);
+    bonus_weights_of<DT>(xp, xq, v0, A.V, residual, job.mp, job.izp, job.mq, job.izq, A.s, wv);
+    const double own8 = static_cast<double>(sum8(wv));
+    double inc8 = own8;
+    for (int off = 1; off < 32; off <<= 1) {
+        const double v = __shfl_up_sync(0xffffffffu, inc8, off);
+        if (lane >= off) inc8 += v;
+    }
+    const unsigned hit8 = __ballot_sync(0xffffffffu, before + inc8 > thr);
+    int chosen = -1;
+    if (hit8) {
+        const int src = __ffs(hit8) - 1;
+        if (lane == src) {
+            double cum = before + inc8 - own8;
+            for (int e = 0; e < 8; ++e) {
+                cum += static_cast<double>(wv[e]);
+                if (cum > thr) { chosen = v0 + e; break; }
+            }
+        }
+        chosen = __shfl_sync(0xffffffffu, chosen, src);
+    }
+    if (chosen < 0) {                                 // rounding fallback
+        int cand = -1;
+        for (int e = 7; e >= 0; --e)
+            if (wv[e] > 0.0f) { cand = v0 + e; break; }
+        for (int off = 16; off > 0; off >>= 1) cand = max(cand, __shfl_xor_sync(0xffffffffu, cand, off));
+        chosen = cand >= 0 ? cand : min(tile * 256, A.V - 1);
+    }
+    if (lane == 0) A.committed[job.slot] = chosen;
+}
+
 template <int DT, bool STOCH>
-int run_verify(const VerifyCall& c, const Plan& plan, void* part_t, void* part_d,
-               cudaStream_t stream)
+int run_verify(const VerifyCall& c, const Plan& plan, void* part_t, void* part_d, void* jobs,
+               void* tiles, cudaStream_t stream)
 {
     DeviceInfo dev;
     int rc = current_device(&dev);
@@ -773,7 +879,7 @@ int run_verify(const VerifyCall& c, const Plan& plan, void* part_t, void* part_d
     }
     const int L = c.gamma - 1;
     const double inv_t = STOCH ? 1.0 / static_cast<double>(c.temperature) : 1.0;
-    const float s = static_cast<float>(1.4426950408889634 * inv_t);
+    const float s = static_cast<float>(1.4426950408889634 * inv_t);   // log2(e) / T
 
     StreamArgs sa;
     sa.target = c.target;
@@ -832,22 +938,49 @@ int run_verify(const VerifyCall& c, const Plan& plan, void* part_t, void* part_d
     fa.target_rows = c.target_rows;
     fa.rows_max = plan.rows_max;
     fa.s = s;
-    fa.inv_t = inv_t;
-    fa.temp = static_cast<double>(c.temperature);
-    const size_t smem = STOCH ? sizeof(double) * static_cast<size_t>((c.V + 255) / 256) : 0;
-    return launch_pdl("verify (finalize)", verify_finalize_kernel<DT, STOCH>, dim3(c.B),
-                      dim3(STOCH ? kFinalThreadsStoch : kFinalThreadsGreedy), smem, stream, fa);
+    fa.jobs = static_cast<BonusJob*>(jobs);
+    fa.tiles = static_cast<float*>(tiles);
+    fa.n_tiles = (c.V + 255) / 256;
+    rc = launch_pdl("verify (finalize)", verify_finalize_kernel<DT, STOCH>, dim3(c.B),
+                    dim3(kFinalThreads), 0, stream, fa);
+    if (rc != DSPARK_OK || !STOCH) return rc;
+    const int cpr = static_cast<int>(ceil_div(fa.n_tiles, kTilesPerCta));
+    rc = launch_pdl("verify (bonus tiles)", bonus_tiles_kernel<DT>,
+                    dim3(static_cast<unsigned>(static_cast<int64_t>(c.B) * cpr)), dim3(kTileThreads),
+                    0, stream, fa, cpr);
+    if (rc != DSPARK_OK) return rc;
+    return launch_pdl("verify (bonus pick)", bonus_pick_kernel<DT>, dim3(c.B), dim3(kPickThreads),
+                      0, stream, fa);
 }
 
 }  // namespace
 
-size_t verify_workspace_bytes(int B, int gamma, int V, int stochastic)
+// Workspace layout: target-row partials; then, stochastic only, draft-row partials, the bonus
+// jobs [B] and the bonus tile sums [B][n_tiles][2].
+struct WsLayout {
+    size_t part, jobs, tiles, total;
+};
+
+WsLayout ws_layout(int B, int gamma, int V, int stochastic)
 {
-    if (B <= 0) return 0;
+    WsLayout l = {0, 0, 0, 0};
+    if (B <= 0) return l;
     const Plan plan = make_plan(V, B, gamma);
     const size_t per = stochastic ? sizeof(SoftPart) : sizeof(ArgPart);
-    const size_t one = align_up(static_cast<size_t>(plan.rows_max) * plan.nc * per, 256);
-    return stochastic ? 2 * one : one;
+    l.part = align_up(static_cast<size_t>(plan.rows_max) * plan.nc * per, 256);
+    if (!stochastic) {
+        l.total = l.part;
+        return l;
+    }
+    l.jobs = align_up(sizeof(BonusJob) * static_cast<size_t>(B), 256);
+    l.tiles = align_up(sizeof(float) * 2 * static_cast<size_t>(B) * ((V + 255) / 256), 256);
+    l.total = 2 * l.part + l.jobs + l.tiles;
+    return l;
+}
+
+size_t verify_workspace_bytes(int B, int gamma, int V, int stochastic)
+{
+    return ws_layout(B, gamma, V, stochastic).total;
 }
 
 int launch_verify(const VerifyCall& c, cudaStream_t stream)
@@ -862,13 +995,17 @@ int launch_verify(const VerifyCall& c, cudaStream_t stream)
                     c.ws_bytes, need);
     if (need > 0 && (c.ws == nullptr || reinterpret_cast<uintptr_t>(c.ws) % 16 != 0))
         return fail(DSPARK_ERR_INVALID_ARG, "dspark_verify: workspace must be a 16-byte aligned device pointer");
-    void* part_t = c.ws;
-    void* part_d = c.stochastic ? static_cast<char*>(c.ws) + need / 2 : nullptr;
+    const WsLayout lay = ws_layout(c.B, c.gamma, c.V, c.stochastic);
+    char* ws = static_cast<char*>(c.ws);
+    void* part_t = ws;
+    void* part_d = c.stochastic ? ws + lay.part : nullptr;
+    void* jobs = c.stochastic ? ws + 2 * lay.part : nullptr;
+    void* tiles = c.stochastic ? ws + 2 * lay.part + lay.jobs : nullptr;
     if (c.dtype == DSPARK_BF16)
-        return c.stochastic ? run_verify<DSPARK_BF16, true>(c, plan, part_t, part_d, stream)
-                            : run_verify<DSPARK_BF16, false>(c, plan, part_t, part_d, stream);
-    return c.stochastic ? run_verify<DSPARK_F32, true>(c, plan, part_t, part_d, stream)
-                        : run_verify<DSPARK_F32, false>(c, plan, part_t, part_d, stream);
+        return c.stochastic ? run_verify<DSPARK_BF16, true>(c, plan, part_t, part_d, jobs, tiles, stream)
+                            : run_verify<DSPARK_BF16, false>(c, plan, part_t, part_d, jobs, tiles, stream);
+    return c.stochastic ? run_verify<DSPARK_F32, true>(c, plan, part_t, part_d, jobs, tiles, stream)
+                        : run_verify<DSPARK_F32, false>(c, plan, part_t, part_d, jobs, tiles, stream);
 }
 
 }  // namespace dspark

@@ -15,7 +15,8 @@ from . import _binding as bd
 
 
 class DSparkStep:
-    LAUNCHES_PER_STEP = 5   # schedule, pack, verify (stream + finalize), scatter
+    LAUNCHES_PER_STEP = 5   # greedy: schedule, pack, verify (stream + finalize), scatter
+    LAUNCHES_PER_STEP_STOCHASTIC = 7   # + the bonus tile and pick kernels
 
     def __init__(self, B: int, gamma: int, V: int, tiers: Sequence[int], bias: float,
                  alpha, theta, *, mode: str = "compact", stochastic: bool = False,
@@ -23,6 +24,8 @@ class DSparkStep:
         self.B, self.gamma, self.V = B, gamma, V
         self.mode = mode
         self.stochastic = stochastic
+        self.launches_per_step = (self.LAUNCHES_PER_STEP_STOCHASTIC if stochastic
+                                  else self.LAUNCHES_PER_STEP)
         self.device = torch.device(device)
         dev = dict(device=self.device)
         i32 = dict(dtype=torch.int32, **dev)
