@@ -41,7 +41,7 @@ constexpr int kFinalWarps = kFinalThreads / 32;
 constexpr int kBonusGroup = 4;            // tiles a warp loads before reducing them
 constexpr int kTileThreads = 256;
 constexpr int kTilesPerCta = (kTileThreads / 32) * kBonusGroup;
-constexpr int kPickThreads = 256;
+constexpr int kPickThreads = kTileThreads;
 constexpr int kTargetUnits = 4096;    // aim: about one unit per resident warp
 #ifndef DSPARK_MAX_CHUNK
 #define DSPARK_MAX_CHUNK 4096
@@ -405,6 +405,7 @@ struct FinalArgs {
     int32_t* status;
     BonusJob* jobs;   // [B] (stochastic)
     float* tiles;     // [B][n_tiles][2]: residual and p weight sums per 256-token tile
+    unsigned* done;   // [B]: tile CTAs finished per request (zeroed by the finaliser)
     uint64_t seed, step;
     int mode, V, nc, vec, B, gamma, target_rows, n_tiles;
     int64_t rows_max;
@@ -578,6 +579,7 @@ verify_finalize_kernel(FinalArgs A)
                 BonusJob job = {};
                 job.slot = -1;
                 A.jobs[b] = job;
+                A.done[b] = 0u;
             }
         }
         return;
@@ -673,7 +675,7 @@ verify_finalize_kernel(FinalArgs A)
         for (int k = tid; k < gamma; k += kFinalThreads)
             out[k] = (k < Lc - 1) ? A.tokens[static_cast<int64_t>(b) * gamma + k + 1] : -1;
         // 4. the bonus draw: the residual of the rejecting position, or p of the last verified
-        //    position after full acceptance; carried out by the tile and pick kernels
+        //    position after full acceptance; carried out by the bonus kernel
         if (tid == 0) {
             const int pos = Lc - 1;
             const bool residual = pos < w - 1;
@@ -687,6 +689,7 @@ verify_finalize_kernel(FinalArgs A)
             job.u = ub_s[pos];
             job.slot = static_cast<int64_t>(b) * gamma + Lc - 1;
             A.jobs[b] = job;
+            A.done[b] = 0u;
         }
     }
     // status bits of the CTA
@@ -698,10 +701,117 @@ verify_finalize_kernel(FinalArgs A)
     }
 }
 
+// Stochastic bonus, step 2, by the last tile CTA of the request: a block scan of the tile sums
+// (fp64 running sums) finds the tile where the running sum first exceeds u' * R; one warp then
+// walks that tile's tokens in order. The token is the smallest v whose running weight sum
+// exceeds u' * R; a residual summing to zero falls back to p; rounding that leaves no crossing
+// takes the last token with positive weight in the last candidate tile.
+template <int DT>
+__device__ void bonus_pick(const FinalArgs& A, int b, const BonusJob& job)
+{
+    constexpr int E = (DT == DSPARK_BF16) ? 2 : 4;
+    constexpr int kWarps = kPickThreads / 32;
+    __shared__ double warp_incl[kWarps];
+    __shared__ int first_s;
+    __shared__ int tile_s;
+    __shared__ double before_s;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const float* sums = A.tiles + static_cast<int64_t>(b) * A.n_tiles * 2;
+    const int n = A.n_tiles;
+    const int per = (n + kPickThreads - 1) / kPickThreads;
+    const int t0 = tid * per, t1 = min(t0 + per, n);
+    int col = job.drow >= 0 ? 0 : 1;                  // residual sums, or p sums
+    double own = 0.0, incl = 0.0, R = 0.0;
+    for (int attempt = 0; attempt < 2; ++attempt) {
+        own = 0.0;
+        for (int t = t0; t < t1; ++t) own += static_cast<double>(__ldcg(sums + 2 * t + col));
+        incl = own;
+        for (int off = 1; off < 32; off <<= 1) {
+            const double v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        if (lane == 31) warp_incl[warp] = incl;
+        __syncthreads();
+        double offset = 0.0;
+        R = 0.0;
+        for (int k = 0; k < kWarps; ++k) {
+            if (k < warp) offset += warp_incl[k];
+            R += warp_incl[k];
+        }
+        incl += offset;
+        __syncthreads();
+        if (col == 1 || R > 0.0) break;
+        col = 1;                                      // the residual vanished: draw from p
+    }
+    const double thr = job.u * R;
+    if (tid == 0) first_s = kPickThreads;
+    __syncthreads();
+    if (incl > thr && t0 < t1) atomicMin(&first_s, tid);
+    __syncthreads();
+    if (tid == first_s) {
+        double cum = incl - own;
+        int tile = -1;
+        for (int t = t0; t < t1; ++t) {
+            const double v = static_cast<double>(__ldcg(sums + 2 * t + col));
+            if (cum + v > thr) { tile = t; break; }
+            cum += v;
+        }
+        if (tile < 0) { tile = t1 - 1; cum -= static_cast<double>(__ldcg(sums + 2 * tile + col)); }
+        tile_s = tile;
+        before_s = cum;
+    }
+    if (tid == 0 && first_s == kPickThreads) {       // rounding left no crossing
+        tile_s = n - 1;
+        before_s = R - static_cast<double>(__ldcg(sums + 2 * (n - 1) + col));
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    const int tile = tile_s;
+    const double before = before_s;
+    const bool residual = col == 0;
+    const char* trow = static_cast<const char*>(A.target) + job.trow * A.V * E;
+    const char* drow = static_cast<const char*>(A.draft) + (job.drow >= 0 ? job.drow : 0) * A.V * E;
+    float xp[8], xq[8], wv[8];
+    const int v0 = tile * 256 + lane * 8;
+    load8<DT>(trow, v0, A.V, A.vec, xp);
+    if (residual) load8<DT>(drow, v0, A.V, A.vec, xq);
+    bonus_weights_of<DT>(xp, xq, v0, A.V, residual, job.mp, job.izp, job.mq, job.izq, A.s, wv);
+    const double own8 = static_cast<double>(sum8(wv));
+    double inc8 = own8;
+    for (int off = 1; off < 32; off <<= 1) {
+        const double v = __shfl_up_sync(0xffffffffu, inc8, off);
+        if (lane >= off) inc8 += v;
+    }
+    const unsigned hit8 = __ballot_sync(0xffffffffu, before + inc8 > thr);
+    int chosen = -1;
+    if (hit8) {
+        const int src = __ffs(hit8) - 1;
+        if (lane == src) {
+            double cum = before + inc8 - own8;
+            for (int e = 0; e < 8; ++e) {
+                cum += static_cast<double>(wv[e]);
+                if (cum > thr) { chosen = v0 + e; break; }
+            }
+        }
+        chosen = __shfl_sync(0xffffffffu, chosen, src);
+    }
+    if (chosen < 0) {                                 // rounding fallback
+        int cand = -1;
+        for (int e = 7; e >= 0; --e)
+            if (wv[e] > 0.0f) { cand = v0 + e; break; }
+        for (int off = 16; off > 0; off >>= 1) cand = max(cand, __shfl_xor_sync(0xffffffffu, cand, off));
+        chosen = cand >= 0 ? cand : min(tile * 256, A.V - 1);
+    }
+    if (lane == 0) A.committed[job.slot] = chosen;
+}
+
 // Stochastic bonus, step 1: weight sums of every 256-token tile of each request's bonus row(s),
 // spread over the whole grid (kTilesPerCta tiles per CTA, kBonusGroup per warp, all loads of a
 // warp issued before its exponentials). A residual draw also records p's sums, for the rare
-// fallback to p when rounding leaves a residual of zero.
+// fallback to p when rounding leaves a residual of zero. The last of a request's CTAs to finish
+// (a per-request counter the finaliser zeroed) then performs step 2.
 template <int DT>
 __global__ void __launch_bounds__(kTileThreads)
 bonus_tiles_kernel(FinalArgs A, int ctas_per_request)
@@ -748,117 +858,16 @@ bonus_tiles_kernel(FinalArgs A, int ctas_per_request)
             out[2 * t + 1] = sp;
         }
     }
-}
-
-// Stochastic bonus, step 2, one CTA per request: a block scan of the tile sums (fp64 running
-// sums) finds the tile where the running sum first exceeds u' * R; one warp then walks that
-// tile's tokens in order. The token is the smallest v whose running weight sum exceeds u' * R;
-// a residual summing to zero falls back to p; rounding that leaves no crossing takes the last
-// token with positive weight in the last candidate tile.
-template <int DT>
-__global__ void __launch_bounds__(kPickThreads)
-bonus_pick_kernel(FinalArgs A)
-{
-    constexpr int E = (DT == DSPARK_BF16) ? 2 : 4;
-    constexpr int kWarps = kPickThreads / 32;
-    __shared__ double warp_incl[kWarps];
-    __shared__ int first_s;
-    __shared__ int tile_s;
-    __shared__ double before_s;
-    pdl_wait_and_trigger();
-    const int b = blockIdx.x;
-    const int tid = threadIdx.x;
-    const int lane = tid & 31;
-    const int warp = tid >> 5;
-    const BonusJob job = A.jobs[b];
-    if (job.slot < 0) return;
-    const float* sums = A.tiles + static_cast<int64_t>(b) * A.n_tiles * 2;
-    const int n = A.n_tiles;
-    const int per = (n + kPickThreads - 1) / kPickThreads;
-    const int t0 = tid * per, t1 = min(t0 + per, n);
-    int col = job.drow >= 0 ? 0 : 1;                  // residual sums, or p sums
-    double own = 0.0, incl = 0.0, R = 0.0;
-    for (int attempt = 0; attempt < 2; ++attempt) {
-        own = 0.0;
-        for (int t = t0; t < t1; ++t) own += static_cast<double>(sums[2 * t + col]);
-        incl = own;
-        for (int off = 1; off < 32; off <<= 1) {
-            const double v = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += v;
-        }
-        if (lane == 31) warp_incl[warp] = incl;
-        __syncthreads();
-        double offset = 0.0;
-        R = 0.0;
-        for (int k = 0; k < kWarps; ++k) {
-            if (k < warp) offset += warp_incl[k];
-            R += warp_incl[k];
-        }
-        incl += offset;
-        __syncthreads();
-        if (col == 1 || R > 0.0) break;
-        col = 1;                                      // the residual vanished: draw from p
-    }
-    const double thr = job.u * R;
-    if (tid == 0) first_s = kPickThreads;
+    // the request's last tile CTA to finish draws the token (no CTA ever waits for another)
+    __shared__ bool last_s;
+    __threadfence();
     __syncthreads();
-    if (incl > thr && t0 < t1) atomicMin(&first_s, tid);
+    if (threadIdx.x == 0)
+        last_s = atomicAdd(A.done + b, 1u) == static_cast<unsigned>(ctas_per_request) - 1;
     __syncthreads();
-    if (tid == first_s) {
-        double cum = incl - own;
-        int tile = -1;
-        for (int t = t0; t < t1; ++t) {
-            const double v = static_cast<double>(sums[2 * t + col]);
-            if (cum + v > thr) { tile = t; break; }
-            cum += v;
-        }
-        if (tile < 0) { tile = t1 - 1; cum -= static_cast<double>(sums[2 * tile + col]); }
-        tile_s = tile;
-        before_s = cum;
-    }
-    if (tid == 0 && first_s == kPickThreads) {       // rounding left no crossing
-        tile_s = n - 1;
-        before_s = R - static_cast<double>(sums[2 * (n - 1) + col]);
-    }
-    __syncthreads();
-    if (warp != 0) return;
-    const int tile = tile_s;
-    const double before = before_s;
-    const bool residual = col == 0;
-    const char* trow = static_cast<const char*>(A.target) + job.trow * A.V * E;
-    const char* drow = static_cast<const char*>(A.draft) + (job.drow >= 0 ? job.drow : 0) * A.V * E;
-    float xp[8], xq[8], wv[8];
-    const int v0 = tile * 256 + lane * 8;
-    load8<DT>(trow, v0, A.V, A.vec, xp);
-    if (residual) load8<DT>(drow, v0, A.V, A.vec, xq);
-    bonus_weights_of<DT>(xp, xq, v0, A.V, residual, job.mp, job.izp, job.mq, job.izq, A.s, wv);
-    const double own8 = static_cast<double>(sum8(wv));
-    double inc8 = own8;
-    for (int off = 1; off < 32; off <<= 1) {
-        const double v = __shfl_up_sync(0xffffffffu, inc8, off);
-        if (lane >= off) inc8 += v;
-    }
-    const unsigned hit8 = __ballot_sync(0xffffffffu, before + inc8 > thr);
-    int chosen = -1;
-    if (hit8) {
-        const int src = __ffs(hit8) - 1;
-        if (lane == src) {
-            double cum = before + inc8 - own8;
-            for (int e = 0; e < 8; ++e) {
-                cum += static_cast<double>(wv[e]);
-                if (cum > thr) { chosen = v0 + e; break; }
-            }
-        }
-        chosen = __shfl_sync(0xffffffffu, chosen, src);
-    }
-    if (chosen < 0) {                                 // rounding fallback
-        int cand = -1;
-        for (int e = 7; e >= 0; --e)
-            if (wv[e] > 0.0f) { cand = v0 + e; break; }
-        for (int off = 16; off > 0; off >>= 1) cand = max(cand, __shfl_xor_sync(0xffffffffu, cand, off));
-        chosen = cand >= 0 ? cand : min(tile * 256, A.V - 1);
-    }
-    if (lane == 0) A.committed[job.slot] = chosen;
+    if (!last_s) return;
+    __threadfence();
+    bonus_pick<DT>(A, b, job);
 }
 
 template <int DT, bool STOCH>
@@ -939,18 +948,16 @@ int run_verify(const VerifyCall& c, const Plan& plan, void* part_t, void* part_d
     fa.rows_max = plan.rows_max;
     fa.s = s;
     fa.jobs = static_cast<BonusJob*>(jobs);
+    fa.done = reinterpret_cast<unsigned*>(static_cast<BonusJob*>(jobs) + c.B);
     fa.tiles = static_cast<float*>(tiles);
     fa.n_tiles = (c.V + 255) / 256;
     rc = launch_pdl("verify (finalize)", verify_finalize_kernel<DT, STOCH>, dim3(c.B),
                     dim3(kFinalThreads), 0, stream, fa);
     if (rc != DSPARK_OK || !STOCH) return rc;
     const int cpr = static_cast<int>(ceil_div(fa.n_tiles, kTilesPerCta));
-    rc = launch_pdl("verify (bonus tiles)", bonus_tiles_kernel<DT>,
-                    dim3(static_cast<unsigned>(static_cast<int64_t>(c.B) * cpr)), dim3(kTileThreads),
-                    0, stream, fa, cpr);
-    if (rc != DSPARK_OK) return rc;
-    return launch_pdl("verify (bonus pick)", bonus_pick_kernel<DT>, dim3(c.B), dim3(kPickThreads),
-                      0, stream, fa);
+    return launch_pdl("verify (bonus)", bonus_tiles_kernel<DT>,
+                      dim3(static_cast<unsigned>(static_cast<int64_t>(c.B) * cpr)),
+                      dim3(kTileThreads), 0, stream, fa, cpr);
 }
 
 }  // namespace
@@ -972,7 +979,7 @@ WsLayout ws_layout(int B, int gamma, int V, int stochastic)
         l.total = l.part;
         return l;
     }
-    l.jobs = align_up(sizeof(BonusJob) * static_cast<size_t>(B), 256);
+    l.jobs = align_up((sizeof(BonusJob) + sizeof(unsigned)) * static_cast<size_t>(B), 256);
     l.tiles = align_up(sizeof(float) * 2 * static_cast<size_t>(B) * ((V + 255) / 256), 256);
     l.total = 2 * l.part + l.jobs + l.tiles;
     return l;

@@ -16,7 +16,7 @@ from . import _binding as bd
 
 class DSparkStep:
     LAUNCHES_PER_STEP = 5   # greedy: schedule, pack, verify (stream + finalize), scatter
-    LAUNCHES_PER_STEP_STOCHASTIC = 7   # + the bonus tile and pick kernels
+    LAUNCHES_PER_STEP_STOCHASTIC = 6   # + the bonus kernel
 
     def __init__(self, B: int, gamma: int, V: int, tiers: Sequence[int], bias: float,
                  alpha, theta, *, mode: str = "compact", stochastic: bool = False,

@@ -66,10 +66,10 @@ def test_workspace_size_is_a_function_of_sizes(lib):
     assert bd.dspark_verify_workspace_bytes(0, 8, 1000, False) == 0
     g = bd.dspark_verify_workspace_bytes(256, 8, 151936, False)
     s = bd.dspark_verify_workspace_bytes(256, 8, 151936, True)
-    # stochastic: target and draft partials (8 B each, like greedy's), 48-byte bonus jobs per
-    # request and two fp32 sums per 256-token tile per request
+    # stochastic: target and draft partials (8 B each, like greedy's), a 48-byte bonus job and
+    # a 4-byte counter per request, and two fp32 sums per 256-token tile per request
     align = lambda x: (x + 255) // 256 * 256
-    assert g > 0 and s == 2 * g + align(48 * 256) + align(8 * 256 * ((151936 + 255) // 256))
+    assert g > 0 and s == 2 * g + align(52 * 256) + align(8 * 256 * ((151936 + 255) // 256))
     assert g % 256 == 0
     assert bd.dspark_verify_workspace_bytes(-1, 8, 10, False) == 0
     assert "bad sizes" in bd.last_error()
