@@ -229,17 +229,17 @@ def run_native(args, rank, world, local):
     calls = [st.prepare(b["conf"], b["tokens"], b["packed"]) for b in batches]
 
     def step(i, ev=None):
-        sched, pack, verify, scatter = calls[i % nb]
+        # fused calls: dspark_schedule_pack, then dspark_verify_scatter (whose compact scatter
+        # runs inside the finaliser)
+        sched_pack, verify_scatter = calls[i % nb]
         if ev is not None:
             ev[0].record(stream)
-        sched()
-        pack()
+        sched_pack()
         if ev is not None:
             ev[1].record(stream)
-        verify()
+        verify_scatter()
         if ev is not None:
             ev[2].record(stream)
-        scatter()
 
     for i in range(args.warmup):
         step(i)
@@ -329,7 +329,8 @@ def run_native(args, rank, world, local):
         "verify_us": statistics.median(verify_us),
         "step_us": ms / K * 1e3,
         "events_sampled_steps": len(sampled),
-        "roofline": {"bound": "hbm", "kernel": "dspark_verify (stream + finalize)",
+        "roofline": {"bound": "hbm",
+                     "kernel": "dspark_verify_scatter (stream + finalize with scatter)",
                      "achieved": ach_gbs, "peak": peak, "peak_source": peak_kind,
                      "unit": "GB/s", "frac": ach_gbs / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": statistics.mean(verify_bytes),
@@ -347,8 +348,9 @@ def run_native(args, rank, world, local):
 def latency_leg(dev, steps, pool=64):
     """Per-step time of the batch-1 workload (B=1, gamma=16, V=129280 bf16, compact), greedy
     and stochastic (T = 0.7): `steps` consecutive steps cycling through `pool` seeded inputs
-    (the pool's logits exceed L2), launched eagerly (five kernels per step), as one CUDA graph
-    replay per step, and as one graph holding a whole pool cycle (the GPU-side step time)."""
+    (the pool's logits exceed L2), launched eagerly (the fused calls: three kernels per greedy
+    step, four per stochastic step), as one CUDA graph replay per step, and as one graph
+    holding a whole pool cycle (the GPU-side step time)."""
     from speculative_decoding_ragged_gb300 import synth
     from speculative_decoding_ragged_gb300.step import DSparkGraph, DSparkStep
     wl = synth.WORKLOADS["latency_b1"]

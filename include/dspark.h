@@ -137,6 +137,21 @@ int dspark_pack(const int32_t* windows, const int32_t* block_tokens, int B, int 
                 int32_t* meta, int32_t* status, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * dspark_schedule_pack — dspark_schedule followed by dspark_pack of the windows it writes, in
+ * one kernel ("A2 method details", performance: the step's small operations fused to cut the
+ * per-step cost; the scheduler's verify-length selection and the ragged window pack are two
+ * of the kernels the pages list). Every output (windows, k_star, cu_seqlens, packed_ids,
+ * row_req, row_pos, meta, status bits) equals what the two calls in sequence produce; the
+ * arguments mean what they mean there, with the same limits and the same errors (messages
+ * name dspark_schedule_pack). B == 0 or gamma == 1 run the two plain kernels.
+ * ------------------------------------------------------------------------------------- */
+int dspark_schedule_pack(const float* conf, int B, int gamma, const dspark_cost* cost,
+                         const int32_t* block_tokens, const int32_t* tiers, int n_tiers,
+                         int32_t* windows, int32_t* k_star, int32_t* cu_seqlens,
+                         int32_t* packed_ids, int32_t* row_req, int32_t* row_pos,
+                         int packed_cap, int32_t* meta, int32_t* status, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------------
  * dspark_verify — verify over the target logits and reduce to per-request accept lengths.
  *
  * Rows. Target row for (request b, block position i):
@@ -206,6 +221,25 @@ size_t dspark_verify_workspace_bytes(int B, int gamma, int V, int stochastic);
 int dspark_scatter(const int32_t* committed, const int32_t* accept_len, int B, int gamma,
                    int32_t* out_tokens, int32_t* out_len, int out_cap, int32_t* status,
                    cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * dspark_verify_scatter — dspark_verify followed by dspark_scatter of its committed tokens,
+ * without the scatter's own launch ("A2 method details", performance: the compact scatter is
+ * one of the fused kernels). Each request's tokens are appended by the CTA that decides them
+ * (greedy: the finaliser; stochastic: the CTA that draws the bonus token). Every output,
+ * including out_tokens, out_len and the status bits, equals what dspark_verify then
+ * dspark_scatter(committed, accept_len, B, gamma, out_tokens, out_len, out_cap) produce; the
+ * arguments, limits and errors are those two calls' (messages name dspark_verify_scatter).
+ * ------------------------------------------------------------------------------------- */
+int dspark_verify_scatter(dspark_mode mode, int stochastic,
+                          const void* target_logits, int target_rows, const void* draft_logits,
+                          dspark_dtype dtype, int V,
+                          const int32_t* cu_seqlens, const int32_t* windows,
+                          const int32_t* block_tokens, int B, int gamma, float temperature,
+                          uint64_t seed, uint64_t step, int32_t* accept_len, int32_t* committed,
+                          int32_t* ceiling_len, float* row_prob, void* workspace,
+                          size_t workspace_bytes, int32_t* out_tokens, int32_t* out_len,
+                          int out_cap, int32_t* status, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------------------
  * dspark_observe — calibration and utilisation counters ("A2 method details", observability:

@@ -59,6 +59,11 @@ SYMBOLS = {
                        _p, _p, _p, _p, _p, ctypes.c_size_t, _p, _p], _i),
     "dspark_verify_workspace_bytes": ([_i, _i, _i, _i], ctypes.c_size_t),
     "dspark_scatter": ([_p, _p, _i, _i, _p, _p, _i, _p, _p], _i),
+    "dspark_schedule_pack": ([_p, _i, _i, ctypes.POINTER(_Cost), _p, _p, _i, _p, _p, _p, _p, _p,
+                              _p, _i, _p, _p, _p], _i),
+    "dspark_verify_scatter": ([_i, _i, _p, _i, _p, _i, _i, _p, _p, _p, _i, _i, ctypes.c_float,
+                               _u64, _u64, _p, _p, _p, _p, _p, ctypes.c_size_t, _p, _p, _i, _p,
+                               _p], _i),
     "dspark_verify_noalloc": ([_i, _i, _p, _i, _p, _i, _i, _p, _p, _p, _i, _i, ctypes.c_float,
                                _u64, _u64, _p, _p, _p, _p, _p, _p], _i),
     "dspark_observe": ([_p, _p, _p, _i, _i, _i, _p, _p, _p, _p], _i),
@@ -195,6 +200,34 @@ def dspark_pack(windows: torch.Tensor, block_tokens: torch.Tensor, tiers: torch.
     return _call("dspark_pack", args, prepare)
 
 
+def dspark_schedule_pack(conf: torch.Tensor, cost: CostTable, block_tokens: torch.Tensor,
+                         tiers: torch.Tensor, windows: torch.Tensor, k_star: torch.Tensor,
+                         cu_seqlens: torch.Tensor, packed_ids: torch.Tensor, meta: torch.Tensor,
+                         row_req: Optional[torch.Tensor] = None,
+                         row_pos: Optional[torch.Tensor] = None,
+                         status: Optional[torch.Tensor] = None, stream=None,
+                         prepare: bool = False):
+    """dspark_schedule then dspark_pack of the windows it writes, in one kernel."""
+    B, gamma = block_tokens.shape
+    L = gamma - 1
+    if conf.dim() == 2 and tuple(conf.shape) != (B, L):
+        raise ValueError(f"conf must be [{B}, {L}]")
+    cap = packed_ids.numel()
+    args = (
+        _ptr(conf, "conf", torch.float32, numel=B * L, required=L > 0 and B > 0), B, gamma,
+        ctypes.byref(cost.c), _ptr(block_tokens, "block_tokens", torch.int32, required=B > 0),
+        _ptr(tiers, "tiers", torch.int32), tiers.numel(),
+        _ptr(windows, "windows", torch.int32, numel=B),
+        _ptr(k_star, "k_star", torch.int32, min_numel=1),
+        _ptr(cu_seqlens, "cu_seqlens", torch.int32, min_numel=B + 1),
+        _ptr(packed_ids, "packed_ids", torch.int32, required=cap > 0),
+        _ptr(row_req, "row_req", torch.int32, min_numel=cap, required=False),
+        _ptr(row_pos, "row_pos", torch.int32, min_numel=cap, required=False), cap,
+        _ptr(meta, "meta", torch.int32, min_numel=2),
+        _ptr(status, "status", torch.int32, min_numel=1, required=False), _stream(stream))
+    return _call("dspark_schedule_pack", args, prepare)
+
+
 def dspark_verify_workspace_bytes(B: int, gamma: int, V: int, stochastic: bool) -> int:
     return int(lib().dspark_verify_workspace_bytes(B, gamma, V, int(bool(stochastic))))
 
@@ -207,15 +240,8 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise ValueError(f"logits must be bfloat16 or float32, got {t.dtype}")
 
 
-def dspark_verify(mode, target: torch.Tensor, block_tokens: torch.Tensor,
-                  accept_len: torch.Tensor, committed: torch.Tensor, workspace: torch.Tensor, *,
-                  stochastic: bool = False, draft: Optional[torch.Tensor] = None,
-                  cu_seqlens: Optional[torch.Tensor] = None,
-                  windows: Optional[torch.Tensor] = None,
-                  ceiling_len: Optional[torch.Tensor] = None,
-                  row_prob: Optional[torch.Tensor] = None, temperature: float = 1.0,
-                  seed: int = 0, step: int = 0, status: Optional[torch.Tensor] = None,
-                  stream=None, prepare: bool = False):
+def _verify_args(mode, target, block_tokens, accept_len, committed, workspace, stochastic,
+                 draft, cu_seqlens, windows, ceiling_len, row_prob, temperature, seed, step):
     mode = MODES[mode] if isinstance(mode, str) else int(mode)
     B, gamma = block_tokens.shape
     rows, V = target.shape
@@ -225,7 +251,7 @@ def dspark_verify(mode, target: torch.Tensor, block_tokens: torch.Tensor,
             raise ValueError("draft logits must match the target's dtype and vocabulary")
         if draft.numel() != B * (gamma - 1) * V:
             raise ValueError(f"draft logits must hold B*(gamma-1) = {B * (gamma - 1)} rows")
-    args = (
+    return (
         mode, int(bool(stochastic)), _ptr(target, "target"), rows,
         _ptr(draft, "draft", required=False), dt, V,
         _ptr(cu_seqlens, "cu_seqlens", torch.int32, min_numel=B + 1, required=False),
@@ -237,9 +263,46 @@ def dspark_verify(mode, target: torch.Tensor, block_tokens: torch.Tensor,
         _ptr(ceiling_len, "ceiling_len", torch.int32, min_numel=B, required=False),
         _ptr(row_prob, "row_prob", torch.float32, min_numel=2 * rows, required=False),
         _ptr(workspace, "workspace", required=False),
-        workspace.numel() * workspace.element_size() if workspace is not None else 0,
-        _ptr(status, "status", torch.int32, min_numel=1, required=False), _stream(stream))
+        workspace.numel() * workspace.element_size() if workspace is not None else 0)
+
+
+def dspark_verify(mode, target: torch.Tensor, block_tokens: torch.Tensor,
+                  accept_len: torch.Tensor, committed: torch.Tensor, workspace: torch.Tensor, *,
+                  stochastic: bool = False, draft: Optional[torch.Tensor] = None,
+                  cu_seqlens: Optional[torch.Tensor] = None,
+                  windows: Optional[torch.Tensor] = None,
+                  ceiling_len: Optional[torch.Tensor] = None,
+                  row_prob: Optional[torch.Tensor] = None, temperature: float = 1.0,
+                  seed: int = 0, step: int = 0, status: Optional[torch.Tensor] = None,
+                  stream=None, prepare: bool = False):
+    args = _verify_args(mode, target, block_tokens, accept_len, committed, workspace,
+                        stochastic, draft, cu_seqlens, windows, ceiling_len, row_prob,
+                        temperature, seed, step)
+    args += (_ptr(status, "status", torch.int32, min_numel=1, required=False), _stream(stream))
     return _call("dspark_verify", args, prepare)
+
+
+def dspark_verify_scatter(mode, target: torch.Tensor, block_tokens: torch.Tensor,
+                          accept_len: torch.Tensor, committed: torch.Tensor,
+                          workspace: torch.Tensor, out_tokens: torch.Tensor,
+                          out_len: torch.Tensor, *, stochastic: bool = False,
+                          draft: Optional[torch.Tensor] = None,
+                          cu_seqlens: Optional[torch.Tensor] = None,
+                          windows: Optional[torch.Tensor] = None,
+                          ceiling_len: Optional[torch.Tensor] = None,
+                          row_prob: Optional[torch.Tensor] = None, temperature: float = 1.0,
+                          seed: int = 0, step: int = 0, status: Optional[torch.Tensor] = None,
+                          stream=None, prepare: bool = False):
+    """dspark_verify then dspark_scatter of its committed tokens, without the scatter launch."""
+    B = block_tokens.shape[0]
+    cap = out_tokens.shape[1] if out_tokens.dim() == 2 else 0
+    args = _verify_args(mode, target, block_tokens, accept_len, committed, workspace,
+                        stochastic, draft, cu_seqlens, windows, ceiling_len, row_prob,
+                        temperature, seed, step)
+    args += (_ptr(out_tokens, "out_tokens", torch.int32, min_numel=B * cap, required=B * cap > 0),
+             _ptr(out_len, "out_len", torch.int32, min_numel=B, required=B > 0), cap,
+             _ptr(status, "status", torch.int32, min_numel=1, required=False), _stream(stream))
+    return _call("dspark_verify_scatter", args, prepare)
 
 
 def dspark_scatter(committed: torch.Tensor, accept_len: torch.Tensor, out_tokens: torch.Tensor,

@@ -69,109 +69,118 @@ namespace {
 
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
-}  // namespace
-
-extern "C" {
-
-int dspark_schedule(const float* conf, int B, int gamma, const dspark_cost* cost,
-                    int32_t* windows, int32_t* k_star, int32_t* status, cudaStream_t stream)
+// Argument checks shared by the single and the fused entry points; `fn` names the entry
+// point in the error message.
+int check_schedule(const char* fn, const float* conf, int B, int gamma, const dspark_cost* cost,
+                   const int32_t* windows, const int32_t* k_star)
 {
     if (B < 0 || B > DSPARK_MAX_BATCH)
-        return fail(DSPARK_ERR_INVALID_ARG, "dspark_schedule: B = %d outside [0, %d]", B,
-                    DSPARK_MAX_BATCH);
+        return fail(DSPARK_ERR_INVALID_ARG, "%s: B = %d outside [0, %d]", fn, B, DSPARK_MAX_BATCH);
     if (gamma < 1 || gamma > DSPARK_MAX_GAMMA)
-        return fail(DSPARK_ERR_INVALID_ARG, "dspark_schedule: gamma = %d outside [1, %d]", gamma,
+        return fail(DSPARK_ERR_INVALID_ARG, "%s: gamma = %d outside [1, %d]", fn, gamma,
                     DSPARK_MAX_GAMMA);
     if (static_cast<int64_t>(B) * (gamma - 1) > DSPARK_MAX_CANDIDATES)
-        return fail(DSPARK_ERR_UNSUPPORTED, "dspark_schedule: B*(gamma-1) = %lld above %d",
+        return fail(DSPARK_ERR_UNSUPPORTED, "%s: B*(gamma-1) = %lld above %d", fn,
                     static_cast<long long>(B) * (gamma - 1), DSPARK_MAX_CANDIDATES);
     if (k_star == nullptr || !aligned4(k_star))
-        return fail(DSPARK_ERR_INVALID_ARG, "dspark_schedule: k_star must be a device int32 pointer");
-    if (B == 0) {
-        const cudaError_t e = cudaMemsetAsync(k_star, 0, sizeof(int32_t), stream);
-        if (e != cudaSuccess)
-            return fail(DSPARK_ERR_CUDA, "dspark_schedule: %s", cudaGetErrorString(e));
-        return DSPARK_OK;
-    }
+        return fail(DSPARK_ERR_INVALID_ARG, "%s: k_star must be a device int32 pointer", fn);
+    if (B == 0) return DSPARK_OK;
     if (cost == nullptr || cost->alpha == nullptr || cost->theta == nullptr)
-        return fail(DSPARK_ERR_INVALID_ARG, "dspark_schedule: cost table and its alpha/theta arrays are required");
+        return fail(DSPARK_ERR_INVALID_ARG, "%s: cost table and its alpha/theta arrays are required", fn);
     if (cost->alpha_len < B + 1)
-        return fail(DSPARK_ERR_INVALID_ARG, "dspark_schedule: alpha_len = %d, need >= B+1 = %d",
+        return fail(DSPARK_ERR_INVALID_ARG, "%s: alpha_len = %d, need >= B+1 = %d", fn,
                     cost->alpha_len, B + 1);
     if (static_cast<int64_t>(cost->theta_len) < static_cast<int64_t>(B) * gamma + 1)
-        return fail(DSPARK_ERR_INVALID_ARG, "dspark_schedule: theta_len = %d, need >= B*gamma+1 = %lld",
+        return fail(DSPARK_ERR_INVALID_ARG, "%s: theta_len = %d, need >= B*gamma+1 = %lld", fn,
                     cost->theta_len, static_cast<long long>(B) * gamma + 1);
     if ((conf == nullptr && gamma > 1) || windows == nullptr || !aligned4(windows))
-        return fail(DSPARK_ERR_INVALID_ARG, "dspark_schedule: conf and windows are required");
-    return dspark::launch_schedule(conf, B, gamma, cost, windows, k_star, status, stream);
+        return fail(DSPARK_ERR_INVALID_ARG, "%s: conf and windows are required", fn);
+    return DSPARK_OK;
 }
 
-int dspark_pack(const int32_t* windows, const int32_t* block_tokens, int B, int gamma,
-                const int32_t* tiers, int n_tiers, int32_t* cu_seqlens, int32_t* packed_ids,
-                int32_t* row_req, int32_t* row_pos, int packed_cap, int32_t* meta,
-                int32_t* status, cudaStream_t stream)
+int schedule_empty(const char* fn, int32_t* k_star, cudaStream_t stream)
+{
+    const cudaError_t e = cudaMemsetAsync(k_star, 0, sizeof(int32_t), stream);
+    if (e != cudaSuccess) return fail(DSPARK_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+    return DSPARK_OK;
+}
+
+int check_pack(const char* fn, const int32_t* windows, const int32_t* block_tokens, int B,
+               int gamma, const int32_t* tiers, int n_tiers, const int32_t* cu_seqlens,
+               const int32_t* packed_ids, int packed_cap, const int32_t* meta)
 {
     if (B < 0 || B > DSPARK_MAX_BATCH)
-        return fail(DSPARK_ERR_INVALID_ARG, "dspark_pack: B = %d outside [0, %d]", B,
-                    DSPARK_MAX_BATCH);
+        return fail(DSPARK_ERR_INVALID_ARG, "%s: B = %d outside [0, %d]", fn, B, DSPARK_MAX_BATCH);
     if (gamma < 1 || gamma > DSPARK_MAX_GAMMA)
-        return fail(DSPARK_ERR_INVALID_ARG, "dspark_pack: gamma = %d outside [1, %d]", gamma,
+        return fail(DSPARK_ERR_INVALID_ARG, "%s: gamma = %d outside [1, %d]", fn, gamma,
                     DSPARK_MAX_GAMMA);
     if (n_tiers < 1 || n_tiers > DSPARK_MAX_TIERS)
-        return fail(DSPARK_ERR_INVALID_ARG, "dspark_pack: n_tiers = %d outside [1, %d]", n_tiers,
+        return fail(DSPARK_ERR_INVALID_ARG, "%s: n_tiers = %d outside [1, %d]", fn, n_tiers,
                     DSPARK_MAX_TIERS);
     if (packed_cap < 0)
-        return fail(DSPARK_ERR_INVALID_ARG, "dspark_pack: packed_cap = %d is negative", packed_cap);
+        return fail(DSPARK_ERR_INVALID_ARG, "%s: packed_cap = %d is negative", fn, packed_cap);
     if (tiers == nullptr || cu_seqlens == nullptr || meta == nullptr ||
         (B > 0 && (windows == nullptr || block_tokens == nullptr)) ||
         (packed_cap > 0 && packed_ids == nullptr))
-        return fail(DSPARK_ERR_INVALID_ARG, "dspark_pack: a required pointer is NULL");
-    return dspark::launch_pack(windows, block_tokens, B, gamma, tiers, n_tiers, cu_seqlens,
-                               packed_ids, row_req, row_pos, packed_cap, meta, status, stream);
+        return fail(DSPARK_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+    return DSPARK_OK;
 }
 
-size_t dspark_verify_workspace_bytes(int B, int gamma, int V, int stochastic)
-{
-    if (B < 0 || gamma < 1 || gamma > DSPARK_MAX_GAMMA || V < 1) {
-        fail(DSPARK_ERR_INVALID_ARG, "dspark_verify_workspace_bytes: bad sizes B=%d gamma=%d V=%d",
-             B, gamma, V);
-        return 0;
-    }
-    return dspark::verify_workspace_bytes(B, gamma, V, stochastic ? 1 : 0);
-}
-
-int dspark_verify(dspark_mode mode, int stochastic, const void* target_logits, int target_rows,
-                  const void* draft_logits, dspark_dtype dtype, int V, const int32_t* cu_seqlens,
-                  const int32_t* windows, const int32_t* block_tokens, int B, int gamma,
-                  float temperature, uint64_t seed, uint64_t step, int32_t* accept_len,
-                  int32_t* committed, int32_t* ceiling_len, float* row_prob, void* workspace,
-                  size_t workspace_bytes, int32_t* status, cudaStream_t stream)
+int check_verify(const char* fn, dspark_mode mode, int stochastic, const void* target_logits,
+                 int target_rows, const void* draft_logits, dspark_dtype dtype, int V,
+                 const int32_t* cu_seqlens, const int32_t* windows, const int32_t* block_tokens,
+                 int B, int gamma, float temperature, const int32_t* accept_len,
+                 const int32_t* committed)
 {
     if (mode != DSPARK_STATIC && mode != DSPARK_COMPACT && mode != DSPARK_CAP_ACCEPT)
-        return fail(DSPARK_ERR_INVALID_ARG, "dspark_verify: unknown mode %d", static_cast<int>(mode));
+        return fail(DSPARK_ERR_INVALID_ARG, "%s: unknown mode %d", fn, static_cast<int>(mode));
     if (dtype != DSPARK_BF16 && dtype != DSPARK_F32)
-        return fail(DSPARK_ERR_INVALID_ARG, "dspark_verify: unknown dtype %d", static_cast<int>(dtype));
+        return fail(DSPARK_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, static_cast<int>(dtype));
     if (B < 0 || gamma < 1 || gamma > DSPARK_MAX_GAMMA || V < 1 || target_rows < 0)
-        return fail(DSPARK_ERR_INVALID_ARG, "dspark_verify: bad sizes B=%d gamma=%d V=%d rows=%d",
-                    B, gamma, V, target_rows);
+        return fail(DSPARK_ERR_INVALID_ARG, "%s: bad sizes B=%d gamma=%d V=%d rows=%d", fn, B,
+                    gamma, V, target_rows);
     if (static_cast<int64_t>(B) * gamma > INT32_MAX)
-        return fail(DSPARK_ERR_UNSUPPORTED, "dspark_verify: B*gamma overflows int32");
+        return fail(DSPARK_ERR_UNSUPPORTED, "%s: B*gamma overflows int32", fn);
     if (stochastic && !(temperature > 0.0f && temperature < INFINITY))
-        return fail(DSPARK_ERR_INVALID_ARG, "dspark_verify: stochastic verify needs a finite temperature > 0");
+        return fail(DSPARK_ERR_INVALID_ARG, "%s: stochastic verify needs a finite temperature > 0", fn);
     if (B == 0) return DSPARK_OK;
     if (target_logits == nullptr || block_tokens == nullptr || accept_len == nullptr ||
         committed == nullptr)
-        return fail(DSPARK_ERR_INVALID_ARG, "dspark_verify: logits, tokens, accept_len and committed are required");
+        return fail(DSPARK_ERR_INVALID_ARG, "%s: logits, tokens, accept_len and committed are required", fn);
     if (mode == DSPARK_COMPACT && cu_seqlens == nullptr)
-        return fail(DSPARK_ERR_INVALID_ARG, "dspark_verify: compact mode needs cu_seqlens");
+        return fail(DSPARK_ERR_INVALID_ARG, "%s: compact mode needs cu_seqlens", fn);
     if (mode != DSPARK_STATIC && windows == nullptr)
-        return fail(DSPARK_ERR_INVALID_ARG, "dspark_verify: compact and cap-accept modes need windows");
+        return fail(DSPARK_ERR_INVALID_ARG, "%s: compact and cap-accept modes need windows", fn);
     if (stochastic && draft_logits == nullptr && gamma > 1)
-        return fail(DSPARK_ERR_INVALID_ARG, "dspark_verify: stochastic verify needs draft logits");
+        return fail(DSPARK_ERR_INVALID_ARG, "%s: stochastic verify needs draft logits", fn);
     const size_t esz = dtype == DSPARK_BF16 ? 2 : 4;
     if ((reinterpret_cast<uintptr_t>(target_logits) % esz) != 0 ||
         (draft_logits != nullptr && (reinterpret_cast<uintptr_t>(draft_logits) % esz) != 0))
-        return fail(DSPARK_ERR_INVALID_ARG, "dspark_verify: logits must be aligned to their element size");
+        return fail(DSPARK_ERR_INVALID_ARG, "%s: logits must be aligned to their element size", fn);
+    return DSPARK_OK;
+}
+
+int check_scatter(const char* fn, const int32_t* committed, const int32_t* accept_len, int B,
+                  int gamma, const int32_t* out_tokens, const int32_t* out_len, int out_cap)
+{
+    if (B < 0 || gamma < 1 || gamma > DSPARK_MAX_GAMMA || out_cap < 0)
+        return fail(DSPARK_ERR_INVALID_ARG, "%s: bad sizes B=%d gamma=%d out_cap=%d", fn, B,
+                    gamma, out_cap);
+    if (B == 0) return DSPARK_OK;
+    if (committed == nullptr || accept_len == nullptr || out_len == nullptr ||
+        (out_cap > 0 && out_tokens == nullptr))
+        return fail(DSPARK_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+    return DSPARK_OK;
+}
+
+dspark::VerifyCall verify_call(dspark_mode mode, int stochastic, const void* target_logits,
+                               int target_rows, const void* draft_logits, dspark_dtype dtype,
+                               int V, const int32_t* cu_seqlens, const int32_t* windows,
+                               const int32_t* block_tokens, int B, int gamma, float temperature,
+                               uint64_t seed, uint64_t step, int32_t* accept_len,
+                               int32_t* committed, int32_t* ceiling_len, float* row_prob,
+                               void* workspace, size_t workspace_bytes, int32_t* status)
+{
     dspark::VerifyCall c;
     c.mode = static_cast<int>(mode);
     c.stochastic = stochastic ? 1 : 0;
@@ -195,6 +204,121 @@ int dspark_verify(dspark_mode mode, int stochastic, const void* target_logits, i
     c.ws = workspace;
     c.ws_bytes = workspace_bytes;
     c.status = status;
+    c.out_tokens = nullptr;
+    c.out_len = nullptr;
+    c.out_cap = 0;
+    return c;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dspark_schedule(const float* conf, int B, int gamma, const dspark_cost* cost,
+                    int32_t* windows, int32_t* k_star, int32_t* status, cudaStream_t stream)
+{
+    const char* fn = "dspark_schedule";
+    int rc = check_schedule(fn, conf, B, gamma, cost, windows, k_star);
+    if (rc != DSPARK_OK) return rc;
+    if (B == 0) return schedule_empty(fn, k_star, stream);
+    return dspark::launch_schedule(conf, B, gamma, cost, windows, k_star, status, stream);
+}
+
+int dspark_pack(const int32_t* windows, const int32_t* block_tokens, int B, int gamma,
+                const int32_t* tiers, int n_tiers, int32_t* cu_seqlens, int32_t* packed_ids,
+                int32_t* row_req, int32_t* row_pos, int packed_cap, int32_t* meta,
+                int32_t* status, cudaStream_t stream)
+{
+    int rc = check_pack("dspark_pack", windows, block_tokens, B, gamma, tiers, n_tiers,
+                        cu_seqlens, packed_ids, packed_cap, meta);
+    if (rc != DSPARK_OK) return rc;
+    return dspark::launch_pack(windows, block_tokens, B, gamma, tiers, n_tiers, cu_seqlens,
+                               packed_ids, row_req, row_pos, packed_cap, meta, status, stream);
+}
+
+int dspark_schedule_pack(const float* conf, int B, int gamma, const dspark_cost* cost,
+                         const int32_t* block_tokens, const int32_t* tiers, int n_tiers,
+                         int32_t* windows, int32_t* k_star, int32_t* cu_seqlens,
+                         int32_t* packed_ids, int32_t* row_req, int32_t* row_pos,
+                         int packed_cap, int32_t* meta, int32_t* status, cudaStream_t stream)
+{
+    const char* fn = "dspark_schedule_pack";
+    int rc = check_schedule(fn, conf, B, gamma, cost, windows, k_star);
+    if (rc != DSPARK_OK) return rc;
+    rc = check_pack(fn, windows, block_tokens, B, gamma, tiers, n_tiers, cu_seqlens, packed_ids,
+                    packed_cap, meta);
+    if (rc != DSPARK_OK) return rc;
+    if (B == 0 || gamma == 1) {   // nothing to rank: the two plain kernels
+        rc = B == 0 ? schedule_empty(fn, k_star, stream)
+                    : dspark::launch_schedule(conf, B, gamma, cost, windows, k_star, status, stream);
+        if (rc != DSPARK_OK) return rc;
+        return dspark::launch_pack(windows, block_tokens, B, gamma, tiers, n_tiers, cu_seqlens,
+                                   packed_ids, row_req, row_pos, packed_cap, meta, status, stream);
+    }
+    dspark::PackArgs pk;
+    pk.tokens = block_tokens;
+    pk.tiers = tiers;
+    pk.n_tiers = n_tiers;
+    pk.cu = cu_seqlens;
+    pk.packed_ids = packed_ids;
+    pk.row_req = row_req;
+    pk.row_pos = row_pos;
+    pk.packed_cap = packed_cap;
+    pk.meta = meta;
+    return dspark::launch_schedule_pack(conf, B, gamma, cost, windows, k_star, pk, status, stream);
+}
+
+size_t dspark_verify_workspace_bytes(int B, int gamma, int V, int stochastic)
+{
+    if (B < 0 || gamma < 1 || gamma > DSPARK_MAX_GAMMA || V < 1) {
+        fail(DSPARK_ERR_INVALID_ARG, "dspark_verify_workspace_bytes: bad sizes B=%d gamma=%d V=%d",
+             B, gamma, V);
+        return 0;
+    }
+    return dspark::verify_workspace_bytes(B, gamma, V, stochastic ? 1 : 0);
+}
+
+int dspark_verify(dspark_mode mode, int stochastic, const void* target_logits, int target_rows,
+                  const void* draft_logits, dspark_dtype dtype, int V, const int32_t* cu_seqlens,
+                  const int32_t* windows, const int32_t* block_tokens, int B, int gamma,
+                  float temperature, uint64_t seed, uint64_t step, int32_t* accept_len,
+                  int32_t* committed, int32_t* ceiling_len, float* row_prob, void* workspace,
+                  size_t workspace_bytes, int32_t* status, cudaStream_t stream)
+{
+    int rc = check_verify("dspark_verify", mode, stochastic, target_logits, target_rows,
+                          draft_logits, dtype, V, cu_seqlens, windows, block_tokens, B, gamma,
+                          temperature, accept_len, committed);
+    if (rc != DSPARK_OK || B == 0) return rc;
+    const dspark::VerifyCall c = verify_call(
+        mode, stochastic, target_logits, target_rows, draft_logits, dtype, V, cu_seqlens, windows,
+        block_tokens, B, gamma, temperature, seed, step, accept_len, committed, ceiling_len,
+        row_prob, workspace, workspace_bytes, status);
+    return dspark::launch_verify(c, stream);
+}
+
+int dspark_verify_scatter(dspark_mode mode, int stochastic, const void* target_logits,
+                          int target_rows, const void* draft_logits, dspark_dtype dtype, int V,
+                          const int32_t* cu_seqlens, const int32_t* windows,
+                          const int32_t* block_tokens, int B, int gamma, float temperature,
+                          uint64_t seed, uint64_t step, int32_t* accept_len, int32_t* committed,
+                          int32_t* ceiling_len, float* row_prob, void* workspace,
+                          size_t workspace_bytes, int32_t* out_tokens, int32_t* out_len,
+                          int out_cap, int32_t* status, cudaStream_t stream)
+{
+    const char* fn = "dspark_verify_scatter";
+    int rc = check_verify(fn, mode, stochastic, target_logits, target_rows, draft_logits, dtype,
+                          V, cu_seqlens, windows, block_tokens, B, gamma, temperature,
+                          accept_len, committed);
+    if (rc != DSPARK_OK) return rc;
+    rc = check_scatter(fn, committed, accept_len, B, gamma, out_tokens, out_len, out_cap);
+    if (rc != DSPARK_OK || B == 0) return rc;
+    dspark::VerifyCall c = verify_call(
+        mode, stochastic, target_logits, target_rows, draft_logits, dtype, V, cu_seqlens, windows,
+        block_tokens, B, gamma, temperature, seed, step, accept_len, committed, ceiling_len,
+        row_prob, workspace, workspace_bytes, status);
+    c.out_tokens = out_tokens;
+    c.out_len = out_len;
+    c.out_cap = out_cap;
     return dspark::launch_verify(c, stream);
 }
 
@@ -202,13 +326,9 @@ int dspark_scatter(const int32_t* committed, const int32_t* accept_len, int B, i
                    int32_t* out_tokens, int32_t* out_len, int out_cap, int32_t* status,
                    cudaStream_t stream)
 {
-    if (B < 0 || gamma < 1 || gamma > DSPARK_MAX_GAMMA || out_cap < 0)
-        return fail(DSPARK_ERR_INVALID_ARG, "dspark_scatter: bad sizes B=%d gamma=%d out_cap=%d",
-                    B, gamma, out_cap);
-    if (B == 0) return DSPARK_OK;
-    if (committed == nullptr || accept_len == nullptr || out_len == nullptr ||
-        (out_cap > 0 && out_tokens == nullptr))
-        return fail(DSPARK_ERR_INVALID_ARG, "dspark_scatter: a required pointer is NULL");
+    int rc = check_scatter("dspark_scatter", committed, accept_len, B, gamma, out_tokens,
+                           out_len, out_cap);
+    if (rc != DSPARK_OK || B == 0) return rc;
     return dspark::launch_scatter(committed, accept_len, B, gamma, out_tokens, out_len, out_cap,
                                   status, stream);
 }

@@ -35,6 +35,21 @@ int launch_pack(const int32_t* windows, const int32_t* tokens, int B, int gamma,
                 const int32_t* tiers, int n_tiers, int32_t* cu, int32_t* packed_ids,
                 int32_t* row_req, int32_t* row_pos, int packed_cap, int32_t* meta,
                 int32_t* status, cudaStream_t stream);
+struct PackArgs {
+    const int32_t* tokens;
+    const int32_t* tiers;
+    int n_tiers;
+    int32_t* cu;
+    int32_t* packed_ids;
+    int32_t* row_req;
+    int32_t* row_pos;
+    int packed_cap;
+    int32_t* meta;
+};
+// The schedule, then the pack of the windows it wrote, in one single-CTA kernel.
+int launch_schedule_pack(const float* conf, int B, int gamma, const dspark_cost* cost,
+                         int32_t* windows, int32_t* k_star, const PackArgs& pk, int32_t* status,
+                         cudaStream_t stream);
 struct VerifyCall {
     int mode, stochastic;
     const void* target;
@@ -54,6 +69,10 @@ struct VerifyCall {
     void* ws;
     size_t ws_bytes;
     int32_t* status;
+    // fused compact scatter (dspark_verify_scatter); out_tokens == nullptr: none
+    int32_t* out_tokens;
+    int32_t* out_len;
+    int out_cap;
 };
 size_t verify_workspace_bytes(int B, int gamma, int V, int stochastic);
 int launch_verify(const VerifyCall& c, cudaStream_t stream);
@@ -103,6 +122,29 @@ __device__ __forceinline__ void pdl_wait_and_trigger()
 __device__ __forceinline__ void raise_status(int32_t* status, int bits)
 {
     if (status != nullptr && bits != 0) atomicOr(status, bits);
+}
+
+// Compact scatter of one request by one warp: lane i < L holds committed token i, which is
+// appended to the request's history at out_len[b] + i (clamped lengths, overflow dropped and
+// flagged). Every lane reads out_len[b] before lane 0 advances it. Returns the status bits
+// (the same on every lane).
+__device__ __forceinline__ int scatter_request(int64_t b, int L, int gamma, int tok, int lane,
+                                               int32_t* out_tokens, int32_t* out_len, int out_cap)
+{
+    int bits = 0;
+    int n = out_len[b];
+    if (L < 0 || L > gamma) { bits |= DSPARK_STATUS_BAD_LENGTH; L = L < 0 ? 0 : gamma; }
+    if (n < 0 || n > out_cap) { bits |= DSPARK_STATUS_BAD_LENGTH; n = n < 0 ? 0 : out_cap; }
+    if (lane < L) {
+        if (n + lane < out_cap)
+            out_tokens[b * out_cap + n + lane] = tok;
+        else
+            bits |= DSPARK_STATUS_OUT_OVERFLOW;
+    }
+    __syncwarp();
+    if (lane == 0) out_len[b] = (n + L < out_cap) ? n + L : out_cap;
+    for (int off = 16; off > 0; off >>= 1) bits |= __shfl_xor_sync(0xffffffffu, bits, off);
+    return bits;
 }
 
 // bf16 is the upper half of an IEEE fp32: widening is a shift, exact.

@@ -1,143 +1,23 @@
-// pack.cu — ragged front-pack as one single-CTA kernel.
+// pack.cu — ragged front-pack as one single-CTA kernel (the body is in pack_block.cuh).
 //
 // "DSpark in SGLang" (LMSYS blog summary), A2, ragged verify over full CUDA graphs: the
-// variable windows are front-packed into one compact cu_seqlens-style buffer and only the
-// total is rounded up to the nearest captured graph tier, so a smaller budget replays a truly
-// smaller graph; padding rows up to the tier are waste (figure 2).
-//
-//   1. every load is issued up front: each thread's windows and its requests' block tokens,
-//      and one tier per thread (n_tiers <= 1024), so the kernel pays one memory round trip;
-//   2. windows clamped to [1, gamma]; block-wide exclusive scan -> cu_seqlens;
-//   3. tier = min over tiers >= M (tiers need not be sorted);
-//   4. each thread writes its requests' rows (token, request, position); padding rows up to
-//      the tier get 0 / -1 / -1.
-#include "common.cuh"
+// variable windows are front-packed into one cu_seqlens-style buffer whose total is rounded
+// up to the nearest captured graph tier.
+#include "pack_block.cuh"
 
 namespace dspark {
 namespace {
 
-constexpr int kThreads = 1024;
-constexpr int kWarps = kThreads / 32;
-
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kPackThreads, 1)
 pack_kernel(const int32_t* __restrict__ windows, const int32_t* __restrict__ tokens, int B,
             int gamma, const int32_t* __restrict__ tiers, int n_tiers,
             int32_t* __restrict__ cu_out, int32_t* __restrict__ packed_ids,
             int32_t* __restrict__ row_req, int32_t* __restrict__ row_pos, int packed_cap,
             int32_t* __restrict__ meta, int32_t* __restrict__ status)
 {
-    __shared__ int warp_total[kWarps];
-    __shared__ int tier_s;
     pdl_wait_and_trigger();
-    const int tid = threadIdx.x;
-    const int lane = tid & 31;
-    const int warp = tid >> 5;
-
-    // 1. loads
-    const int tier_v = tid < n_tiers ? __ldg(tiers + tid) : INT_MAX;
-    const int items = (B + kThreads - 1) / kThreads;
-    const int b0 = tid * items;
-    int tok[DSPARK_MAX_GAMMA];
-    int w_first = 1;
-    if (items == 1 && b0 < B) {
-        w_first = __ldg(windows + b0);
-#pragma unroll
-        for (int i = 0; i < DSPARK_MAX_GAMMA; ++i)
-            if (i < gamma) tok[i] = __ldg(tokens + static_cast<int64_t>(b0) * gamma + i);
-    }
-    if (tid == 0) tier_s = INT_MAX;
-
-    // 2. exclusive scan of the clamped windows
-    int bad = 0;
-    int run = 0;
-    for (int it = 0; it < items; ++it) {
-        const int b = b0 + it;
-        if (b >= B) break;
-        int w = items == 1 ? w_first : __ldg(windows + b);
-        if (w < 1 || w > gamma) {
-            bad = DSPARK_STATUS_BAD_WINDOW;
-            w = w < 1 ? 1 : gamma;
-        }
-        run += w;
-    }
-    int incl = run;
-    for (int off = 1; off < 32; off <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += v;
-    }
-    if (lane == 31) warp_total[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        int t = warp_total[lane];
-        for (int off = 1; off < 32; off <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, t, off);
-            if (lane >= off) t += v;
-        }
-        warp_total[lane] = t;
-    }
-    __syncthreads();
-    const int M = warp_total[kWarps - 1];
-    const int excl = incl - run + (warp > 0 ? warp_total[warp - 1] : 0);
-
-    // 3. tier
-    int best = tier_v >= M ? tier_v : INT_MAX;
-    for (int off = 16; off > 0; off >>= 1) best = min(best, __shfl_xor_sync(0xffffffffu, best, off));
-    if (lane == 0 && best != INT_MAX) atomicMin(&tier_s, best);
-    __syncthreads();
-    int tier = tier_s;
-    if (tier == INT_MAX) {
-        tier = M;
-        bad |= DSPARK_STATUS_TIER_OVERFLOW;
-    }
-    if (tier > packed_cap) bad |= DSPARK_STATUS_PACK_CAPACITY;
-
-    // 4. rows of this thread's requests, then padding
-    int acc = excl;
-    for (int it = 0; it < items; ++it) {
-        const int b = b0 + it;
-        if (b >= B) break;
-        int w = items == 1 ? w_first : __ldg(windows + b);
-        w = w < 1 ? 1 : (w > gamma ? gamma : w);
-        cu_out[b] = acc;
-        if (items == 1) {
-#pragma unroll
-            for (int i = 0; i < DSPARK_MAX_GAMMA; ++i) {
-                const int r = acc + i;
-                if (i < w && r < packed_cap) {
-                    packed_ids[r] = tok[i];
-                    if (row_req) row_req[r] = b;
-                    if (row_pos) row_pos[r] = i;
-                }
-            }
-        } else {
-            for (int i = 0; i < w; ++i) {
-                const int r = acc + i;
-                if (r >= packed_cap) break;
-                packed_ids[r] = __ldg(tokens + static_cast<int64_t>(b) * gamma + i);
-                if (row_req) row_req[r] = b;
-                if (row_pos) row_pos[r] = i;
-            }
-        }
-        acc += w;
-    }
-    if (tid == 0) cu_out[B] = M;
-    const int rows_pad = min(tier, packed_cap);
-    for (int r = M + tid; r < rows_pad; r += kThreads) {
-        packed_ids[r] = 0;
-        if (row_req) row_req[r] = -1;
-        if (row_pos) row_pos[r] = -1;
-    }
-    if (tid == 0) {
-        meta[0] = M;
-        meta[1] = tier;
-    }
-    // status bits of every thread
-    const unsigned any = __ballot_sync(0xffffffffu, bad != 0);
-    if (any) {
-        int bits = bad;
-        for (int off = 16; off > 0; off >>= 1) bits |= __shfl_xor_sync(0xffffffffu, bits, off);
-        if (lane == 0) raise_status(status, bits);
-    }
+    pack_block<true>(windows, tokens, B, gamma, tiers, n_tiers, cu_out, packed_ids, row_req,
+                     row_pos, packed_cap, meta, status);
 }
 
 }  // namespace
@@ -147,7 +27,7 @@ int launch_pack(const int32_t* windows, const int32_t* tokens, int B, int gamma,
                 int32_t* row_req, int32_t* row_pos, int packed_cap, int32_t* meta,
                 int32_t* status, cudaStream_t stream)
 {
-    return launch_pdl("pack", pack_kernel, dim3(1), dim3(kThreads), 0, stream, windows, tokens, B,
+    return launch_pdl("pack", pack_kernel, dim3(1), dim3(kPackThreads), 0, stream, windows, tokens, B,
                       gamma, tiers, n_tiers, cu, packed_ids, row_req, row_pos, packed_cap, meta,
                       status);
 }

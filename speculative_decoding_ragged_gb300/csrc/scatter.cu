@@ -2,8 +2,8 @@
 //
 // "DSpark in SGLang" (LMSYS blog summary), A2, performance and zero-overhead scheduling: a
 // fused kernel writes the accepted tokens back into per-request state. One warp per request
-// (gamma <= 32 committed tokens, one lane each); the history length is read by every lane
-// before lane 0 advances it.
+// (gamma <= 32 committed tokens, one lane each), through the same per-request routine that
+// dspark_verify_scatter runs at the end of its verify.
 #include "common.cuh"
 
 namespace dspark {
@@ -20,20 +20,9 @@ scatter_kernel(const int32_t* __restrict__ committed, const int32_t* __restrict_
     const int64_t b = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (b >= B) return;   // whole warps leave together
-    int bits = 0;
-    int L = accept_len[b];
-    int n = out_len[b];
-    if (L < 0 || L > gamma) { bits |= DSPARK_STATUS_BAD_LENGTH; L = L < 0 ? 0 : gamma; }
-    if (n < 0 || n > out_cap) { bits |= DSPARK_STATUS_BAD_LENGTH; n = n < 0 ? 0 : out_cap; }
-    if (lane < L) {
-        if (n + lane < out_cap)
-            out_tokens[b * out_cap + n + lane] = committed[b * gamma + lane];
-        else
-            bits |= DSPARK_STATUS_OUT_OVERFLOW;
-    }
-    __syncwarp();
-    if (lane == 0) out_len[b] = (n + L < out_cap) ? n + L : out_cap;
-    for (int off = 16; off > 0; off >>= 1) bits |= __shfl_xor_sync(0xffffffffu, bits, off);
+    const int L = accept_len[b];
+    const int tok = (lane < L && lane < gamma) ? committed[b * gamma + lane] : -1;
+    const int bits = scatter_request(b, L, gamma, tok, lane, out_tokens, out_len, out_cap);
     if (lane == 0) raise_status(status, bits);
 }
 

@@ -26,6 +26,7 @@
 //   5. windows w_b = 1 + count of request b among the first K* candidates.
 // Latency-bound (microseconds); the grid is one CTA by construction of the problem.
 #include "common.cuh"
+#include "pack_block.cuh"
 
 namespace dspark {
 namespace {
@@ -124,12 +125,13 @@ __device__ __forceinline__ uint64_t key_value(uint32_t k32)
     return k32 == 0xFFFFFFFFu ? (1ull << 32) : static_cast<uint64_t>(k32);
 }
 
-template <bool MERGE>
+// PACK: the same CTA then front-packs the windows it wrote (dspark_schedule_pack).
+template <bool MERGE, bool PACK>
 __global__ void __launch_bounds__(kThreads, 1)
 schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, double bias,
                 const double* __restrict__ alpha, const double* __restrict__ theta,
                 int32_t* __restrict__ windows, int32_t* __restrict__ k_star,
-                int32_t* __restrict__ status)
+                int32_t* __restrict__ status, PackArgs pk)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     // MERGE: keys [2][n] (u32) and indices [2][n]; else words [n_pad] (u64). Then count [B].
@@ -437,6 +439,12 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
     for (int p = tid; p < K_star; p += kThreads) atomicAdd(&count[index_at(p) / L], 1);
     __syncthreads();
     for (int b = tid; b < B; b += kThreads) windows[b] = 1 + count[b];
+    if (PACK) {
+        static_assert(kPackThreads == kThreads, "the pack body runs on the scheduler's CTA");
+        __syncthreads();   // every window written (and visible to the block) before the pack
+        pack_block<false>(windows, pk.tokens, B, L + 1, pk.tiers, pk.n_tiers, pk.cu,
+                          pk.packed_ids, pk.row_req, pk.row_pos, pk.packed_cap, pk.meta, status);
+    }
 }
 
 __global__ void schedule_trivial_kernel(int B, double bias, const double* __restrict__ alpha,
@@ -457,15 +465,16 @@ __global__ void schedule_trivial_kernel(int B, double bias, const double* __rest
 
 }  // namespace
 
-int launch_schedule(const float* conf, int B, int gamma, const dspark_cost* cost,
-                    int32_t* windows, int32_t* k_star, int32_t* status, cudaStream_t stream)
+namespace {
+
+// Launches schedule_kernel<merge, PACK> with the dynamic shared memory its size needs; the
+// opt-in limit (static plus dynamic) is configured once per device and variant.
+template <bool PACK>
+int launch_schedule_kernel(const char* what, const float* conf, int B, int L,
+                           const dspark_cost* cost, int32_t* windows, int32_t* k_star,
+                           int32_t* status, const PackArgs& pk, cudaStream_t stream)
 {
-    const int L = gamma - 1;
     const int n = B * L;
-    if (n == 0) {
-        return launch_pdl("schedule", schedule_trivial_kernel, dim3(1), dim3(256), 0, stream, B,
-                          cost->bias, cost->alpha, cost->theta, windows, k_star, status);
-    }
     int n_pad = 1;
     while (n_pad < n) n_pad <<= 1;
     const bool merge = n <= kMergeMax;
@@ -474,12 +483,11 @@ int launch_schedule(const float* conf, int B, int gamma, const dspark_cost* cost
     DeviceInfo dev;
     int rc = current_device(&dev);
     if (rc != DSPARK_OK) return rc;
-    // the opt-in limit covers static plus dynamic shared memory
     static thread_local int configured_device = -1;
     static thread_local size_t max_dynamic[2] = {0, 0};
     if (configured_device != dev.device) {
-        const void* fns[2] = {reinterpret_cast<const void*>(schedule_kernel<false>),
-                              reinterpret_cast<const void*>(schedule_kernel<true>)};
+        const void* fns[2] = {reinterpret_cast<const void*>(schedule_kernel<false, PACK>),
+                              reinterpret_cast<const void*>(schedule_kernel<true, PACK>)};
         for (int v = 0; v < 2; ++v) {
             cudaFuncAttributes attr;
             if (cudaFuncGetAttributes(&attr, fns[v]) != cudaSuccess)
@@ -492,15 +500,38 @@ int launch_schedule(const float* conf, int B, int gamma, const dspark_cost* cost
         configured_device = dev.device;
     }
     if (smem > max_dynamic[merge ? 1 : 0])
-        return fail(DSPARK_ERR_UNSUPPORTED, "dspark_schedule: %zu bytes of shared memory needed, "
-                    "the device allows %zu", smem, max_dynamic[merge ? 1 : 0]);
+        return fail(DSPARK_ERR_UNSUPPORTED, "%s: %zu bytes of shared memory needed, the device "
+                    "allows %zu", what, smem, max_dynamic[merge ? 1 : 0]);
     if (merge)
-        return launch_pdl("schedule", schedule_kernel<true>, dim3(1), dim3(kThreads), smem, stream,
-                          conf, B, L, n, n_pad, cost->bias, cost->alpha, cost->theta, windows,
-                          k_star, status);
-    return launch_pdl("schedule", schedule_kernel<false>, dim3(1), dim3(kThreads), smem, stream,
-                      conf, B, L, n, n_pad, cost->bias, cost->alpha, cost->theta, windows, k_star,
-                      status);
+        return launch_pdl(what, schedule_kernel<true, PACK>, dim3(1), dim3(kThreads), smem,
+                          stream, conf, B, L, n, n_pad, cost->bias, cost->alpha, cost->theta,
+                          windows, k_star, status, pk);
+    return launch_pdl(what, schedule_kernel<false, PACK>, dim3(1), dim3(kThreads), smem, stream,
+                      conf, B, L, n, n_pad, cost->bias, cost->alpha, cost->theta, windows,
+                      k_star, status, pk);
+}
+
+}  // namespace
+
+int launch_schedule(const float* conf, int B, int gamma, const dspark_cost* cost,
+                    int32_t* windows, int32_t* k_star, int32_t* status, cudaStream_t stream)
+{
+    const int L = gamma - 1;
+    if (B * L == 0) {
+        return launch_pdl("schedule", schedule_trivial_kernel, dim3(1), dim3(256), 0, stream, B,
+                          cost->bias, cost->alpha, cost->theta, windows, k_star, status);
+    }
+    const PackArgs none = {};
+    return launch_schedule_kernel<false>("dspark_schedule", conf, B, L, cost, windows, k_star,
+                                         status, none, stream);
+}
+
+int launch_schedule_pack(const float* conf, int B, int gamma, const dspark_cost* cost,
+                         int32_t* windows, int32_t* k_star, const PackArgs& pk, int32_t* status,
+                         cudaStream_t stream)
+{
+    return launch_schedule_kernel<true>("dspark_schedule_pack", conf, B, gamma - 1, cost,
+                                        windows, k_star, status, pk, stream);
 }
 
 }  // namespace dspark

@@ -379,8 +379,8 @@ __device__ __forceinline__ void philox4x64_10(uint64_t c0, uint64_t c1, uint64_t
     out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
 }
 
-// The bonus draw of one request, decided by the finaliser and carried out by the tile and
-// pick kernels (stochastic verify).
+// The bonus draw of one request, decided by the finaliser and carried out by the bonus kernel
+// (stochastic verify).
 struct BonusJob {
     int64_t trow;   // target row of the bonus position
     int64_t drow;   // draft row of a residual draw; -1 for a draw from p
@@ -406,6 +406,9 @@ struct FinalArgs {
     BonusJob* jobs;   // [B] (stochastic)
     float* tiles;     // [B][n_tiles][2]: residual and p weight sums per 256-token tile
     unsigned* done;   // [B]: tile CTAs finished per request (zeroed by the finaliser)
+    int32_t* out_tokens;   // fused compact scatter (nullptr: none)
+    int32_t* out_len;
+    int out_cap;
     uint64_t seed, step;
     int mode, V, nc, vec, B, gamma, target_rows, n_tiles;
     int64_t rows_max;
@@ -582,6 +585,11 @@ verify_finalize_kernel(FinalArgs A)
                 A.done[b] = 0u;
             }
         }
+        if (A.out_tokens && warp == 0) {         // nothing committed: lengths checked only
+            const int sb = scatter_request(b, 0, gamma, -1, lane, A.out_tokens, A.out_len,
+                                           A.out_cap);
+            if (lane == 0) raise_status(A.status, sb);
+        }
         return;
     }
     const int ndec = nrows - 1;   // accept tests this mode runs
@@ -668,6 +676,12 @@ verify_finalize_kernel(FinalArgs A)
             if (A.ceiling) A.ceiling[b] = (A.mode == DSPARK_COMPACT) ? -1 : Lf;
         }
         if (!STOCH && lane < gamma) out[lane] = (lane < Lc) ? g_s[lane] : -1;
+        if (!STOCH && A.out_tokens) {
+            const int tok = lane < Lc ? g_s[lane] : -1;
+            const int sb = scatter_request(b, Lc, gamma, tok, lane, A.out_tokens, A.out_len,
+                                           A.out_cap);
+            if (lane == 0) bits |= sb;
+        }
     }
     __syncthreads();
     const int Lc = walk_s[0];
@@ -805,6 +819,16 @@ __device__ void bonus_pick(const FinalArgs& A, int b, const BonusJob& job)
         chosen = cand >= 0 ? cand : min(tile * 256, A.V - 1);
     }
     if (lane == 0) A.committed[job.slot] = chosen;
+    if (A.out_tokens) {                               // fused compact scatter of the request
+        const int64_t row0 = static_cast<int64_t>(b) * A.gamma;
+        const int Lc = static_cast<int>(job.slot - row0) + 1;
+        int tok = -1;
+        if (lane < Lc - 1) tok = __ldg(A.tokens + row0 + lane + 1);
+        else if (lane == Lc - 1) tok = chosen;
+        const int sb = scatter_request(b, Lc, A.gamma, tok, lane, A.out_tokens, A.out_len,
+                                       A.out_cap);
+        if (lane == 0) raise_status(A.status, sb);
+    }
 }
 
 // Stochastic bonus, step 1: weight sums of every 256-token tile of each request's bonus row(s),
@@ -950,6 +974,9 @@ int run_verify(const VerifyCall& c, const Plan& plan, void* part_t, void* part_d
     fa.jobs = static_cast<BonusJob*>(jobs);
     fa.done = reinterpret_cast<unsigned*>(static_cast<BonusJob*>(jobs) + c.B);
     fa.tiles = static_cast<float*>(tiles);
+    fa.out_tokens = c.out_tokens;
+    fa.out_len = c.out_len;
+    fa.out_cap = c.out_cap;
     fa.n_tiles = (c.V + 255) / 256;
     rc = launch_pdl("verify (finalize)", verify_finalize_kernel<DT, STOCH>, dim3(c.B),
                     dim3(kFinalThreads), 0, stream, fa);

@@ -64,11 +64,21 @@ class StandIn:
         return out
 
 
+def grid_M(bs: int, gamma: int, tiers: Sequence[int], points: int) -> list:
+    """Up to `points` values of M for batch size bs, both ends included: bs, the capture tiers
+    between bs and gamma*bs (so that batch sizes share theta entries and the fit is
+    over-determined), and gamma*bs, evenly thinned."""
+    cand = sorted(set([bs, gamma * bs] + [int(t) for t in tiers if bs < t < gamma * bs]))
+    if len(cand) <= points:
+        return cand
+    idx = np.unique(np.round(np.linspace(0, len(cand) - 1, points)).astype(int))
+    return [cand[i] for i in idx]
+
+
 def record(batch_sizes: Sequence[int], gamma: int = 8, V: int = 151936, H: int = 4096,
-           tiers: Optional[Sequence[int]] = None, points: int = 8, ctx_bytes: int = 2 << 20,
+           tiers: Optional[Sequence[int]] = None, points: int = 12, ctx_bytes: int = 2 << 20,
            warmup: int = 3, reps: int = 10, device="cuda") -> list:
-    """Median step time (us) of every (bs, M) grid cell: `points` values of M from bs to
-    gamma*bs per batch size."""
+    """Median step time (us) of every (bs, M) grid cell (grid_M per batch size)."""
     device = torch.device(device)
     tiers = list(tiers) if tiers is not None else list(range(32, 2049, 32))
     max_bs = max(batch_sizes)
@@ -83,9 +93,7 @@ def record(batch_sizes: Sequence[int], gamma: int = 8, V: int = 151936, H: int =
         bt = synth.make_batch(wl.with_(B=bs, gamma=gamma), seed=bs)
         conf = torch.as_tensor(bt.conf, device=device)
         tokens = torch.as_tensor(bt.tokens, device=device)
-        Ms = sorted(set(int(round(bs + f * (gamma - 1) * bs))
-                        for f in np.linspace(0.0, 1.0, points)))
-        for M in Ms:
+        for M in grid_M(bs, gamma, tiers, points):
             w = torch.as_tensor(forced_windows(bs, gamma, M), device=device)
             rows = int(tier_key([M], tiers)[0])
 
@@ -118,15 +126,15 @@ def record(batch_sizes: Sequence[int], gamma: int = 8, V: int = 151936, H: int =
 
 
 def evaluate(samples: list, tiers: Optional[Sequence[int]]) -> dict:
-    """Fit on every other M of each batch size (the ends always in), predict the rest."""
+    """Fit on two of every three cells of each batch size (the ends always in) and predict the
+    third; a held-out cell whose key no training cell shares is predicted by interpolation."""
     bs = np.array([s["bs"] for s in samples])
     M = np.array([s["M"] for s in samples])
     T = np.array([s["us"] for s in samples])
-    train = np.zeros(bs.size, bool)
+    train = np.ones(bs.size, bool)
     for b in np.unique(bs):
         idx = np.flatnonzero(bs == b)
-        train[idx[::2]] = True
-        train[idx[-1]] = True
+        train[idx[1:-1][1::3]] = False
     fit = fit_additive(bs[train], M[train], T[train], tiers=tiers)
     held = ~train
     return dict(
@@ -143,11 +151,11 @@ def evaluate(samples: list, tiers: Optional[Sequence[int]]) -> dict:
 
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
-    ap.add_argument("--batch-sizes", default="1,2,4,8,16,32,64,128,256")
+    ap.add_argument("--batch-sizes", default="1,2,4,8,16,24,32,48,64,96,128,192,256")
     ap.add_argument("--gamma", type=int, default=8)
     ap.add_argument("--V", type=int, default=151936)
     ap.add_argument("--H", type=int, default=4096)
-    ap.add_argument("--points", type=int, default=8)
+    ap.add_argument("--points", type=int, default=12)
     ap.add_argument("--reps", type=int, default=10)
     ap.add_argument("--out", default=None)
     a = ap.parse_args(argv)

@@ -1,8 +1,11 @@
 """A buffer-owning runner of one DSpark decode step: schedule -> pack -> verify -> scatter.
 
-All buffers are allocated once, on the device, at construction; `run` only enqueues the four
-library calls (five kernel launches) on the current stream and never synchronises, so it can
-be timed with CUDA events or captured into a CUDA graph.
+All buffers are allocated once, on the device, at construction; `run` only enqueues the
+library calls on the current stream and never synchronises, so it can be timed with CUDA
+events or captured into a CUDA graph. By default the step uses the two fused calls
+(dspark_schedule_pack, dspark_verify_scatter: three kernels greedy, four stochastic); with
+fused=False it issues the four single calls (five and six kernels). Both give identical
+results.
 """
 from __future__ import annotations
 
@@ -14,18 +17,24 @@ import torch
 from . import _binding as bd
 
 
-class DSparkStep:
-    LAUNCHES_PER_STEP = 5   # greedy: schedule, pack, verify (stream + finalize), scatter
-    LAUNCHES_PER_STEP_STOCHASTIC = 6   # + the bonus kernel
+def launches_per_step(gamma: int, stochastic: bool, fused: bool) -> int:
+    """Kernel launches of one step: schedule (+ pack), verify stream and finalize (+ the
+    stochastic bonus kernel), scatter unless fused."""
+    verify = 2 + (1 if stochastic else 0)
+    if fused:
+        return (1 if gamma > 1 else 2) + verify
+    return 2 + verify + 1
 
+
+class DSparkStep:
     def __init__(self, B: int, gamma: int, V: int, tiers: Sequence[int], bias: float,
                  alpha, theta, *, mode: str = "compact", stochastic: bool = False,
-                 out_cap: int = 4096, device="cuda"):
+                 out_cap: int = 4096, fused: bool = True, device="cuda"):
         self.B, self.gamma, self.V = B, gamma, V
         self.mode = mode
         self.stochastic = stochastic
-        self.launches_per_step = (self.LAUNCHES_PER_STEP_STOCHASTIC if stochastic
-                                  else self.LAUNCHES_PER_STEP)
+        self.fused = fused
+        self.launches_per_step = launches_per_step(gamma, stochastic, fused)
         self.device = torch.device(device)
         dev = dict(device=self.device)
         i32 = dict(dtype=torch.int32, **dev)
@@ -69,11 +78,32 @@ class DSparkStep:
         bd.dspark_scatter(self.committed, self.accept_len, self.out_tokens, self.out_len,
                           self.status)
 
+    def schedule_pack(self, conf: torch.Tensor, block_tokens: torch.Tensor, prepare=False):
+        return bd.dspark_schedule_pack(conf, self.cost, block_tokens, self.tiers, self.windows,
+                                       self.k_star, self.cu, self.packed_ids, self.meta,
+                                       self.row_req, self.row_pos, self.status, prepare=prepare)
+
+    def verify_scatter(self, target: torch.Tensor, block_tokens: torch.Tensor,
+                       draft: Optional[torch.Tensor] = None, *, temperature: float = 1.0,
+                       seed: int = 0, step: int = 0, row_prob: Optional[torch.Tensor] = None,
+                       prepare=False):
+        return bd.dspark_verify_scatter(
+            self.mode, target, block_tokens, self.accept_len, self.committed, self.workspace,
+            self.out_tokens, self.out_len, stochastic=self.stochastic, draft=draft,
+            cu_seqlens=self.cu, windows=self.windows, ceiling_len=self.ceiling,
+            row_prob=row_prob, temperature=temperature, seed=seed, step=step,
+            status=self.status, prepare=prepare)
+
     def prepare(self, conf, block_tokens, target, draft=None, *, temperature=1.0, seed=0,
                 step=0, row_prob=None):
-        """The step's four calls, checked and marshalled once for these input tensors (which
-        must stay alive and in place): returns [schedule, pack, verify, scatter], each a
-        callable that re-issues its C call on the current stream without Python-side checks."""
+        """The step's calls, checked and marshalled once for these input tensors (which must
+        stay alive and in place): [schedule_pack, verify_scatter] when fused, else [schedule,
+        pack, verify, scatter]; each a callable that re-issues its C call on the current stream
+        without Python-side checks."""
+        if self.fused:
+            return [self.schedule_pack(conf, block_tokens, prepare=True),
+                    self.verify_scatter(target, block_tokens, draft, temperature=temperature,
+                                        seed=seed, step=step, row_prob=row_prob, prepare=True)]
         return [
             bd.dspark_schedule(conf, self.cost, self.windows, self.k_star, self.status,
                                prepare=True),
@@ -92,6 +122,11 @@ class DSparkStep:
             row_prob=None):
         """One whole step. `target` holds the rows this mode verifies: the packed [>=M, V]
         rows of the scheduled windows (compact) or the full block [B*gamma, V]."""
+        if self.fused:
+            self.schedule_pack(conf, block_tokens)
+            self.verify_scatter(target, block_tokens, draft, temperature=temperature, seed=seed,
+                                step=step, row_prob=row_prob)
+            return
         self.schedule(conf)
         self.pack(block_tokens)
         self.verify(target, block_tokens, draft, temperature=temperature, seed=seed, step=step,

@@ -61,6 +61,32 @@ def test_argument_errors_are_reported_on_the_host(lib):
     assert rc == -1
 
 
+def test_fused_entry_points_check_both_halves(lib):
+    from speculative_decoding_ragged_gb300 import _binding as bd
+    cost = bd._Cost(1.0, None, 0, None, 0)
+    rc = lib.dspark_schedule_pack(None, -1, 4, ctypes.byref(cost), None, None, 1, None, None,
+                                  None, None, None, None, 0, None, None, None)
+    assert rc == -1 and "dspark_schedule_pack: B = -1" in bd.last_error()
+    rc = lib.dspark_schedule_pack(None, 8192, 4, ctypes.byref(cost), None, None, 1, None, None,
+                                  None, None, None, None, 0, None, None, None)
+    assert rc == -2 and "B*(gamma-1)" in bd.last_error()
+    # the schedule half is valid (B == 0), the pack half is not (no tiers)
+    k = ctypes.c_int32(0)
+    rc = lib.dspark_schedule_pack(None, 0, 4, ctypes.byref(cost), None, None, 0, None,
+                                  ctypes.byref(k), None, None, None, None, 0, None, None, None)
+    assert rc == -1 and "n_tiers" in bd.last_error()
+    rc = lib.dspark_verify_scatter(1, 0, None, 0, None, 0, 16, None, None, None, 1, 2, 1.0, 0,
+                                   0, None, None, None, None, None, 0, None, None, 4, None, None)
+    assert rc == -1 and "dspark_verify_scatter" in bd.last_error()
+    # the verify half is valid (B == 0), the scatter half is not (negative capacity)
+    rc = lib.dspark_verify_scatter(1, 0, None, 0, None, 0, 16, None, None, None, 0, 2, 1.0, 0,
+                                   0, None, None, None, None, None, 0, None, None, -1, None, None)
+    assert rc == -1 and "out_cap=-1" in bd.last_error()
+    rc = lib.dspark_verify_scatter(1, 0, None, 0, None, 0, 16, None, None, None, 0, 2, 1.0, 0,
+                                   0, None, None, None, None, None, 0, None, None, 4, None, None)
+    assert rc == 0
+
+
 def test_workspace_size_is_a_function_of_sizes(lib):
     from speculative_decoding_ragged_gb300 import _binding as bd
     assert bd.dspark_verify_workspace_bytes(0, 8, 1000, False) == 0

@@ -144,3 +144,12 @@ def test_forced_windows_sum_to_M_and_stay_in_range():
             assert w.max() - w.min() <= 1
     with pytest.raises(ValueError):
         forced_windows(4, 2, 9)
+
+
+def test_recorder_grid_includes_both_ends_and_shares_tiers():
+    from speculative_decoding_ragged_gb300.sps_profile import grid_M
+    tiers = list(range(32, 2049, 32))
+    grids = {bs: grid_M(bs, 8, tiers, 12) for bs in (1, 16, 48, 256)}
+    for bs, g in grids.items():
+        assert g[0] == bs and g[-1] == 8 * bs and len(g) <= 12 and g == sorted(set(g))
+    assert set(grids[16]) & set(grids[48])          # batch sizes meet on common tiers
