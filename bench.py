@@ -35,6 +35,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "packed verify rows/s & logits HBM GB/s vs GB300 peak; sched+pack µs/step"
+NOMINAL_HBM_GBS = 8000.0     # the GB300's nominal HBM3e bandwidth, for context beside the measured peak
 UNIT = "rows/s"
 WORKLOAD = "large_vocab_mixed"
 FALLBACK_HBM_GBS = 6800.0
@@ -54,6 +55,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batches", type=int, default=N_BATCHES)
     ap.add_argument("--latency-steps", type=int, default=10000)
+    ap.add_argument("--config-reps", type=int, default=30,
+                    help="timed verify calls per extra workload leg (0: skip the legs)")
     ap.add_argument("--event-every", type=int, default=8,
                     help="record the per-kernel events on every n-th timed step only: an event "
                          "between two kernels stops the second from launching early")
@@ -110,7 +113,7 @@ def measured_peak():
 
 def profile_traffic():
     """DRAM bytes over algorithmic bytes of the captured verify-stream launch recorded in
-    profiles/, if verify.cu still hashes to the value recorded with it."""
+    profiles/, if the source files the record names still hash to the value recorded with it."""
     try:
         with open(PROFILE) as f:
             text = f.read()
@@ -121,10 +124,14 @@ def profile_traffic():
         if ":" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split(":", 1)
             rec[k.strip()] = v.strip().strip("`")
-    src = os.path.join(ROOT, "speculative_decoding_ragged_gb300", "csrc", "verify.cu")
-    with open(src, "rb") as f:
-        digest = hashlib.sha256(f.read()).hexdigest()[:16]
-    if rec.get("verify_cu_sha256_16") != digest:
+    h = hashlib.sha256()
+    try:
+        for name in rec.get("sources", "").split():
+            with open(os.path.join(ROOT, "speculative_decoding_ragged_gb300", "csrc", name), "rb") as f:
+                h.update(f.read())
+    except OSError:
+        return None
+    if not rec.get("sources") or rec.get("sources_sha256_16") != h.hexdigest()[:16]:
         return None
     try:
         return float(rec["traffic_over_algorithmic"])
@@ -307,6 +314,7 @@ def run_native(args, rank, world, local):
     e2e_rows = sum_over_ranks(e2e_rows, world)
 
     latency = latency_leg(dev, args.latency_steps) if args.latency_steps > 0 else None
+    legs = config_legs(dev, args.config_reps) if args.config_reps > 0 and rank == 0 else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -333,6 +341,8 @@ def run_native(args, rank, world, local):
                      "kernel": "dspark_verify_scatter (stream + finalize with scatter)",
                      "achieved": ach_gbs, "peak": peak, "peak_source": peak_kind,
                      "unit": "GB/s", "frac": ach_gbs / peak, "traffic": traffic,
+                     "frac_of_nominal_8tbs": ach_gbs / NOMINAL_HBM_GBS,
+                     "launch_us_p10_p90": [percentile(verify_us, 10), percentile(verify_us, 90)],
                      "algorithmic_bytes_per_launch": statistics.mean(verify_bytes),
                      "launch_us_mean": verify_mean_us},
         "cpu_baseline": cpu,
@@ -342,6 +352,7 @@ def run_native(args, rank, world, local):
         "gpu_launches": K * st.launches_per_step,
         "clocks": clk,
         "latency_b1": latency,
+        "verify_legs": legs,
     }
 
 
@@ -402,6 +413,87 @@ def latency_leg(dev, steps, pool=64):
         out["pool_mb"] = round(sum(sum(t.numel() * t.element_size() for t in e[2:] if t is not None)
                                    for e in entries) / 1e6, 1)
         del graphs, cycle, calls, entries
+    return out
+
+
+def percentile(xs, q):
+    return float(np.percentile(np.asarray(xs, dtype=np.float64), q))
+
+
+# (workload, mode, stochastic): the other workloads' verify launches, timed alone
+CONFIG_LEGS = [("stochastic", "compact", True), ("stochastic", "cap_accept", True),
+               ("high_load", "compact", False), ("high_load", "cap_accept", False)]
+
+
+def config_legs(dev, reps):
+    """Roofline of dspark_verify_scatter (stream + finalize with the fused scatter, + the bonus
+    kernel when stochastic) on the other workloads, each launch timed alone with CUDA events on
+    its stream after an L2 flush (a 256 MB buffer read between launches). Windows come from
+    the library's own schedule. Algorithmic bytes: the target rows the mode verifies (M
+    compact, B*gamma cap-accept), the draft rows of the tested drafts (stochastic: M - B
+    compact, B*(gamma-1) cap-accept) and the bonus pass (two rows per request that rejected,
+    one per request that accepted its whole window), each V*e bytes."""
+    from speculative_decoding_ragged_gb300 import synth
+    from speculative_decoding_ragged_gb300.step import DSparkStep
+    peak, _ = measured_peak()
+    flush = torch.ones(64 << 20, dtype=torch.int32, device=dev)     # 256 MB, read to evict L2
+    stream = torch.cuda.current_stream()
+    out = {}
+    cache = {}
+    for name, mode, stochastic in CONFIG_LEGS:
+        wl = synth.WORKLOADS[name]
+        if name not in cache:
+            cache.clear()
+            cache[name] = synth.make_batch(wl, seed=77, stochastic=stochastic)
+        bt = cache[name]
+        B, g, V = wl.B, wl.gamma, wl.V
+        e = 2 if wl.dtype == "bf16" else 4
+        st = DSparkStep(B, g, V, wl.tiers, bt.bias, bt.alpha, bt.theta, mode=mode,
+                        stochastic=stochastic, out_cap=g * (reps + 8), device=dev)
+        conf = torch.as_tensor(bt.conf, device=dev)
+        tokens = torch.as_tensor(bt.tokens, device=dev)
+        st.schedule_pack(conf, tokens)
+        torch.cuda.synchronize()
+        w = st.windows.cpu().numpy()
+        M = int(w.sum())
+        if mode == "compact":
+            tier = int(st.meta[1].item())
+            target = synth.gather_packed(bt.target, B, g, w, rows_cap=tier).to(dev)
+        else:
+            target = bt.target.to(dev)
+        draft = bt.draft.to(dev) if stochastic else None
+        call = st.verify_scatter(target, tokens, draft, temperature=wl.temperature, seed=5,
+                                 prepare=True)
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)]
+        for e0, e1 in evs:
+            torch.max(flush)      # a read: evicts the logits from L2 without leaving dirty lines
+            e0.record(stream)
+            call()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        us = [e0.elapsed_time(e1) * 1e3 for e0, e1 in evs]
+        rows_t = M if mode == "compact" else B * g
+        rows_d = 0
+        bonus = 0
+        if stochastic:
+            rows_d = (M - B) if mode == "compact" else B * (g - 1)
+            acc = st.accept_len.cpu().numpy()
+            bonus = int(np.sum(np.where(acc < w, 2, 1)))
+        algo = (rows_t + rows_d + bonus) * V * e
+        med = statistics.median(us)
+        out[f"{name}/{mode}"] = {
+            "B": B, "gamma": g, "V": V, "verify": "stochastic" if stochastic else "greedy",
+            "M": M, "algorithmic_bytes": algo, "us_median": med,
+            "us_p10_p90": [percentile(us, 10), percentile(us, 90)],
+            "gbs": algo / (med * 1e-6) / 1e9, "frac": algo / (med * 1e-6) / 1e9 / peak,
+            "frac_of_nominal_8tbs": algo / (med * 1e-6) / 1e9 / NOMINAL_HBM_GBS,
+            "launches": 3 if stochastic else 2, "reps": reps, "l2": "flushed between launches"}
+        del st, target, draft, call
+    del flush
     return out
 
 

@@ -58,6 +58,8 @@ extern "C" {
 #define DSPARK_STATUS_BAD_ROWS       0x20 /* a request's logits rows lie outside the buffer      */
 #define DSPARK_STATUS_BAD_TOKEN      0x40 /* a draft id outside [0,V): treated as rejected       */
 #define DSPARK_STATUS_BAD_LENGTH     0x80 /* accept_len / out_len outside range: clamped         */
+#define DSPARK_STATUS_STALL         0x100 /* a bounded in-kernel wait gave up: this call's verify
+                                             results are invalid (not expected in operation)   */
 
 /* ---- limits of this build ------------------------------------------------------------- */
 #define DSPARK_MAX_GAMMA        32     /* block width                                         */
@@ -240,6 +242,24 @@ int dspark_verify_scatter(dspark_mode mode, int stochastic,
                           int32_t* ceiling_len, float* row_prob, void* workspace,
                           size_t workspace_bytes, int32_t* out_tokens, int32_t* out_len,
                           int out_cap, int32_t* status, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * dspark_set_stream_kernel — which kernel streams the logits inside dspark_verify and
+ * dspark_verify_scatter, for every later call in this process:
+ *   DSPARK_STREAM_AUTO (0, the default): this build's choice;
+ *   DSPARK_STREAM_REGISTER (1): warps stream 16-byte loads into registers;
+ *   DSPARK_STREAM_BULK (2): a producer warp per CTA moves whole chunks into shared memory with
+ *     the TMA bulk-copy engine (cp.async.bulk, mbarrier completion) and four warps fold them;
+ *     used when the logit rows are 16-byte aligned and V % 8 == 0, else the register kernel.
+ * AUTO takes the bulk kernel when B*gamma rows of V logits reach 64 MB, else the register one.
+ * Both fold every chunk in the same order, so results are bit-identical whichever runs; only
+ * speed differs. Not thread-safe against concurrent verify calls. Returns DSPARK_OK or
+ * DSPARK_ERR_INVALID_ARG for an unknown value.
+ * ------------------------------------------------------------------------------------- */
+#define DSPARK_STREAM_AUTO      0
+#define DSPARK_STREAM_REGISTER  1
+#define DSPARK_STREAM_BULK      2
+int dspark_set_stream_kernel(int which);
 
 /* ---------------------------------------------------------------------------------------
  * dspark_observe — calibration and utilisation counters ("A2 method details", observability:

@@ -27,6 +27,9 @@ STATUS_BAD_COST = 0x10
 STATUS_BAD_ROWS = 0x20
 STATUS_BAD_TOKEN = 0x40
 STATUS_BAD_LENGTH = 0x80
+STATUS_STALL = 0x100
+
+STREAM_AUTO, STREAM_REGISTER, STREAM_BULK = 0, 1, 2
 
 MAX_GAMMA = 32
 MAX_CANDIDATES = 16384
@@ -67,6 +70,7 @@ SYMBOLS = {
     "dspark_verify_noalloc": ([_i, _i, _p, _i, _p, _i, _i, _p, _p, _p, _i, _i, ctypes.c_float,
                                _u64, _u64, _p, _p, _p, _p, _p, _p], _i),
     "dspark_observe": ([_p, _p, _p, _i, _i, _i, _p, _p, _p, _p], _i),
+    "dspark_set_stream_kernel": ([_i], _i),
     "dspark_last_error": ([], ctypes.c_char_p),
     "dspark_version": ([], _i),
 }
@@ -147,6 +151,12 @@ def _call(name: str, args, prepare: bool):
         return Prepared(name, args)
     _check(name, getattr(lib(), name)(*args))
     return None
+
+
+def set_stream_kernel(which: int) -> None:
+    """Which kernel streams the logits inside verify (STREAM_AUTO, STREAM_REGISTER,
+    STREAM_BULK); results are bit-identical, only speed differs."""
+    _check("dspark_set_stream_kernel", lib().dspark_set_stream_kernel(int(which)))
 
 
 def version() -> int:

@@ -350,6 +350,8 @@ int dspark_observe(const float* conf, const int32_t* accept_len, const int32_t* 
                                   status, stream);
 }
 
+int dspark_set_stream_kernel(int which) { return dspark::set_stream_kernel(which); }
+
 const char* dspark_last_error(void) { return dspark::last_error(); }
 
 int dspark_version(void) { return 100; }

@@ -1,0 +1,396 @@
+// verify_stream.cu — the HBM-bound part of dspark_verify: one partial per (row, chunk) unit.
+//
+// Two interchangeable persistent kernels (bit-identical partials: each lane folds its groups in
+// the same order through group_update):
+//   verify_stream_kernel — register streaming: each warp owns a contiguous run of units and
+//     reads each chunk with 16-byte read-only loads, eight in flight per lane (scalar loads
+//     when the rows are not 16-byte aligned or V % 8 != 0);
+//   verify_bulk_kernel — bulk-copy streaming: one producer warp per CTA moves whole chunks from
+//     HBM into a ring of shared-memory stages with cp.async.bulk (the TMA engine), completion
+//     counted on an mbarrier per stage; consumer warps fold the staged chunks.
+// The default picks the bulk kernel for launches of 64 MB and more at full size, the register
+// kernel below that (dspark_set_stream_kernel overrides).
+// Verify rules: lshu.cn DSpark article, 1.2 (greedy), 2.3 and 3.3 (min(1, p/q)); modes: "DSpark
+// in SGLang" (LMSYS blog summary), A2 verify-mode design.
+#include "verify_common.cuh"
+
+namespace dspark {
+namespace {
+
+template <int DT, bool STOCH>
+__device__ __forceinline__ void chunk_lane(const char* row, int v0, int v1, int vec, float s,
+                                           int lane, float& a, float& b, int& idx)
+{
+    constexpr int E = (DT == DSPARK_BF16) ? 2 : 4;
+    constexpr int Q = (DT == DSPARK_BF16) ? 1 : 2;   // uint4 per 8 elements
+    uint4 best = make_uint4(0, 0, 0, 0);             // bf16 greedy: vector holding the maximum
+    if (vec) {
+        const char* base = row + static_cast<int64_t>(v0) * E;
+        const int n8 = (v1 - v0) >> 3;               // groups of 8 elements
+        for (int g0 = lane; g0 < n8; g0 += 32 * kUnroll) {
+            uint4 buf[kUnroll * Q];
+#pragma unroll
+            for (int k = 0; k < kUnroll; ++k) {
+                const int g = g0 + k * 32;
+                if (g < n8) {
+#pragma unroll
+                    for (int h = 0; h < Q; ++h)
+                        buf[k * Q + h] = ld_stream16(base + (static_cast<int64_t>(g) * Q + h) * 16);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kUnroll; ++k) {
+                const int g = g0 + k * 32;
+                if (g < n8) group_update<DT, STOCH>(buf + k * Q, v0 + g * 8, s, a, b, idx, best);
+            }
+        }
+        if (!STOCH && DT == DSPARK_BF16 && idx != 0x7FFFFFFF) idx += bf16_first_equal(best, a);
+    } else {
+        for (int v = v0 + lane; v < v1; v += 32) {
+            const float x = load_logit<DT>(row, v);
+            if (!STOCH) {
+                if (x > a) { a = x; idx = v; }
+            } else {
+                if (x > a) {
+                    b *= ex2_approx((a - x) * s);
+                    a = x;
+                }
+                if (a != -INFINITY) b += ex2_approx((x - a) * s);
+            }
+        }
+    }
+}
+
+// Register-streaming variant: any alignment (scalar loads when the rows are not 16-byte
+// aligned or V % 8 != 0).
+template <int DT, bool STOCH>
+__global__ void __launch_bounds__(kStreamThreads)
+verify_stream_kernel(StreamArgs A)
+{
+    constexpr int E = (DT == DSPARK_BF16) ? 2 : 4;
+    pdl_wait_and_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = static_cast<int64_t>(blockIdx.x) * kStreamWarps + (threadIdx.x >> 5);
+    const int64_t GW = static_cast<int64_t>(gridDim.x) * kStreamWarps;
+    int64_t n_t;
+    const int64_t U = unit_count<STOCH>(A, n_t);
+    const int64_t u0 = gw * U / GW, u1 = (gw + 1) * U / GW;
+
+    int64_t job = u0 / A.nc;
+    int c = static_cast<int>(u0 - job * A.nc);
+    for (int64_t u = u0; u < u1; ++u) {
+        const UnitSrc src = unit_source<E>(A, job, c, n_t);
+        if (++c == A.nc) { c = 0; ++job; }
+        if (src.skip) continue;
+        const int v0 = src.c * A.C;
+        const int v1 = min(A.V, v0 + A.C);
+        float a = -INFINITY, bsum = 0.0f;
+        int idx = 0x7FFFFFFF;
+        chunk_lane<DT, STOCH>(src.row, v0, v1, A.vec, A.s, lane, a, bsum, idx);
+        write_partial<STOCH>(A, src, lane, a, bsum, idx);
+    }
+}
+
+// ---- bulk-copy streaming -----------------------------------------------------------------
+// A persistent grid (a few CTAs per SM) where each CTA owns a contiguous run of units. Warp
+// kBulkConsumers is the producer: its lane 0 walks the run and, for the k-th unit, waits until
+// stage k % S is free, arms that stage's "full" mbarrier with the unit's byte count and starts
+// one cp.async.bulk of the whole chunk into the stage. Consumer warp k % kBulkConsumers waits on the full barrier,
+// folds the staged chunk with the same per-lane order as the register kernel, releases the
+// stage on its "empty" barrier and writes the unit's partial. Every wait is bounded (about a
+// second of SM clock); a wait that gives up sets DSPARK_STATUS_STALL and the producer still
+// waits, bounded, for every copy it started before the CTA exits.
+// Measured on GB300 (dspark_verify_scatter alone, L2 flushed): 4 consumer warps and a 48 KB
+// ring (four CTAs per SM, up to 16 chunks of 8 KB in flight per SM) beat 8 consumers with
+// 64-128 KB rings; one CTA per SM reached only 4 TB/s.
+#ifndef DSPARK_BULK_CONSUMERS
+#define DSPARK_BULK_CONSUMERS 4
+#endif
+constexpr int kBulkConsumers = DSPARK_BULK_CONSUMERS;
+constexpr int kBulkThreads = (kBulkConsumers + 1) * 32;
+#ifndef DSPARK_BULK_RING_BYTES
+#define DSPARK_BULK_RING_BYTES (48 * 1024)
+#endif
+constexpr int kBulkRingBytes = DSPARK_BULK_RING_BYTES;   // stage ring per CTA
+// The bulk kernel serves launches whose full size (B*gamma rows of V logits) reaches this;
+// smaller ones are latency-bound and the register kernel starts faster.
+constexpr int64_t kBulkMinBytes = 64ll << 20;
+constexpr int kBulkMaxStages = 32;
+constexpr long long kWaitCycles = 1ll << 31;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Waits for the completion of the barrier phase of this parity; false once the deadline (an
+// SM clock value) has passed.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long deadline)
+{
+    while (true) {
+        uint32_t done;
+        asm volatile(
+            "{\n"
+            " .reg .pred p;\n"
+            " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n"
+            "}\n"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if (clock64() > deadline) return false;
+    }
+}
+
+// Global -> shared copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) by the
+// TMA engine; completion is counted on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// The producer's source of unit u: the same row as unit_source, with the request of a compact
+// draft job tracked by a cursor (units arrive in increasing order) instead of searched per unit.
+struct DraftCursor {
+    int b = -1;
+};
+
+template <int E>
+__device__ __forceinline__ const char* bulk_source(const StreamArgs& A, int64_t job, int64_t n_t,
+                                                   DraftCursor& cur)
+{
+    if (job < n_t) return static_cast<const char*>(A.target) + job * A.V * E;
+    const int L = A.gamma - 1;
+    const int64_t k = job - n_t;
+    int b, i;
+    if (A.mode == DSPARK_COMPACT) {
+        const int64_t r = k;
+        if (cur.b < 0) {                          // first draft job: search as unit_source does
+            int lo = 0, hi = A.B;
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (A.cu[mid] <= r) lo = mid; else hi = mid;
+            }
+            cur.b = lo;
+        }
+        while (cur.b + 1 < A.B && A.cu[cur.b + 1] <= r) ++cur.b;
+        b = cur.b;
+        i = static_cast<int>(r - A.cu[b]);
+        int w = A.windows[b];
+        w = w < 1 ? 1 : (w > A.gamma ? A.gamma : w);
+        if (i < 0 || i >= w - 1 || i >= L) return nullptr;   // last row of a request: no draft
+    } else {
+        const int kk = static_cast<int>(k);
+        b = kk / L;
+        i = kk - b * L;
+    }
+    return static_cast<const char*>(A.draft) + (static_cast<int64_t>(b) * L + i) * A.V * E;
+}
+
+template <int DT, bool STOCH>
+__global__ void __launch_bounds__(kBulkThreads, 1)
+verify_bulk_kernel(StreamArgs A, int stages, int stage_bytes)
+{
+    constexpr int E = (DT == DSPARK_BF16) ? 2 : 4;
+    constexpr int Q = (DT == DSPARK_BF16) ? 1 : 2;   // uint4 per 8 elements
+    extern __shared__ __align__(128) unsigned char ring[];
+    __shared__ __align__(8) uint64_t full_bar[kBulkMaxStages];
+    __shared__ __align__(8) uint64_t empty_bar[kBulkMaxStages];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(smem_addr(&full_bar[s]), 1);
+            mbar_init(smem_addr(&empty_bar[s]), 1);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    pdl_wait_and_trigger();
+    int64_t n_t;
+    const int64_t U = unit_count<STOCH>(A, n_t);
+    const int64_t u0 = static_cast<int64_t>(blockIdx.x) * U / gridDim.x;
+    const int64_t u1 = static_cast<int64_t>(blockIdx.x + 1) * U / gridDim.x;
+    const int64_t K = u1 - u0;
+    const long long deadline = clock64() + kWaitCycles;
+
+    if (warp == kBulkConsumers) {                     // producer warp: lane 0 issues
+        if (lane != 0) return;
+        bool ok = true;
+        DraftCursor cur;
+        int64_t job = u0 / A.nc;
+        int c = static_cast<int>(u0 - job * A.nc);
+        int s = 0;
+        uint32_t ph = 0;                              // parity of this use of stage s
+        int64_t k = 0;
+        for (; k < K; ++k) {
+            const uint32_t full = smem_addr(&full_bar[s]);
+            if (k >= stages && !mbar_wait(smem_addr(&empty_bar[s]), ph ^ 1u, deadline)) {
+                ok = false;
+                break;
+            }
+            const char* row = bulk_source<E>(A, job, n_t, cur);
+            if (row == nullptr) {
+                mbar_arrive(full);                    // a skipped unit: complete the phase
+            } else {
+                const int v0 = c * A.C;
+                const int v1 = min(A.V, v0 + A.C);
+                const uint32_t bytes = static_cast<uint32_t>(v1 - v0) * E;
+                mbar_arrive_expect_tx(full, bytes);
+                bulk_load(smem_addr(ring + static_cast<size_t>(s) * stage_bytes),
+                          row + static_cast<int64_t>(v0) * E, bytes, full);
+            }
+            if (++c == A.nc) { c = 0; ++job; }
+            if (++s == stages) { s = 0; ph ^= 1u; }
+        }
+        // every started copy must land before this CTA may exit
+        const int64_t issued = k;
+        const long long drain = clock64() + kWaitCycles;
+        for (int s = 0; s < stages && s < issued; ++s) {
+            const int64_t uses = (issued - s + stages - 1) / stages;
+            if (!mbar_wait(smem_addr(&full_bar[s]), static_cast<uint32_t>((uses - 1) & 1), drain))
+                ok = false;
+        }
+        if (!ok) raise_status(A.status, DSPARK_STATUS_STALL);
+        return;
+    }
+
+    int64_t job = (u0 + warp) / A.nc;
+    int c = static_cast<int>(u0 + warp - job * A.nc);
+    int s = warp;                                     // stages % kBulkConsumers == 0
+    uint32_t ph = 0;
+    for (int64_t k = warp; k < K; k += kBulkConsumers) {
+        bool ok = mbar_wait(smem_addr(&full_bar[s]), ph, deadline);
+        if (!__all_sync(0xffffffffu, ok)) {
+            if (lane == 0) raise_status(A.status, DSPARK_STATUS_STALL);
+            break;
+        }
+        const UnitSrc src = unit_source<E>(A, job, c, n_t);
+        float a = -INFINITY, bsum = 0.0f;
+        int idx = 0x7FFFFFFF;
+        if (!src.skip) {
+            const int v0 = src.c * A.C;
+            const int n8 = (min(A.V, v0 + A.C) - v0) >> 3;
+            const uint4* q = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(s) * stage_bytes);
+            uint4 best = make_uint4(0, 0, 0, 0);
+            for (int g = lane; g < n8; g += 32) {
+                uint4 v[Q];
+#pragma unroll
+                for (int h = 0; h < Q; ++h) v[h] = q[g * Q + h];
+                group_update<DT, STOCH>(v, v0 + g * 8, A.s, a, bsum, idx, best);
+            }
+            if (!STOCH && DT == DSPARK_BF16 && idx != 0x7FFFFFFF) idx += bf16_first_equal(best, a);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&empty_bar[s]));
+        if (!src.skip) write_partial<STOCH>(A, src, lane, a, bsum, idx);
+        c += kBulkConsumers;
+        while (c >= A.nc) { c -= A.nc; ++job; }
+        s += kBulkConsumers;
+        if (s >= stages) { s -= stages; ph ^= 1u; }
+    }
+}
+
+}  // namespace
+
+namespace {
+
+int g_stream_kernel = DSPARK_STREAM_AUTO;   // dspark_set_stream_kernel
+
+template <int DT, bool STOCH>
+int launch_stream_t(const StreamArgs& sa, int64_t max_units, cudaStream_t stream)
+{
+    constexpr int E = (DT == DSPARK_BF16) ? 2 : 4;
+    DeviceInfo dev;
+    int rc = current_device(&dev);
+    if (rc != DSPARK_OK) return rc;
+    int which = g_stream_kernel;
+    if (which == DSPARK_STREAM_AUTO)
+        which = sa.rows_max * sa.V * E >= kBulkMinBytes ? DSPARK_STREAM_BULK : DSPARK_STREAM_REGISTER;
+    if (which == DSPARK_STREAM_BULK && sa.vec) {
+        const int stage_bytes = static_cast<int>(align_up(static_cast<size_t>(sa.C) * E, 128));
+        int stages = (kBulkRingBytes / stage_bytes) / kBulkConsumers * kBulkConsumers;
+        if (stages > kBulkMaxStages) stages = kBulkMaxStages;
+        if (stages >= kBulkConsumers) {
+            const size_t smem = static_cast<size_t>(stages) * stage_bytes;
+            static thread_local int bulk_device = -1;
+            static thread_local int bulk_occ = 0;
+            if (bulk_device != dev.device) {
+                if (cudaFuncSetAttribute(verify_bulk_kernel<DT, STOCH>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kBulkRingBytes) != cudaSuccess)
+                    return check_launch("verify (bulk stream shared-memory opt-in)");
+                if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                        &bulk_occ, verify_bulk_kernel<DT, STOCH>, kBulkThreads, kBulkRingBytes) !=
+                    cudaSuccess)
+                    return check_launch("verify (bulk stream occupancy query)");
+                if (bulk_occ < 1) bulk_occ = 1;
+                bulk_device = dev.device;
+            }
+            int64_t grid = static_cast<int64_t>(dev.sm_count) * bulk_occ;
+            const int64_t need = ceil_div(max_units, kBulkConsumers);
+            if (grid > need) grid = need;
+            if (grid < 1) grid = 1;
+            return launch_pdl("verify (bulk stream)", verify_bulk_kernel<DT, STOCH>,
+                              dim3(static_cast<unsigned>(grid)), dim3(kBulkThreads), smem, stream,
+                              sa, stages, stage_bytes);
+        }
+    }
+    static thread_local int occ_device = -1;
+    static thread_local int occ = 0;
+    if (occ_device != dev.device) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, verify_stream_kernel<DT, STOCH>,
+                                                          kStreamThreads, 0) != cudaSuccess)
+            return check_launch("verify (occupancy query)");
+        if (occ < 1) occ = 1;
+        occ_device = dev.device;
+    }
+    int64_t grid = static_cast<int64_t>(dev.sm_count) * occ;
+    const int64_t need = ceil_div(max_units, kStreamWarps);
+    if (grid > need) grid = need;
+    if (grid < 1) grid = 1;
+    return launch_pdl("verify (stream)", verify_stream_kernel<DT, STOCH>,
+                      dim3(static_cast<unsigned>(grid)), dim3(kStreamThreads), 0, stream, sa);
+}
+
+}  // namespace
+
+int set_stream_kernel(int which)
+{
+    if (which != DSPARK_STREAM_AUTO && which != DSPARK_STREAM_REGISTER && which != DSPARK_STREAM_BULK)
+        return fail(DSPARK_ERR_INVALID_ARG, "dspark_set_stream_kernel: unknown kernel %d", which);
+    g_stream_kernel = which;
+    return DSPARK_OK;
+}
+
+int launch_verify_stream(int dtype, bool stochastic, const StreamArgs& sa, int64_t max_units,
+                         cudaStream_t stream)
+{
+    if (dtype == DSPARK_BF16)
+        return stochastic ? launch_stream_t<DSPARK_BF16, true>(sa, max_units, stream)
+                          : launch_stream_t<DSPARK_BF16, false>(sa, max_units, stream);
+    return stochastic ? launch_stream_t<DSPARK_F32, true>(sa, max_units, stream)
+                      : launch_stream_t<DSPARK_F32, false>(sa, max_units, stream);
+}
+
+}  // namespace dspark

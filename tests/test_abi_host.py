@@ -99,3 +99,10 @@ def test_workspace_size_is_a_function_of_sizes(lib):
     assert g % 256 == 0
     assert bd.dspark_verify_workspace_bytes(-1, 8, 10, False) == 0
     assert "bad sizes" in bd.last_error()
+
+
+def test_stream_kernel_setting_is_checked(lib):
+    from speculative_decoding_ragged_gb300 import _binding as bd
+    assert lib.dspark_set_stream_kernel(7) == -1 and "unknown kernel 7" in bd.last_error()
+    assert lib.dspark_set_stream_kernel(bd.STREAM_BULK) == 0
+    assert lib.dspark_set_stream_kernel(bd.STREAM_AUTO) == 0
