@@ -39,7 +39,7 @@ NOMINAL_HBM_GBS = 8000.0     # the GB300's nominal HBM3e bandwidth, for context 
 UNIT = "rows/s"
 WORKLOAD = "large_vocab_mixed"
 FALLBACK_HBM_GBS = 6800.0
-PROFILE = os.path.join(ROOT, "profiles", "verify_stream_large_vocab_mixed.md")
+PROFILE = os.path.join(ROOT, "profiles", "verify_large_vocab_mixed.md")
 N_BATCHES = 3
 
 
@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batches", type=int, default=N_BATCHES)
     ap.add_argument("--latency-steps", type=int, default=10000)
+    ap.add_argument("--stream-kernel", default="auto", choices=["auto", "register", "bulk"],
+                    help="which logit-streaming kernel verify uses (results are identical)")
     ap.add_argument("--config-reps", type=int, default=30,
                     help="timed verify calls per extra workload leg (0: skip the legs)")
     ap.add_argument("--event-every", type=int, default=8,
@@ -224,6 +226,9 @@ def run_native(args, rank, world, local):
     build.build()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    from speculative_decoding_ragged_gb300 import _binding as bd
+    bd.set_stream_kernel({"auto": bd.STREAM_AUTO, "register": bd.STREAM_REGISTER,
+                          "bulk": bd.STREAM_BULK}[args.stream_kernel])
     wl = synth.WORKLOADS[args.workload]
     seeds = [1000 * rank + i for i in range(args.batches)]
     st = DSparkStep(wl.B, wl.gamma, wl.V, wl.tiers, wl.bias,
@@ -328,6 +333,7 @@ def run_native(args, rank, world, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "B": wl.B, "gamma": wl.gamma, "V": wl.V,
                    "mode": "compact", "verify": "greedy", "logits": "bf16",
+                   "stream_kernel": args.stream_kernel,
                    "batches_rotating": nb, "rows_per_step_mean": rows / K / world,
                    "l2": "inputs larger than L2: each step reads >=300 MB of packed logits, "
                          f"{nb} batches rotate",
