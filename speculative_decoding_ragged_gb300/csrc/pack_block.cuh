@@ -10,9 +10,13 @@
 //      and one tier per thread (n_tiers <= 1024), so the block pays one memory round trip;
 //   2. windows clamped to [1, gamma]; block-wide exclusive scan -> cu_seqlens;
 //   3. tier = min over tiers >= M (tiers need not be sorted);
-//   4. each thread writes its requests' rows (token, request, position); padding rows up to
-//      the tier get 0 / -1 / -1.
+//   4. cu_seqlens into shared memory; then each thread writes whole rows (token, request,
+//      position), finding a row's request by binary search over cu, so that the stores of a
+//      warp are contiguous; padding rows up to the tier get 0 / -1 / -1.
 // kLdg: windows may be read through the read-only path (false when this CTA wrote them).
+// win_count (shared memory, or nullptr): the scheduler's per-request counts, window = 1 + count,
+// read instead of the windows array by the fused schedule-and-pack kernel, which also passes
+// each thread's tier (tiers[tid], or INT_MAX past n_tiers) loaded at its start as tier_pre.
 #pragma once
 #include "common.cuh"
 
@@ -21,8 +25,9 @@ namespace dspark {
 constexpr int kPackThreads = 1024;
 
 template <bool kLdg>
-__device__ __forceinline__ int pack_load_window(const int32_t* windows, int b)
+__device__ __forceinline__ int pack_load_window(const int32_t* windows, const int* win_count, int b)
 {
+    if (win_count != nullptr) return 1 + win_count[b];
     return kLdg ? __ldg(windows + b) : windows[b];
 }
 
@@ -33,27 +38,25 @@ __device__ __forceinline__ void pack_block(const int32_t* windows, const int32_t
                                            int32_t* __restrict__ packed_ids,
                                            int32_t* __restrict__ row_req,
                                            int32_t* __restrict__ row_pos, int packed_cap,
-                                           int32_t* __restrict__ meta, int32_t* __restrict__ status)
+                                           int32_t* __restrict__ meta, int32_t* __restrict__ status,
+                                           const int* win_count = nullptr,
+                                           const int* tier_pre = nullptr)
 {
     constexpr int kWarps = kPackThreads / 32;
     __shared__ int warp_total[kWarps];
     __shared__ int tier_s;
+    __shared__ int cu_s[DSPARK_MAX_BATCH + 1];
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
 
     // 1. loads
-    const int tier_v = tid < n_tiers ? __ldg(tiers + tid) : INT_MAX;
+    const int tier_v = tier_pre != nullptr ? *tier_pre
+                                           : (tid < n_tiers ? __ldg(tiers + tid) : INT_MAX);
     const int items = (B + kPackThreads - 1) / kPackThreads;
     const int b0 = tid * items;
-    int tok[DSPARK_MAX_GAMMA];
     int w_first = 1;
-    if (items == 1 && b0 < B) {
-        w_first = pack_load_window<kLdg>(windows, b0);
-#pragma unroll
-        for (int i = 0; i < DSPARK_MAX_GAMMA; ++i)
-            if (i < gamma) tok[i] = __ldg(tokens + static_cast<int64_t>(b0) * gamma + i);
-    }
+    if (items == 1 && b0 < B) w_first = pack_load_window<kLdg>(windows, win_count, b0);
     if (tid == 0) tier_s = INT_MAX;
 
     // 2. exclusive scan of the clamped windows
@@ -62,7 +65,7 @@ __device__ __forceinline__ void pack_block(const int32_t* windows, const int32_t
     for (int it = 0; it < items; ++it) {
         const int b = b0 + it;
         if (b >= B) break;
-        int w = items == 1 ? w_first : pack_load_window<kLdg>(windows, b);
+        int w = items == 1 ? w_first : pack_load_window<kLdg>(windows, win_count, b);
         if (w < 1 || w > gamma) {
             bad = DSPARK_STATUS_BAD_WINDOW;
             w = w < 1 ? 1 : gamma;
@@ -100,36 +103,31 @@ __device__ __forceinline__ void pack_block(const int32_t* windows, const int32_t
     }
     if (tier > packed_cap) bad |= DSPARK_STATUS_PACK_CAPACITY;
 
-    // 4. rows of this thread's requests, then padding
+    // 4. cu_seqlens, then the rows: row r belongs to the largest b with cu[b] <= r
     int acc = excl;
     for (int it = 0; it < items; ++it) {
         const int b = b0 + it;
         if (b >= B) break;
-        int w = items == 1 ? w_first : pack_load_window<kLdg>(windows, b);
+        int w = items == 1 ? w_first : pack_load_window<kLdg>(windows, win_count, b);
         w = w < 1 ? 1 : (w > gamma ? gamma : w);
+        cu_s[b] = acc;
         cu_out[b] = acc;
-        if (items == 1) {
-#pragma unroll
-            for (int i = 0; i < DSPARK_MAX_GAMMA; ++i) {
-                const int r = acc + i;
-                if (i < w && r < packed_cap) {
-                    packed_ids[r] = tok[i];
-                    if (row_req) row_req[r] = b;
-                    if (row_pos) row_pos[r] = i;
-                }
-            }
-        } else {
-            for (int i = 0; i < w; ++i) {
-                const int r = acc + i;
-                if (r >= packed_cap) break;
-                packed_ids[r] = __ldg(tokens + static_cast<int64_t>(b) * gamma + i);
-                if (row_req) row_req[r] = b;
-                if (row_pos) row_pos[r] = i;
-            }
-        }
         acc += w;
     }
     if (tid == 0) cu_out[B] = M;
+    __syncthreads();
+    const int rows = min(M, packed_cap);
+    for (int r = tid; r < rows; r += kPackThreads) {
+        int lo = 0, hi = B;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (cu_s[mid] <= r) lo = mid; else hi = mid;
+        }
+        const int i = r - cu_s[lo];
+        packed_ids[r] = __ldg(tokens + static_cast<int64_t>(lo) * gamma + i);
+        if (row_req) row_req[r] = lo;
+        if (row_pos) row_pos[r] = i;
+    }
     const int rows_pad = min(tier, packed_cap);
     for (int r = M + tid; r < rows_pad; r += kPackThreads) {
         packed_ids[r] = 0;

@@ -35,7 +35,8 @@ constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMergeMax = 4096;          // ping-pong merge buffers up to this many words
 constexpr int kMergeItems = kMergeMax / kThreads;
-constexpr int kBuckets = 1056;           // key 0, then 32 buckets per power of two of the key
+constexpr int kBuckets = 4096;           // 128 buckets per power of two of the key (keys 0, 1 share)
+constexpr int kBucketsPerThread = kBuckets / 1024;
 constexpr int kBucketMax = 64;           // larger buckets (many equal keys): merge instead
 constexpr float kScreen = 1.0f - 1e-5f;  // fp32 screen: candidates within 1e-5 of the best
 constexpr float kTmin = 1e-20f, kTmax = 1e20f;   // T range the fp32 screen judges
@@ -112,12 +113,20 @@ __device__ __forceinline__ void write_run(const float* __restrict__ conf, int b,
 }
 
 // Order-preserving bucket of a 32-bit key (equal keys share a bucket): the fp32 exponent and
-// top five mantissa bits of the key truncated to fp32, so a bucket spans about 3 % of its keys.
+// top seven mantissa bits of the key truncated to fp32, so a bucket spans under 1 % of its
+// keys; keys 0 and 1 share bucket 0.
 __device__ __forceinline__ int key_bucket(uint32_t k32)
 {
     if (k32 == 0) return 0;
     const uint32_t f = __float_as_uint(__uint2float_rz(k32));
-    return static_cast<int>((f >> 18) - (127u << 5)) + 1;
+    return static_cast<int>((f >> 16) - (127u << 7));
+}
+
+// A key and its candidate index as one word that orders like (key descending, index
+// ascending) when compared as an unsigned integer, larger first.
+__device__ __forceinline__ uint64_t rank_word(uint32_t k32, int idx)
+{
+    return (static_cast<uint64_t>(k32) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(idx));
 }
 
 __device__ __forceinline__ uint64_t key_value(uint32_t k32)
@@ -134,12 +143,15 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
                 int32_t* __restrict__ status, PackArgs pk)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    // MERGE: keys [2][n] (u32) and indices [2][n]; else words [n_pad] (u64). Then count [B].
+    // MERGE: keys ksrc [n] (u32), indices isrc [n], then the ping-pong pair kdst, idst (the
+    // bucket path uses that second half as n 64-bit rank words); else words [n_pad] (u64).
+    // Then count [B].
     uint64_t* word = reinterpret_cast<uint64_t*>(smem_raw);
     uint32_t* ksrc = reinterpret_cast<uint32_t*>(smem_raw);
-    uint32_t* kdst = ksrc + n;
-    int* isrc = reinterpret_cast<int*>(kdst + n);
-    int* idst = isrc + n;
+    int* isrc = reinterpret_cast<int*>(ksrc + n);
+    uint32_t* kdst = reinterpret_cast<uint32_t*>(isrc + n);
+    int* idst = reinterpret_cast<int*>(kdst + n);
+    uint64_t* rword = reinterpret_cast<uint64_t*>(kdst);   // 8n-byte aligned: offset 8n
     int* count = MERGE ? (idst + n) : reinterpret_cast<int*>(word + n_pad);
     __shared__ uint64_t warp_total[kWarps];
     __shared__ uint64_t red_obj[kWarps];
@@ -148,15 +160,23 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
     __shared__ int k_best;
     __shared__ float f_best;
     __shared__ double t0_s;
-    __shared__ int bucket_cnt[MERGE ? kBuckets : 1];
-    __shared__ int bucket_start[MERGE ? kBuckets : 1];
-    __shared__ int bucket_fill[MERGE ? kBuckets : 1];
+    __shared__ __align__(16) int bucket_cnt[MERGE ? kBuckets : 4];
+    __shared__ __align__(16) int bucket_start[MERGE ? kBuckets : 4];
     __shared__ int warp_int[kWarps];
 
     pdl_wait_and_trigger();
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
+    int tier_pre = INT_MAX;
+    if (PACK) {
+        // the pack's inputs are read only at the end: its tier now, its tokens into L2
+        const char* tp = reinterpret_cast<const char*>(pk.tokens);
+        const int64_t tb = static_cast<int64_t>(B) * (L + 1) * 4;
+        for (int64_t off = static_cast<int64_t>(tid) * 128; off < tb; off += kThreads * 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(tp + off));
+        if (tid < pk.n_tiers) tier_pre = __ldg(pk.tiers + tid);
+    }
     constexpr int kMaxItems = MERGE ? kMergeItems : DSPARK_MAX_CANDIDATES / kThreads;
     const int items = (n + kThreads - 1) / kThreads;   // positions per thread, contiguous
     const int p0 = tid * items;
@@ -179,10 +199,7 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
         count[b] = 0;
     }
     if (MERGE)
-        for (int j = tid; j < kBuckets; j += kThreads) {
-            bucket_cnt[j] = 0;
-            bucket_fill[j] = 0;
-        }
+        for (int j = tid; j < kBuckets; j += kThreads) bucket_cnt[j] = 0;
     if (!MERGE)
         for (int i = n + tid; i < n_pad; i += kThreads) word[i] = 0;   // sorts after all words
     __syncthreads();
@@ -196,11 +213,14 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
         int big = 0;
         for (int j = tid; j < kBuckets; j += kThreads) big |= bucket_cnt[j] > kBucketMax;
         if (!__syncthreads_or(big)) {
-            // bucket starts in descending bucket order; thread t owns reversed buckets 2t, 2t+1
-            const int j0 = kBuckets - 1 - 2 * tid, j1 = j0 - 1;
-            const int a0 = j0 >= 0 ? bucket_cnt[j0] : 0;
-            const int a1 = j1 >= 0 ? bucket_cnt[j1] : 0;
-            int incl_b = a0 + a1;
+            // bucket starts in descending bucket order; thread t owns the reversed buckets
+            // kBuckets - 1 - (kBucketsPerThread * t + m), m = 0..kBucketsPerThread-1
+            static_assert(kBucketsPerThread == 4, "one 16-byte vector of counts per thread");
+            const int jv = kBuckets - 4 - 4 * tid;            // the thread's four buckets
+            const int4 cv = *reinterpret_cast<const int4*>(bucket_cnt + jv);
+            const int a[4] = {cv.w, cv.z, cv.y, cv.x};        // descending bucket order
+            const int own = (cv.x + cv.y) + (cv.z + cv.w);
+            int incl_b = own;
             for (int off = 1; off < 32; off <<= 1) {
                 const int v = __shfl_up_sync(0xffffffffu, incl_b, off);
                 if (lane >= off) incl_b += v;
@@ -216,32 +236,27 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
                 warp_int[lane] = t;
             }
             __syncthreads();
-            const int ex = incl_b - (a0 + a1) + (warp > 0 ? warp_int[warp - 1] : 0);
-            if (j0 >= 0) bucket_start[j0] = ex;
-            if (j1 >= 0) bucket_start[j1] = ex + a0;
+            const int ex = incl_b - own + (warp > 0 ? warp_int[warp - 1] : 0);
+            *reinterpret_cast<int4*>(bucket_start + jv) =
+                make_int4(ex + a[0] + a[1] + a[2], ex + a[0] + a[1], ex + a[0], ex);
             __syncthreads();
-            // scatter into the bucket ranges (any order inside a bucket)
+            // scatter rank words into the bucket ranges (any order inside a bucket); afterwards
+            // bucket_start[j] holds the end of bucket j
             for (int p = tid; p < n; p += kThreads) {
                 const uint32_t k = ksrc[p];
-                const int j = key_bucket(k);
-                const int q = bucket_start[j] + atomicAdd(&bucket_fill[j], 1);
-                kdst[q] = k;
-                idst[q] = p;                      // runs start in index order
+                const int q = atomicAdd(&bucket_start[key_bucket(k)], 1);
+                rword[q] = rank_word(k, p);      // runs start in index order: isrc[p] == p
             }
             __syncthreads();
-            // exact place inside the bucket: key descending, then index ascending
+            // exact place inside the bucket: one unsigned compare orders (key desc, index asc)
             for (int q = tid; q < n; q += kThreads) {
-                const uint32_t x = kdst[q];
-                const int xi = idst[q];
-                const int j = key_bucket(x);
-                const int s0 = bucket_start[j], c = bucket_cnt[j];
+                const uint64_t x = rword[q];
+                const int j = key_bucket(static_cast<uint32_t>(x >> 32));
+                const int c = bucket_cnt[j], s0 = bucket_start[j] - c;
                 int r = 0;
-                for (int t = s0; t < s0 + c; ++t) {
-                    const uint32_t y = kdst[t];
-                    r += (y > x) || (y == x && idst[t] < xi);
-                }
-                ksrc[s0 + r] = x;
-                isrc[s0 + r] = xi;
+                for (int t = s0; t < s0 + c; ++t) r += rword[t] > x;
+                ksrc[s0 + r] = static_cast<uint32_t>(x >> 32);
+                isrc[s0 + r] = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(x));
             }
             __syncthreads();
             sorted = true;
@@ -440,10 +455,11 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
     __syncthreads();
     for (int b = tid; b < B; b += kThreads) windows[b] = 1 + count[b];
     if (PACK) {
+        // count[] is complete (barrier above) and the pack reads the windows from it
         static_assert(kPackThreads == kThreads, "the pack body runs on the scheduler's CTA");
-        __syncthreads();   // every window written (and visible to the block) before the pack
         pack_block<false>(windows, pk.tokens, B, L + 1, pk.tiers, pk.n_tiers, pk.cu,
-                          pk.packed_ids, pk.row_req, pk.row_pos, pk.packed_cap, pk.meta, status);
+                          pk.packed_ids, pk.row_req, pk.row_pos, pk.packed_cap, pk.meta, status,
+                          count, &tier_pre);
     }
 }
 
