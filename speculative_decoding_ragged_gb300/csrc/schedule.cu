@@ -479,6 +479,176 @@ __global__ void schedule_trivial_kernel(int B, double bias, const double* __rest
     }
 }
 
+// ---- one warp for at most 32 candidates ---------------------------------------------------
+// The same outputs as schedule_kernel (and, with PACK, as the pack body) when n = B*(gamma-1)
+// <= 32: lane i holds candidate i; the warp sorts the candidates' rank words with a shuffle
+// bitonic network, scans their keys, evaluates the objective of every K exactly in fp64 (at
+// most 33 divisions, one or two per lane) and reduces with the same comparator, so no block
+// barrier is needed anywhere. A batch of one request lives here.
+constexpr int kSmallMax = 32;
+
+template <bool PACK>
+__global__ void __launch_bounds__(32, 1)
+schedule_small_kernel(const float* __restrict__ conf, int B, int L, double bias,
+                      const double* __restrict__ alpha, const double* __restrict__ theta,
+                      int32_t* __restrict__ windows, int32_t* __restrict__ k_star,
+                      int32_t* __restrict__ status, PackArgs pk)
+{
+    __shared__ int cu_s[kSmallMax];
+    pdl_wait_and_trigger();
+    const unsigned full = 0xffffffffu;
+    const int lane = threadIdx.x;
+    const int n = B * L;
+    const int gamma = L + 1;
+    if (PACK) {
+        const char* tp = reinterpret_cast<const char*>(pk.tokens);
+        const int tb = B * gamma * 4;
+        for (int off = lane * 128; off < tb; off += 32 * 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(tp + off));
+    }
+    // inputs: this lane's confidences (its request's first j_own + 1), theta of K = lane + 1
+    const uint64_t* theta_bits = reinterpret_cast<const uint64_t*>(theta);
+    const bool mine = lane < n;
+    const int b_own = mine ? lane / L : 0;
+    const int j_own = mine ? lane - b_own * L : -1;
+    float c[DSPARK_MAX_GAMMA - 1];
+#pragma unroll
+    for (int j = 0; j < DSPARK_MAX_GAMMA - 1; ++j)
+        if (j <= j_own) c[j] = __ldg(conf + static_cast<int64_t>(b_own) * L + j);
+    const uint64_t th_k = mine ? __ldg(theta_bits + B + lane + 1) : 0;
+    const uint64_t th_0 = __ldg(theta_bits + B);
+    const double t0 = bias + __ldg(alpha + B);
+
+    // 1. survival key and rank word of the lane's candidate
+    float sv = 1.0f;
+#pragma unroll
+    for (int j = 0; j < DSPARK_MAX_GAMMA - 1; ++j)
+        if (j <= j_own) sv = __fmul_rn(sv, fminf(fmaxf(c[j], 0.0f), 1.0f));   // NaN -> 0
+    const uint32_t k32 = sv >= 1.0f ? 0xFFFFFFFFu : __float2uint_rn(__fmul_rn(sv, 4294967296.0f));
+    uint64_t w = mine ? rank_word(k32, lane) : 0ull;   // 0 sorts after every candidate
+
+    // 2. bitonic sort of the 32 words, descending
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const uint64_t o = __shfl_xor_sync(full, w, j);
+            const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
+            w = keep_max ? (w > o ? w : o) : (w < o ? w : o);
+        }
+    }
+    const uint32_t kp = static_cast<uint32_t>(w >> 32);
+    const int idx = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(w));
+
+    // 3. S(K) for K = lane + 1: inclusive scan of the sorted keys
+    uint64_t S = lane < n ? key_value(kp) : 0ull;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint64_t v = __shfl_up_sync(full, S, off);
+        if (lane >= off) S += v;
+    }
+
+    // 4. exact objectives and the argmax (larger objective, then smaller K)
+    const uint64_t base_E = static_cast<uint64_t>(B) << 32;
+    uint64_t best_obj = 0;
+    int best_k = -1;
+    if (lane < n) {
+        const double T = t0 + __longlong_as_double(th_k);
+        if (T > 0.0 && T < INFINITY) {
+            best_obj = __double_as_longlong(static_cast<double>(base_E + S) / T);
+            best_k = lane + 1;
+        }
+    }
+    if (lane == 0) {
+        const double T = t0 + __longlong_as_double(th_0);
+        if (T > 0.0 && T < INFINITY) {
+            const uint64_t o = __double_as_longlong(static_cast<double>(base_E) / T);
+            if (better(o, 0, best_obj, best_k)) {
+                best_obj = o;
+                best_k = 0;
+            }
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const uint64_t o = __shfl_xor_sync(full, best_obj, off);
+        const int kk = __shfl_xor_sync(full, best_k, off);
+        if (better(o, kk, best_obj, best_k)) {
+            best_obj = o;
+            best_k = kk;
+        }
+    }
+    int bits = 0;
+    if (best_k < 0) {
+        bits |= DSPARK_STATUS_BAD_COST;
+        best_k = 0;
+    }
+    const int K_star = best_k;
+
+    // 5. windows: 1 + the request's candidates among the first K*
+    const bool in = lane < K_star;
+    const int req = in ? idx / L : -1;
+    int cnt = 0;
+    for (int b = 0; b < B; ++b) {
+        const int cb = __popc(__ballot_sync(full, req == b));
+        if (lane == b) cnt = cb;
+    }
+    if (lane < B) windows[lane] = 1 + cnt;
+    if (lane == 0) *k_star = K_star;
+
+    if (PACK) {
+        // front-pack: cu by a warp scan of the windows, tier, rows, padding (as pack_block)
+        const int wv = lane < B ? 1 + cnt : 0;
+        int incl = wv;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(full, incl, off);
+            if (lane >= off) incl += v;
+        }
+        const int M = __shfl_sync(full, incl, 31);
+        const int excl = incl - wv;
+        if (lane < B) {
+            cu_s[lane] = excl;
+            pk.cu[lane] = excl;
+        }
+        if (lane == 0) pk.cu[B] = M;
+        int best = INT_MAX;
+        for (int t = lane; t < pk.n_tiers; t += 32) {
+            const int tv = __ldg(pk.tiers + t);
+            if (tv >= M && tv < best) best = tv;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) best = min(best, __shfl_xor_sync(full, best, off));
+        int tier = best;
+        if (tier == INT_MAX) {
+            tier = M;
+            bits |= DSPARK_STATUS_TIER_OVERFLOW;
+        }
+        if (tier > pk.packed_cap) bits |= DSPARK_STATUS_PACK_CAPACITY;
+        __syncwarp();
+        const int rows = min(M, pk.packed_cap);
+        for (int r = lane; r < rows; r += 32) {
+            int b = 0;
+            while (b + 1 < B && cu_s[b + 1] <= r) ++b;
+            const int i = r - cu_s[b];
+            pk.packed_ids[r] = __ldg(pk.tokens + static_cast<int64_t>(b) * gamma + i);
+            if (pk.row_req) pk.row_req[r] = b;
+            if (pk.row_pos) pk.row_pos[r] = i;
+        }
+        const int rows_pad = min(tier, pk.packed_cap);
+        for (int r = M + lane; r < rows_pad; r += 32) {
+            pk.packed_ids[r] = 0;
+            if (pk.row_req) pk.row_req[r] = -1;
+            if (pk.row_pos) pk.row_pos[r] = -1;
+        }
+        if (lane == 0) {
+            pk.meta[0] = M;
+            pk.meta[1] = tier;
+        }
+    }
+    if (lane == 0) raise_status(status, bits);
+}
+
 }  // namespace
 
 namespace {
@@ -538,6 +708,10 @@ int launch_schedule(const float* conf, int B, int gamma, const dspark_cost* cost
                           cost->bias, cost->alpha, cost->theta, windows, k_star, status);
     }
     const PackArgs none = {};
+    if (B * L <= kSmallMax)
+        return launch_pdl("schedule", schedule_small_kernel<false>, dim3(1), dim3(32), 0, stream,
+                          conf, B, L, cost->bias, cost->alpha, cost->theta, windows, k_star,
+                          status, none);
     return launch_schedule_kernel<false>("dspark_schedule", conf, B, L, cost, windows, k_star,
                                          status, none, stream);
 }
@@ -546,6 +720,10 @@ int launch_schedule_pack(const float* conf, int B, int gamma, const dspark_cost*
                          int32_t* windows, int32_t* k_star, const PackArgs& pk, int32_t* status,
                          cudaStream_t stream)
 {
+    if (B * (gamma - 1) <= kSmallMax)
+        return launch_pdl("schedule_pack", schedule_small_kernel<true>, dim3(1), dim3(32), 0,
+                          stream, conf, B, gamma - 1, cost->bias, cost->alpha, cost->theta,
+                          windows, k_star, status, pk);
     return launch_schedule_kernel<true>("dspark_schedule_pack", conf, B, gamma - 1, cost,
                                         windows, k_star, status, pk, stream);
 }

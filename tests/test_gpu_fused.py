@@ -39,7 +39,8 @@ def _host(o):
 
 
 @pytest.mark.parametrize("B,gamma", [(1, 2), (1, 16), (4, 4), (33, 8), (256, 8), (600, 8),
-                                     (1000, 17), (8192, 2), (2048, 9)])
+                                     (1000, 17), (8192, 2), (2048, 9), (32, 2), (2, 17), (1, 32),
+                                     (33, 2)])
 def test_schedule_pack_equals_the_two_calls(dev, B, gamma):
     rng = np.random.default_rng(B * 31 + gamma)
     for trial in range(3):

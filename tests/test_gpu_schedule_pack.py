@@ -35,7 +35,9 @@ def tables(rng, B, gamma, kind):
 
 
 SIZES = [(1, 1), (1, 2), (4, 4), (3, 32), (7, 8), (100, 5), (256, 8), (512, 8), (1000, 17),
-         (2048, 9), (8192, 2), (8192, 3), (5, 1), (1023, 2), (1025, 3)]
+         (2048, 9), (8192, 2), (8192, 3), (5, 1), (1023, 2), (1025, 3),
+         # the one-warp kernel's range (n <= 32) and just past it
+         (32, 2), (16, 3), (2, 17), (11, 3), (1, 32), (1, 16), (33, 2), (3, 12)]
 
 
 @pytest.mark.parametrize("B,gamma", SIZES)
