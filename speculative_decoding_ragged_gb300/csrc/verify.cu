@@ -21,12 +21,15 @@
 namespace dspark {
 namespace {
 
-constexpr int kFinalThreads = 256;
-constexpr int kFinalWarps = kFinalThreads / 32;
-constexpr int kBonusGroup = 4;            // tiles a warp loads before reducing them
+// Finaliser CTA size: 256 threads for large batches; 1024 for small ones, where every row's
+// partials (target and draft rows each on a warp of their own) are combined at once.
+constexpr int kFinalThreadsLarge = 256;
+constexpr int kFinalThreadsSmall = 1024;
+constexpr int kFinalSmallBatch = 64;
 constexpr int kTileThreads = 256;
-constexpr int kTilesPerCta = (kTileThreads / 32) * kBonusGroup;
+constexpr int kTileWarps = kTileThreads / 32;
 constexpr int kPickThreads = kTileThreads;
+constexpr int kPickKeep = 4;              // tile sums a pick thread keeps in registers
 constexpr int kMaxVocabStochastic = 1 << 20;
 
 // ---- Philox4x64-10 (Salmon, Moraes, Dror, Shaw, SC'11), device side ---------------------
@@ -105,6 +108,20 @@ __device__ __forceinline__ void load8(const char* row, int v0, int V, int vec, f
     }
 }
 
+// A token's probability under a row with maximum m and 1/Z = iz: exp2((x - m) * s) * iz, with
+// explicitly rounded operations so that every kernel computing it gets the same bits (the
+// tile sums and the in-tile walk must agree).
+__device__ __forceinline__ float token_prob(float x, float m, float iz, float s)
+{
+    return __fmul_rn(ex2_approx(__fmul_rn(__fsub_rn(x, m), s)), iz);
+}
+
+// A non-negative probability mass (at most about 1) as exact 2^-52 fixed point.
+__device__ __forceinline__ uint64_t to_fixed(float x)
+{
+    return __float2ull_rn(__fmul_rn(x, 4503599627370496.0f));
+}
+
 // Bonus weights of 8 consecutive tokens from their logits: p_v (residual == 0) or
 // max(0, p_v - q_v); tokens at or past V weigh 0.
 template <int DT>
@@ -115,14 +132,14 @@ __device__ __forceinline__ void bonus_weights_of(const float (&xp)[8], const flo
     if (residual) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            const float p = (v0 + e < V) ? ex2_approx((xp[e] - mp) * s) * izp : 0.0f;
-            const float q = (v0 + e < V) ? ex2_approx((xq[e] - mq) * s) * izq : 0.0f;
-            w[e] = fmaxf(p - q, 0.0f);
+            const float p = (v0 + e < V) ? token_prob(xp[e], mp, izp, s) : 0.0f;
+            const float q = (v0 + e < V) ? token_prob(xq[e], mq, izq, s) : 0.0f;
+            w[e] = fmaxf(__fsub_rn(p, q), 0.0f);
         }
     } else {
 #pragma unroll
         for (int e = 0; e < 8; ++e)
-            w[e] = (v0 + e < V) ? ex2_approx((xp[e] - mp) * s) * izp : 0.0f;
+            w[e] = (v0 + e < V) ? token_prob(xp[e], mp, izp, s) : 0.0f;
     }
 }
 
@@ -202,10 +219,12 @@ __device__ __forceinline__ int combine_arg(const ArgPart* parts, int nc, int lan
     return idx == 0x7FFFFFFF ? 0 : idx;   // a row of -inf only: index 0
 }
 
-template <int DT, bool STOCH>
-__global__ void __launch_bounds__(kFinalThreads)
+template <int DT, bool STOCH, int FT>
+__global__ void __launch_bounds__(FT)
 verify_finalize_kernel(FinalArgs A)
 {
+    constexpr int kFinalThreads = FT;
+    constexpr int kFinalWarps = FT / 32;
     constexpr int E = (DT == DSPARK_BF16) ? 2 : 4;
     __shared__ int g_s[DSPARK_MAX_GAMMA];
     __shared__ float mp_s[DSPARK_MAX_GAMMA], mq_s[DSPARK_MAX_GAMMA];
@@ -261,19 +280,23 @@ verify_finalize_kernel(FinalArgs A)
     }
     const int ndec = nrows - 1;   // accept tests this mode runs
 
-    // 1. per-row statistics from the chunk partials; one warp per row
-    for (int i = warp; i < nrows; i += kFinalWarps) {
-        const int64_t r = base + i;
+    // 1. per-row statistics from the chunk partials; one warp per row: the target rows, then
+    //    (stochastic) the draft rows of the tested positions
+    const int row_jobs = STOCH ? nrows + ndec : nrows;
+    for (int t = warp; t < row_jobs; t += kFinalWarps) {
         if (!STOCH) {
-            const int g = combine_arg(static_cast<const ArgPart*>(A.part_t) + r * A.nc, A.nc, lane);
-            if (lane == 0) g_s[i] = g;
+            const int g = combine_arg(static_cast<const ArgPart*>(A.part_t) + (base + t) * A.nc,
+                                      A.nc, lane);
+            if (lane == 0) g_s[t] = g;
         } else {
+            const bool target = t < nrows;
+            const int i = target ? t : t - nrows;
+            const SoftPart* parts = static_cast<const SoftPart*>(target ? A.part_t : A.part_d);
             float m, z;
-            combine_soft(static_cast<const SoftPart*>(A.part_t) + r * A.nc, A.nc, A.s, lane, m, z);
-            if (lane == 0) { mp_s[i] = m; zp_s[i] = z; }
-            if (i < ndec) {
-                combine_soft(static_cast<const SoftPart*>(A.part_d) + r * A.nc, A.nc, A.s, lane, m, z);
-                if (lane == 0) { mq_s[i] = m; zq_s[i] = z; }
+            combine_soft(parts + (base + i) * A.nc, A.nc, A.s, lane, m, z);
+            if (lane == 0) {
+                if (target) { mp_s[i] = m; zp_s[i] = z; }
+                else { mq_s[i] = m; zq_s[i] = z; }
             }
         }
     }
@@ -383,8 +406,8 @@ verify_finalize_kernel(FinalArgs A)
 }
 
 // Stochastic bonus, step 2, by the last tile CTA of the request: a block scan of the tile sums
-// (fp64 running sums) finds the tile where the running sum first exceeds u' * R; one warp then
-// walks that tile's tokens in order. The token is the smallest v whose running weight sum
+// (exact 2^-52 fixed-point running sums) finds the tile where the running sum first exceeds
+// u' * R; one warp then walks that tile's tokens in order. The token is the smallest v whose running weight sum
 // exceeds u' * R; a residual summing to zero falls back to p; rounding that leaves no crossing
 // takes the last token with positive weight in the last candidate tile.
 template <int DT>
@@ -392,10 +415,10 @@ __device__ void bonus_pick(const FinalArgs& A, int b, const BonusJob& job)
 {
     constexpr int E = (DT == DSPARK_BF16) ? 2 : 4;
     constexpr int kWarps = kPickThreads / 32;
-    __shared__ double warp_incl[kWarps];
+    __shared__ uint64_t warp_incl[kWarps];
     __shared__ int first_s;
     __shared__ int tile_s;
-    __shared__ double before_s;
+    __shared__ uint64_t before_s;
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
@@ -404,53 +427,85 @@ __device__ void bonus_pick(const FinalArgs& A, int b, const BonusJob& job)
     const int per = (n + kPickThreads - 1) / kPickThreads;
     const int t0 = tid * per, t1 = min(t0 + per, n);
     int col = job.drow >= 0 ? 0 : 1;                  // residual sums, or p sums
-    double own = 0.0, incl = 0.0, R = 0.0;
+    // the thread's tile sums (both columns) stay in registers when it has few tiles
+    const bool kept = per <= kPickKeep;
+    float2 keep[kPickKeep];
+#pragma unroll
+    for (int k = 0; k < kPickKeep; ++k)
+        keep[k] = (kept && t0 + k < t1) ? __ldcg(reinterpret_cast<const float2*>(sums) + t0 + k)
+                                        : make_float2(0.0f, 0.0f);
+    // running sums are exact 2^-52 fixed point (probability masses are at most about 1, so
+    // every sum stays below 2^53); FP64 throughput is scarce on this part
+    uint64_t own = 0, incl = 0, R = 0;
     for (int attempt = 0; attempt < 2; ++attempt) {
-        own = 0.0;
-        for (int t = t0; t < t1; ++t) own += static_cast<double>(__ldcg(sums + 2 * t + col));
+        own = 0;
+        if (kept) {
+#pragma unroll
+            for (int k = 0; k < kPickKeep; ++k)
+                if (t0 + k < t1) own += to_fixed(col ? keep[k].y : keep[k].x);
+        } else {
+            for (int t = t0; t < t1; ++t) own += to_fixed(__ldcg(sums + 2 * t + col));
+        }
         incl = own;
         for (int off = 1; off < 32; off <<= 1) {
-            const double v = __shfl_up_sync(0xffffffffu, incl, off);
+            const uint64_t v = __shfl_up_sync(0xffffffffu, incl, off);
             if (lane >= off) incl += v;
         }
         if (lane == 31) warp_incl[warp] = incl;
         __syncthreads();
-        double offset = 0.0;
-        R = 0.0;
+        uint64_t offset = 0;
+        R = 0;
+#pragma unroll
         for (int k = 0; k < kWarps; ++k) {
-            if (k < warp) offset += warp_incl[k];
-            R += warp_incl[k];
+            const uint64_t v = warp_incl[k];
+            if (k < warp) offset += v;
+            R += v;
         }
         incl += offset;
         __syncthreads();
-        if (col == 1 || R > 0.0) break;
+        if (col == 1 || R > 0) break;
         col = 1;                                      // the residual vanished: draw from p
     }
-    const double thr = job.u * R;
+    // smallest running sum above u' * R: thr = floor(u' * R) for integer sums
+    const uint64_t thr = static_cast<uint64_t>(job.u * static_cast<double>(R));
     if (tid == 0) first_s = kPickThreads;
     __syncthreads();
     if (incl > thr && t0 < t1) atomicMin(&first_s, tid);
     __syncthreads();
     if (tid == first_s) {
-        double cum = incl - own;
+        uint64_t cum = incl - own;
         int tile = -1;
-        for (int t = t0; t < t1; ++t) {
-            const double v = static_cast<double>(__ldcg(sums + 2 * t + col));
-            if (cum + v > thr) { tile = t; break; }
-            cum += v;
+        if (kept) {
+            uint64_t last = 0;
+#pragma unroll
+            for (int k = 0; k < kPickKeep; ++k) {
+                if (tile < 0 && t0 + k < t1) {
+                    const uint64_t v = to_fixed(col ? keep[k].y : keep[k].x);
+                    if (cum + v > thr) tile = t0 + k;
+                    else cum += v;
+                    last = v;
+                }
+            }
+            if (tile < 0) { tile = t1 - 1; cum -= last; }
+        } else {
+            for (int t = t0; t < t1; ++t) {
+                const uint64_t v = to_fixed(__ldcg(sums + 2 * t + col));
+                if (cum + v > thr) { tile = t; break; }
+                cum += v;
+            }
+            if (tile < 0) { tile = t1 - 1; cum -= to_fixed(__ldcg(sums + 2 * tile + col)); }
         }
-        if (tile < 0) { tile = t1 - 1; cum -= static_cast<double>(__ldcg(sums + 2 * tile + col)); }
         tile_s = tile;
         before_s = cum;
     }
     if (tid == 0 && first_s == kPickThreads) {       // rounding left no crossing
         tile_s = n - 1;
-        before_s = R - static_cast<double>(__ldcg(sums + 2 * (n - 1) + col));
+        before_s = R - to_fixed(__ldcg(sums + 2 * (n - 1) + col));
     }
     __syncthreads();
     if (warp != 0) return;
     const int tile = tile_s;
-    const double before = before_s;
+    const uint64_t before = before_s;
     const bool residual = col == 0;
     const char* trow = static_cast<const char*>(A.target) + job.trow * A.V * E;
     const char* drow = static_cast<const char*>(A.draft) + (job.drow >= 0 ? job.drow : 0) * A.V * E;
@@ -459,10 +514,16 @@ __device__ void bonus_pick(const FinalArgs& A, int b, const BonusJob& job)
     load8<DT>(trow, v0, A.V, A.vec, xp);
     if (residual) load8<DT>(drow, v0, A.V, A.vec, xq);
     bonus_weights_of<DT>(xp, xq, v0, A.V, residual, job.mp, job.izp, job.mq, job.izq, A.s, wv);
-    const double own8 = static_cast<double>(sum8(wv));
-    double inc8 = own8;
+    uint64_t wf[8];
+    uint64_t own8 = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        wf[e] = to_fixed(wv[e]);
+        own8 += wf[e];
+    }
+    uint64_t inc8 = own8;
     for (int off = 1; off < 32; off <<= 1) {
-        const double v = __shfl_up_sync(0xffffffffu, inc8, off);
+        const uint64_t v = __shfl_up_sync(0xffffffffu, inc8, off);
         if (lane >= off) inc8 += v;
     }
     const unsigned hit8 = __ballot_sync(0xffffffffu, before + inc8 > thr);
@@ -470,9 +531,9 @@ __device__ void bonus_pick(const FinalArgs& A, int b, const BonusJob& job)
     if (hit8) {
         const int src = __ffs(hit8) - 1;
         if (lane == src) {
-            double cum = before + inc8 - own8;
+            uint64_t cum = before + inc8 - own8;
             for (int e = 0; e < 8; ++e) {
-                cum += static_cast<double>(wv[e]);
+                cum += wf[e];
                 if (cum > thr) { chosen = v0 + e; break; }
             }
         }
@@ -499,14 +560,16 @@ __device__ void bonus_pick(const FinalArgs& A, int b, const BonusJob& job)
 }
 
 // Stochastic bonus, step 1: weight sums of every 256-token tile of each request's bonus row(s),
-// spread over the whole grid (kTilesPerCta tiles per CTA, kBonusGroup per warp, all loads of a
-// warp issued before its exponentials). A residual draw also records p's sums, for the rare
+// spread over the whole grid (G tiles per warp, eight warps per CTA, all loads of a warp issued
+// before its exponentials; G = 1 spreads a small batch over more SMs). A residual draw also records p's sums, for the rare
 // fallback to p when rounding leaves a residual of zero. The last of a request's CTAs to finish
 // (a per-request counter the finaliser zeroed) then performs step 2.
-template <int DT>
+template <int DT, int G>
 __global__ void __launch_bounds__(kTileThreads)
 bonus_tiles_kernel(FinalArgs A, int ctas_per_request)
 {
+    constexpr int kBonusGroup = G;            // tiles a warp loads before reducing them
+    constexpr int kTilesPerCta = kTileWarps * G;
     constexpr int E = (DT == DSPARK_BF16) ? 2 : 4;
     pdl_wait_and_trigger();
     const int b = blockIdx.x / ctas_per_request;
@@ -531,15 +594,20 @@ bonus_tiles_kernel(FinalArgs A, int ctas_per_request)
     for (int g = 0; g < kBonusGroup; ++g) {
         const int t = t0 + g;
         const int v0 = t * 256 + lane * 8;
+        // p once (and q): the residual weight max(p - q, 0) and p's own weight reuse it, with
+        // the arithmetic of bonus_weights_of
         float wr[8], wp[8];
-        bonus_weights_of<DT>(xp[g], xq[g], v0, A.V, false, job.mp, job.izp, 0.0f, 0.0f, A.s, wp);
-        float sp = sum8(wp);
-        float sr = sp;
-        if (residual) {
-            bonus_weights_of<DT>(xp[g], xq[g], v0, A.V, true, job.mp, job.izp, job.mq, job.izq,
-                                 A.s, wr);
-            sr = sum8(wr);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const bool in_v = v0 + e < A.V;
+            wp[e] = in_v ? token_prob(xp[g][e], job.mp, job.izp, A.s) : 0.0f;
+            if (residual) {
+                const float q = in_v ? token_prob(xq[g][e], job.mq, job.izq, A.s) : 0.0f;
+                wr[e] = fmaxf(__fsub_rn(wp[e], q), 0.0f);
+            }
         }
+        float sp = sum8(wp);
+        float sr = residual ? sum8(wr) : sp;
         for (int off = 16; off > 0; off >>= 1) {
             sp += __shfl_xor_sync(0xffffffffu, sp, off);
             sr += __shfl_xor_sync(0xffffffffu, sr, off);
@@ -628,13 +696,26 @@ int run_verify(const VerifyCall& c, const Plan& plan, void* part_t, void* part_d
     fa.out_len = c.out_len;
     fa.out_cap = c.out_cap;
     fa.n_tiles = (c.V + 255) / 256;
-    rc = launch_pdl("verify (finalize)", verify_finalize_kernel<DT, STOCH>, dim3(c.B),
-                    dim3(kFinalThreads), 0, stream, fa);
+    if (c.B <= kFinalSmallBatch)
+        rc = launch_pdl("verify (finalize)", verify_finalize_kernel<DT, STOCH, kFinalThreadsSmall>,
+                        dim3(c.B), dim3(kFinalThreadsSmall), 0, stream, fa);
+    else
+        rc = launch_pdl("verify (finalize)", verify_finalize_kernel<DT, STOCH, kFinalThreadsLarge>,
+                        dim3(c.B), dim3(kFinalThreadsLarge), 0, stream, fa);
     if (rc != DSPARK_OK || !STOCH) return rc;
-    const int cpr = static_cast<int>(ceil_div(fa.n_tiles, kTilesPerCta));
-    return launch_pdl("verify (bonus)", bonus_tiles_kernel<DT>,
-                      dim3(static_cast<unsigned>(static_cast<int64_t>(c.B) * cpr)),
-                      dim3(kTileThreads), 0, stream, fa, cpr);
+    // one tile per warp while the batch's bonus rows would not cover the SMs, four otherwise
+    DeviceInfo dev;
+    rc = current_device(&dev);
+    if (rc != DSPARK_OK) return rc;
+    const int64_t cpr4 = ceil_div(fa.n_tiles, kTileWarps * 4);
+    if (static_cast<int64_t>(c.B) * cpr4 >= dev.sm_count)
+        return launch_pdl("verify (bonus)", bonus_tiles_kernel<DT, 4>,
+                          dim3(static_cast<unsigned>(c.B * cpr4)), dim3(kTileThreads), 0, stream,
+                          fa, static_cast<int>(cpr4));
+    const int64_t cpr1 = ceil_div(fa.n_tiles, kTileWarps);
+    return launch_pdl("verify (bonus)", bonus_tiles_kernel<DT, 1>,
+                      dim3(static_cast<unsigned>(c.B * cpr1)), dim3(kTileThreads), 0, stream, fa,
+                      static_cast<int>(cpr1));
 }
 
 }  // namespace
