@@ -37,6 +37,7 @@ GREEDY_CASES = [
     (3, 32, 777, "bf16", 2.0),
     (1, 1, 64, "bf16", 1.0),        # no drafts at all
     (40, 3, 129280, "bf16", 2.0),
+    (100, 4, 2048, "bf16", 2.0),     # more than 64 requests: the 256-thread finaliser
 ]
 
 
@@ -96,6 +97,8 @@ STOCH_CASES = [
     (5, 4, 2048, "f32", 1.3),
     (32, 8, 32000, "bf16", 1.0),    # the stochastic workload's shape
     (2, 16, 129280, "bf16", 0.7),
+    (80, 4, 32000, "bf16", 1.0),    # 256-thread finaliser; bonus pass with four tiles a warp
+    (2, 4, 300000, "bf16", 1.0),    # more tiles than the pick keeps in registers
 ]
 
 
