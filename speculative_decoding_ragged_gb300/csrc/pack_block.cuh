@@ -16,7 +16,8 @@
 // kLdg: windows may be read through the read-only path (false when this CTA wrote them).
 // win_count (shared memory, or nullptr): the scheduler's per-request counts, window = 1 + count,
 // read instead of the windows array by the fused schedule-and-pack kernel, which also passes
-// each thread's tier (tiers[tid], or INT_MAX past n_tiers) loaded at its start as tier_pre.
+// each thread's tier (tiers[tid], or INT_MAX past n_tiers) loaded at its start as tier_pre and,
+// when they fit, the block tokens copied into shared memory at its start as tok_stage.
 #pragma once
 #include "common.cuh"
 
@@ -40,7 +41,8 @@ __device__ __forceinline__ void pack_block(const int32_t* windows, const int32_t
                                            int32_t* __restrict__ row_pos, int packed_cap,
                                            int32_t* __restrict__ meta, int32_t* __restrict__ status,
                                            const int* win_count = nullptr,
-                                           const int* tier_pre = nullptr)
+                                           const int* tier_pre = nullptr,
+                                           const int* tok_stage = nullptr)
 {
     constexpr int kWarps = kPackThreads / 32;
     __shared__ int warp_total[kWarps];
@@ -124,7 +126,8 @@ __device__ __forceinline__ void pack_block(const int32_t* windows, const int32_t
             if (cu_s[mid] <= r) lo = mid; else hi = mid;
         }
         const int i = r - cu_s[lo];
-        packed_ids[r] = __ldg(tokens + static_cast<int64_t>(lo) * gamma + i);
+        const int64_t ti = static_cast<int64_t>(lo) * gamma + i;
+        packed_ids[r] = tok_stage != nullptr ? tok_stage[ti] : __ldg(tokens + ti);
         if (row_req) row_req[r] = lo;
         if (row_pos) row_pos[r] = i;
     }

@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, double bias,
                 const double* __restrict__ alpha, const double* __restrict__ theta,
                 int32_t* __restrict__ windows, int32_t* __restrict__ k_star,
-                int32_t* __restrict__ status, PackArgs pk)
+                int32_t* __restrict__ status, PackArgs pk, int tok_stage_off)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     // MERGE: keys ksrc [n] (u32), indices isrc [n], then the ping-pong pair kdst, idst (the
@@ -169,13 +169,23 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
     const int lane = tid & 31;
     const int warp = tid >> 5;
     int tier_pre = INT_MAX;
+    int* tok_stage = nullptr;
     if (PACK) {
-        // the pack's inputs are read only at the end: its tier now, its tokens into L2
-        const char* tp = reinterpret_cast<const char*>(pk.tokens);
-        const int64_t tb = static_cast<int64_t>(B) * (L + 1) * 4;
-        for (int64_t off = static_cast<int64_t>(tid) * 128; off < tb; off += kThreads * 128)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(tp + off));
+        // the pack's inputs are read only at the end: its tier now, and its tokens copied into
+        // shared memory (cp.async, 16-byte pieces) while the scheduler works, when they fit
         if (tid < pk.n_tiers) tier_pre = __ldg(pk.tiers + tid);
+        if (tok_stage_off >= 0) {
+            tok_stage = reinterpret_cast<int*>(smem_raw + tok_stage_off);
+            const int nt = B * (L + 1);
+            const int n16 = nt >> 2;
+            for (int c = tid; c < n16; c += kThreads) {
+                const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(tok_stage + 4 * c));
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
+                             "l"(pk.tokens + 4 * c) : "memory");
+            }
+            for (int t = 4 * n16 + tid; t < nt; t += kThreads) tok_stage[t] = __ldg(pk.tokens + t);
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        }
     }
     constexpr int kMaxItems = MERGE ? kMergeItems : DSPARK_MAX_CANDIDATES / kThreads;
     const int items = (n + kThreads - 1) / kThreads;   // positions per thread, contiguous
@@ -455,11 +465,14 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
     __syncthreads();
     for (int b = tid; b < B; b += kThreads) windows[b] = 1 + count[b];
     if (PACK) {
-        // count[] is complete (barrier above) and the pack reads the windows from it
+        // count[] is complete (barrier above) and the pack reads the windows from it; the staged
+        // tokens are complete once every thread's copies have landed (the pack's first barrier
+        // comes before its first read of them)
         static_assert(kPackThreads == kThreads, "the pack body runs on the scheduler's CTA");
+        if (tok_stage != nullptr) asm volatile("cp.async.wait_all;" ::: "memory");
         pack_block<false>(windows, pk.tokens, B, L + 1, pk.tiers, pk.n_tiers, pk.cu,
                           pk.packed_ids, pk.row_req, pk.row_pos, pk.packed_cap, pk.meta, status,
-                          count, &tier_pre);
+                          count, &tier_pre, tok_stage);
     }
 }
 
@@ -653,6 +666,8 @@ schedule_small_kernel(const float* __restrict__ conf, int B, int L, double bias,
 
 namespace {
 
+inline size_t align_to(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
 // Launches schedule_kernel<merge, PACK> with the dynamic shared memory its size needs; the
 // opt-in limit (static plus dynamic) is configured once per device and variant.
 template <bool PACK>
@@ -664,8 +679,8 @@ int launch_schedule_kernel(const char* what, const float* conf, int B, int L,
     int n_pad = 1;
     while (n_pad < n) n_pad <<= 1;
     const bool merge = n <= kMergeMax;
-    const size_t smem = (merge ? 16 * static_cast<size_t>(n) : 8 * static_cast<size_t>(n_pad)) +
-                        sizeof(int) * static_cast<size_t>(B);
+    size_t smem = (merge ? 16 * static_cast<size_t>(n) : 8 * static_cast<size_t>(n_pad)) +
+                  sizeof(int) * static_cast<size_t>(B);
     DeviceInfo dev;
     int rc = current_device(&dev);
     if (rc != DSPARK_OK) return rc;
@@ -688,13 +703,23 @@ int launch_schedule_kernel(const char* what, const float* conf, int B, int L,
     if (smem > max_dynamic[merge ? 1 : 0])
         return fail(DSPARK_ERR_UNSUPPORTED, "%s: %zu bytes of shared memory needed, the device "
                     "allows %zu", what, smem, max_dynamic[merge ? 1 : 0]);
+    // the pack's tokens staged behind the scheduler's arrays when they fit (16-byte aligned)
+    int stage_off = -1;
+    if (PACK && reinterpret_cast<uintptr_t>(pk.tokens) % 16 == 0) {
+        const size_t off = align_to(smem, 16);
+        const size_t need = off + sizeof(int) * static_cast<size_t>(B) * (L + 1);
+        if (need <= max_dynamic[merge ? 1 : 0]) {
+            stage_off = static_cast<int>(off);
+            smem = need;
+        }
+    }
     if (merge)
         return launch_pdl(what, schedule_kernel<true, PACK>, dim3(1), dim3(kThreads), smem,
                           stream, conf, B, L, n, n_pad, cost->bias, cost->alpha, cost->theta,
-                          windows, k_star, status, pk);
+                          windows, k_star, status, pk, stage_off);
     return launch_pdl(what, schedule_kernel<false, PACK>, dim3(1), dim3(kThreads), smem, stream,
                       conf, B, L, n, n_pad, cost->bias, cost->alpha, cost->theta, windows,
-                      k_star, status, pk);
+                      k_star, status, pk, stage_off);
 }
 
 }  // namespace

@@ -26,7 +26,10 @@ constexpr int kTargetUnits = 4096;    // aim: about one unit per resident warp
 #define DSPARK_MAX_CHUNK 4096
 #endif
 constexpr int kMaxChunk = DSPARK_MAX_CHUNK;   // elements per chunk, upper bound
-constexpr int kMinChunk = 256;        // elements per chunk, lower bound
+#ifndef DSPARK_MIN_CHUNK
+#define DSPARK_MIN_CHUNK 256
+#endif
+constexpr int kMinChunk = DSPARK_MIN_CHUNK;   // elements per chunk, lower bound
 
 struct __align__(8) ArgPart {
     float v;
