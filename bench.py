@@ -614,7 +614,8 @@ def run_reference(args, rank, world):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
             "config": {"workload": args.workload, "B": wl.B, "gamma": wl.gamma, "V": wl.V,
-                       "mode": "compact", "verify": "greedy"},
+                       "mode": "compact", "verify": "greedy", "logits": "bf16",
+                       "parallelism": "single CPU thread"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": sample, "cpu": cpu_model()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
