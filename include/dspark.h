@@ -262,6 +262,18 @@ int dspark_verify_scatter(dspark_mode mode, int stochastic,
 int dspark_set_stream_kernel(int which);
 
 /* ---------------------------------------------------------------------------------------
+ * dspark_set_stream_events — measurement hook: every later dspark_verify /
+ * dspark_verify_scatter call records `start` on its stream just before its logit-streaming
+ * kernel and `stop` just after it, so that the caller can time that kernel alone
+ * (cudaEventElapsedTime). Both NULL switch it off (the default). The events belong to the
+ * caller and must outlive the calls that record them. An event between two kernels stops the
+ * next one from starting early (programmatic dependent launch), so a timed call runs slightly
+ * slower than an untimed one. Not thread-safe against concurrent verify calls. Returns
+ * DSPARK_OK, or DSPARK_ERR_INVALID_ARG when exactly one of the two is NULL.
+ * ------------------------------------------------------------------------------------- */
+int dspark_set_stream_events(cudaEvent_t start, cudaEvent_t stop);
+
+/* ---------------------------------------------------------------------------------------
  * dspark_observe — calibration and utilisation counters ("A2 method details", observability:
  * per-request confidence and calibration metrics such as ECE; cap-accept recovers the
  * acceptance ceiling that truncation hides, and utilisation is committed over ceiling).

@@ -71,6 +71,7 @@ SYMBOLS = {
                                _u64, _u64, _p, _p, _p, _p, _p, _p], _i),
     "dspark_observe": ([_p, _p, _p, _i, _i, _i, _p, _p, _p, _p], _i),
     "dspark_set_stream_kernel": ([_i], _i),
+    "dspark_set_stream_events": ([_p, _p], _i),
     "dspark_last_error": ([], ctypes.c_char_p),
     "dspark_version": ([], _i),
 }
@@ -157,6 +158,19 @@ def set_stream_kernel(which: int) -> None:
     """Which kernel streams the logits inside verify (STREAM_AUTO, STREAM_REGISTER,
     STREAM_BULK); results are bit-identical, only speed differs."""
     _check("dspark_set_stream_kernel", lib().dspark_set_stream_kernel(int(which)))
+
+
+def set_stream_events(start: Optional[torch.cuda.Event], stop: Optional[torch.cuda.Event]):
+    """Record `start` / `stop` around the logit-streaming kernel of every later verify call
+    (None, None: off). The events must have been recorded once (torch creates them lazily)."""
+    def handle(ev):
+        if ev is None:
+            return None
+        h = int(ev.cuda_event)
+        if h == 0:
+            raise ValueError("record the event once before handing it to the library")
+        return ctypes.c_void_p(h)
+    _check("dspark_set_stream_events", lib().dspark_set_stream_events(handle(start), handle(stop)))
 
 
 def version() -> int:

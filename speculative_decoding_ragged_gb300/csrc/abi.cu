@@ -352,6 +352,14 @@ int dspark_observe(const float* conf, const int32_t* accept_len, const int32_t* 
 
 int dspark_set_stream_kernel(int which) { return dspark::set_stream_kernel(which); }
 
+int dspark_set_stream_events(cudaEvent_t start, cudaEvent_t stop)
+{
+    if ((start == nullptr) != (stop == nullptr))
+        return fail(DSPARK_ERR_INVALID_ARG, "dspark_set_stream_events: give both events or neither");
+    dspark::set_stream_events(start, stop);
+    return DSPARK_OK;
+}
+
 const char* dspark_last_error(void) { return dspark::last_error(); }
 
 int dspark_version(void) { return 100; }

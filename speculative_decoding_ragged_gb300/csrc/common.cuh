@@ -77,6 +77,8 @@ struct VerifyCall {
 size_t verify_workspace_bytes(int B, int gamma, int V, int stochastic);
 // dspark_set_stream_kernel: DSPARK_STREAM_AUTO / _REGISTER / _BULK for later verify calls.
 int set_stream_kernel(int which);
+// dspark_set_stream_events: events recorded around the streaming kernel of later verify calls.
+void set_stream_events(cudaEvent_t start, cudaEvent_t stop);
 int launch_verify(const VerifyCall& c, cudaStream_t stream);
 int launch_scatter(const int32_t* committed, const int32_t* accept_len, int B, int gamma,
                    int32_t* out_tokens, int32_t* out_len, int out_cap, int32_t* status,

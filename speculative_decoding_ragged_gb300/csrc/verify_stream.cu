@@ -316,6 +316,8 @@ verify_bulk_kernel(StreamArgs A, int stages, int stage_bytes)
 namespace {
 
 int g_stream_kernel = DSPARK_STREAM_AUTO;   // dspark_set_stream_kernel
+cudaEvent_t g_ev_start = nullptr;           // dspark_set_stream_events
+cudaEvent_t g_ev_stop = nullptr;
 
 template <int DT, bool STOCH>
 int launch_stream_t(const StreamArgs& sa, int64_t max_units, cudaStream_t stream)
@@ -383,14 +385,27 @@ int set_stream_kernel(int which)
     return DSPARK_OK;
 }
 
+void set_stream_events(cudaEvent_t start, cudaEvent_t stop)
+{
+    g_ev_start = start;
+    g_ev_stop = stop;
+}
+
 int launch_verify_stream(int dtype, bool stochastic, const StreamArgs& sa, int64_t max_units,
                          cudaStream_t stream)
 {
+    if (g_ev_start != nullptr && cudaEventRecord(g_ev_start, stream) != cudaSuccess)
+        return check_launch("verify (stream start event)");
+    int rc;
     if (dtype == DSPARK_BF16)
-        return stochastic ? launch_stream_t<DSPARK_BF16, true>(sa, max_units, stream)
-                          : launch_stream_t<DSPARK_BF16, false>(sa, max_units, stream);
-    return stochastic ? launch_stream_t<DSPARK_F32, true>(sa, max_units, stream)
-                      : launch_stream_t<DSPARK_F32, false>(sa, max_units, stream);
+        rc = stochastic ? launch_stream_t<DSPARK_BF16, true>(sa, max_units, stream)
+                        : launch_stream_t<DSPARK_BF16, false>(sa, max_units, stream);
+    else
+        rc = stochastic ? launch_stream_t<DSPARK_F32, true>(sa, max_units, stream)
+                        : launch_stream_t<DSPARK_F32, false>(sa, max_units, stream);
+    if (rc == DSPARK_OK && g_ev_stop != nullptr && cudaEventRecord(g_ev_stop, stream) != cudaSuccess)
+        return check_launch("verify (stream stop event)");
+    return rc;
 }
 
 }  // namespace dspark

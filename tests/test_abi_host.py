@@ -106,3 +106,10 @@ def test_stream_kernel_setting_is_checked(lib):
     assert lib.dspark_set_stream_kernel(7) == -1 and "unknown kernel 7" in bd.last_error()
     assert lib.dspark_set_stream_kernel(bd.STREAM_BULK) == 0
     assert lib.dspark_set_stream_kernel(bd.STREAM_AUTO) == 0
+
+
+def test_stream_events_need_both_or_neither(lib):
+    from speculative_decoding_ragged_gb300 import _binding as bd
+    assert lib.dspark_set_stream_events(ctypes.c_void_p(8), None) == -1
+    assert "both events or neither" in bd.last_error()
+    assert lib.dspark_set_stream_events(None, None) == 0

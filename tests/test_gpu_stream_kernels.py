@@ -103,3 +103,27 @@ def test_misaligned_rows_fall_back_to_the_register_kernel(dev):
     k = _run(dev, bd.STREAM_BULK, "static", tgt, None, bt.tokens, None, None, False)
     for key in r:
         np.testing.assert_array_equal(k[key], r[key], err_msg=key)
+
+
+def test_stream_events_time_the_streaming_kernel_alone(dev):
+    wl = synth.WORKLOADS["large_vocab_mixed"].with_(B=64)
+    bt = synth.make_batch(wl, seed=2)
+    B, gamma = bt.tokens.shape
+    w = oracle.schedule(bt.conf, bt.bias, bt.alpha, bt.theta)["windows"]
+    tgt = synth.gather_packed(bt.target, B, gamma, w).to(dev)
+    cu = np.concatenate([[0], np.cumsum(w)])
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for e in ev:
+        e.record()
+    torch.cuda.synchronize()
+    bd.set_stream_events(ev[1], ev[2])
+    try:
+        ev[0].record()
+        r = _run(dev, bd.STREAM_AUTO, "compact", tgt, None, bt.tokens, cu, w, False)
+        ev[3].record()
+    finally:
+        bd.set_stream_events(None, None)
+    torch.cuda.synchronize()
+    kernel_ms, call_ms = ev[1].elapsed_time(ev[2]), ev[0].elapsed_time(ev[3])
+    assert 0.0 < kernel_ms < call_ms
+    assert r["status"][0] == 0
