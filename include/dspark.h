@@ -9,6 +9,9 @@
  *   dspark_verify    packed target logits [M,V] (+ draft logits) -> accept lengths, committed tokens
  *   dspark_scatter   committed tokens -> per-request output histories
  *
+ * dspark_schedule_pack and dspark_verify_scatter produce the same results as the two pairs of
+ * calls with fewer kernel launches; dspark_observe accumulates calibration counters.
+ *
  * Source of the method: "DSpark in SGLang: Speculative Decoding with Confidence-Driven,
  * Variable-Length Verification" (LMSYS blog, as summarised by papercache.org), sections
  * "A2 method details" (confidence scheduler, verify modes, ragged verify over full CUDA graphs,
@@ -197,7 +200,9 @@ int dspark_schedule_pack(const float* conf, int B, int gamma, const dspark_cost*
  *   bytes, 16-byte aligned, owned by the caller, fully rewritten by every call before it is
  *   read (no clearing needed). Calls that share one workspace must not overlap on the GPU.
  * Limits: 0 <= B, 1 <= gamma <= DSPARK_MAX_GAMMA, V >= 1, temperature > 0 (stochastic).
- * Two kernels: a persistent streaming kernel over fixed row chunks, then one CTA per request.
+ * Kernels: a persistent streaming kernel over fixed row chunks (register or TMA bulk-copy
+ * streaming, see dspark_set_stream_kernel), then one CTA per request, and for stochastic calls
+ * a bonus kernel spread over the grid.
  * ------------------------------------------------------------------------------------- */
 int dspark_verify(dspark_mode mode, int stochastic,
                   const void* target_logits, int target_rows, const void* draft_logits,
