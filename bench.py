@@ -596,12 +596,21 @@ def cpu_baseline(batches, wl, seconds):
             "cpu": cpu_model(), "host_cores": os.cpu_count()}
 
 
+ARM_PARTS = {"0xd4f": "Arm Neoverse V2", "0xd40": "Arm Neoverse V1", "0xd0c": "Arm Neoverse N1",
+             "0xd49": "Arm Neoverse N2", "0xd8e": "Arm Neoverse N3", "0xd84": "Arm Neoverse V3"}
+
+
 def cpu_model():
+    """The host CPU's model name (x86), or its Arm part number with the core's name."""
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
-                if line.lower().startswith(("model name", "cpu part")):
+                key = line.lower()
+                if key.startswith("model name"):
                     return line.split(":", 1)[1].strip()
+                if key.startswith("cpu part"):
+                    part = line.split(":", 1)[1].strip().lower()
+                    return f"{ARM_PARTS.get(part, 'Arm core')} (CPU part {part})"
     except OSError:
         pass
     return None
