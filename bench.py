@@ -1,8 +1,9 @@
 #!/usr/bin/env python3
 """Benchmark of the DSpark ragged-verification hot path on GB300.
 
-One step = the whole hot path on one batch: dspark_schedule -> dspark_pack -> dspark_verify
-(compact, greedy) -> dspark_scatter, on the large-vocab mixed-traffic workload (B=256
+One step = the whole hot path on one batch: schedule, pack, verify (compact, greedy) and the
+compact scatter, issued as the two fused calls dspark_schedule_pack and dspark_verify_scatter,
+on the large-vocab mixed-traffic workload (B=256
 requests, block gamma=8, V=151936 bf16 logits, three acceptance classes a = 0.9/0.65/0.35,
 theta(M) = 0.004 M, alpha(bs) = 0.01 bs, bias 2, tiers every 32 up to 2048). The packed
 target logits of the scheduled windows are produced off the clock (they stand in for the
@@ -12,8 +13,10 @@ more than L2 holds.
 Prints one JSON line. `value` is packed verify rows per second over the whole step with
 inputs resident in HBM; `e2e` repeats the measurement with the step's inputs copied from
 pinned host memory and the results read back inside the timed region; `roofline` reports the
-verify kernels' algorithmic bytes (M * V * 2 per launch) over their CUDA-event time against the
-measured HBM copy bandwidth; `cpu_baseline` times the CPU oracle on a bounded sample.
+streaming kernel's algorithmic bytes (M * V * 2 per launch) over its CUDA-event time against
+the measured HBM copy bandwidth (and the whole verify call beside it); `latency_b1` times the
+batch-1 decode step; `verify_legs` the verify call on the other workloads; `cpu_baseline`
+times the CPU oracle on a bounded sample.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 """
