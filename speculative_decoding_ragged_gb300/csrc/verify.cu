@@ -56,7 +56,7 @@ struct BonusJob {
     int64_t drow;   // draft row of a residual draw; -1 for a draw from p
     float mp, izp;  // target row maximum and 1/Z
     float mq, izq;  // draft row maximum and 1/Z (residual draws)
-    double u;       // the position's bonus uniform u'
+    uint64_t ubits; // the position's bonus uniform u' = ubits * 2^-53 (53-bit integer)
     int64_t slot;   // committed[] index that receives the bonus; -1: no draw
 };
 
@@ -116,10 +116,17 @@ __device__ __forceinline__ float token_prob(float x, float m, float iz, float s)
     return __fmul_rn(ex2_approx(__fmul_rn(__fsub_rn(x, m), s)), iz);
 }
 
-// A non-negative probability mass (at most about 1) as exact 2^-52 fixed point.
+// A non-negative probability mass (at most about 2) as 2^-52 fixed point, from the float's
+// exponent and mantissa with integer shifts (64-bit conversions use the scarce FP64 path):
+// exact for x >= 2^-28, truncated below that; zero and subnormals give 0.
 __device__ __forceinline__ uint64_t to_fixed(float x)
 {
-    return __float2ull_rn(__fmul_rn(x, 4503599627370496.0f));
+    const uint32_t b = __float_as_uint(x);
+    const int e = static_cast<int>(b >> 23);          // biased exponent (x >= 0)
+    if (e == 0) return 0;
+    const uint64_t m = static_cast<uint64_t>((b & 0x7FFFFFu) | 0x800000u);
+    const int sh = e - 98;                            // x * 2^52 = m * 2^(e - 127 - 23 + 52)
+    return sh >= 0 ? (m << sh) : (sh > -64 ? (m >> -sh) : 0ull);
 }
 
 // Bonus weights of 8 consecutive tokens from their logits: p_v (residual == 0) or
@@ -229,7 +236,7 @@ verify_finalize_kernel(FinalArgs A)
     __shared__ int g_s[DSPARK_MAX_GAMMA];
     __shared__ float mp_s[DSPARK_MAX_GAMMA], mq_s[DSPARK_MAX_GAMMA];
     __shared__ float zp_s[DSPARK_MAX_GAMMA], zq_s[DSPARK_MAX_GAMMA];
-    __shared__ double ub_s[DSPARK_MAX_GAMMA];
+    __shared__ uint64_t ub_s[DSPARK_MAX_GAMMA];
     __shared__ int acc_s[DSPARK_MAX_GAMMA];
     __shared__ int walk_s[4];                 // Lc, Lf, pos, rejected
 
@@ -319,7 +326,7 @@ verify_finalize_kernel(FinalArgs A)
         } else {
             uint64_t rnd[4];
             philox4x64_10(static_cast<uint64_t>(b), static_cast<uint64_t>(i), A.step, 0ull, A.seed, 0ull, rnd);
-            ub_s[i] = static_cast<double>(rnd[1] >> 11) * 0x1p-53;
+            ub_s[i] = rnd[1] >> 11;                 // u' = ub_s[i] * 2^-53
             float pp = -1.0f, qq = -1.0f;
             if (tested && valid) {
                 const char* trow = static_cast<const char*>(A.target) + (base + i) * A.V * E;
@@ -390,7 +397,7 @@ verify_finalize_kernel(FinalArgs A)
             job.izp = 1.0f / zp_s[pos];
             job.mq = residual ? mq_s[pos] : 0.0f;
             job.izq = residual ? 1.0f / zq_s[pos] : 0.0f;
-            job.u = ub_s[pos];
+            job.ubits = ub_s[pos];
             job.slot = static_cast<int64_t>(b) * gamma + Lc - 1;
             A.jobs[b] = job;
             A.done[b] = 0u;
@@ -466,8 +473,9 @@ __device__ void bonus_pick(const FinalArgs& A, int b, const BonusJob& job)
         if (col == 1 || R > 0) break;
         col = 1;                                      // the residual vanished: draw from p
     }
-    // smallest running sum above u' * R: thr = floor(u' * R) for integer sums
-    const uint64_t thr = static_cast<uint64_t>(job.u * static_cast<double>(R));
+    // smallest running sum above u' * R: thr = floor(u' * R) = (ubits * R) >> 53, exactly, from
+    // the 128-bit product (R < 2^54, so the result fits in 64 bits)
+    const uint64_t thr = (__umul64hi(job.ubits, R) << 11) | ((job.ubits * R) >> 53);
     if (tid == 0) first_s = kPickThreads;
     __syncthreads();
     if (incl > thr && t0 < t1) atomicMin(&first_s, tid);
