@@ -129,14 +129,15 @@ __device__ __forceinline__ void raise_status(int32_t* status, int bits)
 }
 
 // Compact scatter of one request by one warp: lane i < L holds committed token i, which is
-// appended to the request's history at out_len[b] + i (clamped lengths, overflow dropped and
-// flagged). Every lane reads out_len[b] before lane 0 advances it. Returns the status bits
-// (the same on every lane).
+// appended to the request's history at n0 = out_len[b] (read by the caller, the same value on
+// every lane) + i, with clamped lengths and overflow dropped and flagged; lane 0 then advances
+// out_len[b]. Returns the status bits (the same on every lane).
 __device__ __forceinline__ int scatter_request(int64_t b, int L, int gamma, int tok, int lane,
-                                               int32_t* out_tokens, int32_t* out_len, int out_cap)
+                                               int32_t* out_tokens, int32_t* out_len, int out_cap,
+                                               int n0)
 {
     int bits = 0;
-    int n = out_len[b];
+    int n = n0;
     if (L < 0 || L > gamma) { bits |= DSPARK_STATUS_BAD_LENGTH; L = L < 0 ? 0 : gamma; }
     if (n < 0 || n > out_cap) { bits |= DSPARK_STATUS_BAD_LENGTH; n = n < 0 ? 0 : out_cap; }
     if (lane < L) {

@@ -22,7 +22,8 @@ scatter_kernel(const int32_t* __restrict__ committed, const int32_t* __restrict_
     if (b >= B) return;   // whole warps leave together
     const int L = accept_len[b];
     const int tok = (lane < L && lane < gamma) ? committed[b * gamma + lane] : -1;
-    const int bits = scatter_request(b, L, gamma, tok, lane, out_tokens, out_len, out_cap);
+    const int bits = scatter_request(b, L, gamma, tok, lane, out_tokens, out_len, out_cap,
+                                     out_len[b]);
     if (lane == 0) raise_status(status, bits);
 }
 

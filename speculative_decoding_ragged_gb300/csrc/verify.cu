@@ -262,6 +262,10 @@ verify_finalize_kernel(FinalArgs A)
     const int64_t base = (A.mode == DSPARK_COMPACT) ? static_cast<int64_t>(__ldg(A.cu + b))
                                                     : static_cast<int64_t>(b) * gamma;
     const int64_t n_t = target_row_count(A.mode, A.cu, A.B, gamma, A.target_rows, A.rows_max);
+    // the history length the fused scatter appends at: the previous call wrote it, and every
+    // kernel of this library triggers its dependents only after its own wait, so all kernels
+    // before the streaming kernel have completed by the time this one starts
+    const int n_hist = (A.out_tokens != nullptr && warp == 0) ? A.out_len[b] : 0;
     pdl_wait_and_trigger();
     int32_t* out = A.committed + static_cast<int64_t>(b) * gamma;
 
@@ -280,7 +284,7 @@ verify_finalize_kernel(FinalArgs A)
         }
         if (A.out_tokens && warp == 0) {         // nothing committed: lengths checked only
             const int sb = scatter_request(b, 0, gamma, -1, lane, A.out_tokens, A.out_len,
-                                           A.out_cap);
+                                           A.out_cap, n_hist);
             if (lane == 0) raise_status(A.status, sb);
         }
         return;
@@ -376,7 +380,7 @@ verify_finalize_kernel(FinalArgs A)
         if (!STOCH && A.out_tokens) {
             const int tok = lane < Lc ? g_s[lane] : -1;
             const int sb = scatter_request(b, Lc, gamma, tok, lane, A.out_tokens, A.out_len,
-                                           A.out_cap);
+                                           A.out_cap, n_hist);
             if (lane == 0) bits |= sb;
         }
     }
@@ -418,7 +422,7 @@ verify_finalize_kernel(FinalArgs A)
 // exceeds u' * R; a residual summing to zero falls back to p; rounding that leaves no crossing
 // takes the last token with positive weight in the last candidate tile.
 template <int DT>
-__device__ void bonus_pick(const FinalArgs& A, int b, const BonusJob& job)
+__device__ void bonus_pick(const FinalArgs& A, int b, const BonusJob& job, int n_hist)
 {
     constexpr int E = (DT == DSPARK_BF16) ? 2 : 4;
     constexpr int kWarps = kPickThreads / 32;
@@ -562,7 +566,7 @@ __device__ void bonus_pick(const FinalArgs& A, int b, const BonusJob& job)
         if (lane < Lc - 1) tok = __ldg(A.tokens + row0 + lane + 1);
         else if (lane == Lc - 1) tok = chosen;
         const int sb = scatter_request(b, Lc, A.gamma, tok, lane, A.out_tokens, A.out_len,
-                                       A.out_cap);
+                                       A.out_cap, n_hist);
         if (lane == 0) raise_status(A.status, sb);
     }
 }
@@ -579,8 +583,10 @@ bonus_tiles_kernel(FinalArgs A, int ctas_per_request)
     constexpr int kBonusGroup = G;            // tiles a warp loads before reducing them
     constexpr int kTilesPerCta = kTileWarps * G;
     constexpr int E = (DT == DSPARK_BF16) ? 2 : 4;
-    pdl_wait_and_trigger();
     const int b = blockIdx.x / ctas_per_request;
+    // the history length for the fused scatter, read before the wait (see the finaliser)
+    const int n_hist = (A.out_tokens != nullptr && threadIdx.x < 32) ? A.out_len[b] : 0;
+    pdl_wait_and_trigger();
     const int cta = blockIdx.x - b * ctas_per_request;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -634,7 +640,7 @@ bonus_tiles_kernel(FinalArgs A, int ctas_per_request)
     __syncthreads();
     if (!last_s) return;
     __threadfence();
-    bonus_pick<DT>(A, b, job);
+    bonus_pick<DT>(A, b, job, n_hist);
 }
 
 template <int DT, bool STOCH>
