@@ -266,6 +266,14 @@ verify_finalize_kernel(FinalArgs A)
     // kernel of this library triggers its dependents only after its own wait, so all kernels
     // before the streaming kernel have completed by the time this one starts
     const int n_hist = (A.out_tokens != nullptr && warp == 0) ? A.out_len[b] : 0;
+    // stochastic: the two logits of this thread's tested draft are inputs of the call as well
+    float lp_pre = 0.0f, lq_pre = 0.0f;
+    if (STOCH && tid < nrows - 1 && base >= 0 && base + nrows <= n_t && d_mine >= 0 &&
+        d_mine < A.V) {
+        lp_pre = load_logit<DT>(static_cast<const char*>(A.target) + (base + tid) * A.V * E, d_mine);
+        lq_pre = load_logit<DT>(static_cast<const char*>(A.draft) +
+                                    (static_cast<int64_t>(b) * L + tid) * A.V * E, d_mine);
+    }
     pdl_wait_and_trigger();
     int32_t* out = A.committed + static_cast<int64_t>(b) * gamma;
 
@@ -333,10 +341,8 @@ verify_finalize_kernel(FinalArgs A)
             ub_s[i] = rnd[1] >> 11;                 // u' = ub_s[i] * 2^-53
             float pp = -1.0f, qq = -1.0f;
             if (tested && valid) {
-                const char* trow = static_cast<const char*>(A.target) + (base + i) * A.V * E;
-                const char* drow = static_cast<const char*>(A.draft) + (static_cast<int64_t>(b) * L + i) * A.V * E;
-                const float lp = load_logit<DT>(trow, d);
-                const float lq = load_logit<DT>(drow, d);
+                const float lp = lp_pre;                // loaded before the wait
+                const float lq = lq_pre;
                 // fp32 (FP64 is scarce here): exponents relative to each row's maximum, and the
                 // ratio as one exp2 of their difference, so p/q neither under- nor overflows
                 const float ep = (lp - mp_s[i]) * A.s;
