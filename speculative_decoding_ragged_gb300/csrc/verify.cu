@@ -637,15 +637,18 @@ bonus_tiles_kernel(FinalArgs A, int ctas_per_request)
             out[2 * t + 1] = sp;
         }
     }
-    // the request's last tile CTA to finish draws the token (no CTA ever waits for another)
+    // the request's last tile CTA to finish draws the token (no CTA ever waits for another):
+    // each lane that wrote tile sums publishes them at device scope, then one thread counts
+    // the CTA done; the pick reads the sums from L2 (ld.global.cg)
     __shared__ bool last_s;
-    __threadfence();
+    if (lane == 0) __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0) {
         last_s = atomicAdd(A.done + b, 1u) == static_cast<unsigned>(ctas_per_request) - 1;
+        if (last_s) __threadfence();
+    }
     __syncthreads();
     if (!last_s) return;
-    __threadfence();
     bonus_pick<DT>(A, b, job, n_hist);
 }
 
