@@ -17,7 +17,9 @@
 // win_count (shared memory, or nullptr): the scheduler's per-request counts, window = 1 + count,
 // read instead of the windows array by the fused schedule-and-pack kernel, which also passes
 // each thread's tier (tiers[tid], or INT_MAX past n_tiers) loaded at its start as tier_pre and,
-// when they fit, the block tokens copied into shared memory at its start as tok_stage.
+// when they fit, the block tokens copied into shared memory at its start as tok_stage, and
+// row_owner (shared memory for M ints, or nullptr): filled here with each row's request so
+// that the row writers need no search over cu.
 #pragma once
 #include "common.cuh"
 
@@ -42,7 +44,8 @@ __device__ __forceinline__ void pack_block(const int32_t* windows, const int32_t
                                            int32_t* __restrict__ meta, int32_t* __restrict__ status,
                                            const int* win_count = nullptr,
                                            const int* tier_pre = nullptr,
-                                           const int* tok_stage = nullptr)
+                                           const int* tok_stage = nullptr,
+                                           int* row_owner = nullptr)
 {
     constexpr int kWarps = kPackThreads / 32;
     __shared__ int warp_total[kWarps];
@@ -114,16 +117,23 @@ __device__ __forceinline__ void pack_block(const int32_t* windows, const int32_t
         w = w < 1 ? 1 : (w > gamma ? gamma : w);
         cu_s[b] = acc;
         cu_out[b] = acc;
+        if (row_owner != nullptr)
+            for (int i = 0; i < w; ++i) row_owner[acc + i] = b;
         acc += w;
     }
     if (tid == 0) cu_out[B] = M;
     __syncthreads();
     const int rows = min(M, packed_cap);
     for (int r = tid; r < rows; r += kPackThreads) {
-        int lo = 0, hi = B;
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (cu_s[mid] <= r) lo = mid; else hi = mid;
+        int lo = 0;
+        if (row_owner != nullptr) {
+            lo = row_owner[r];
+        } else {
+            int hi = B;
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (cu_s[mid] <= r) lo = mid; else hi = mid;
+            }
         }
         const int i = r - cu_s[lo];
         const int64_t ti = static_cast<int64_t>(lo) * gamma + i;

@@ -465,14 +465,16 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
     __syncthreads();
     for (int b = tid; b < B; b += kThreads) windows[b] = 1 + count[b];
     if (PACK) {
-        // count[] is complete (barrier above) and the pack reads the windows from it; the staged
-        // tokens are complete once every thread's copies have landed (the pack's first barrier
-        // comes before its first read of them)
+        // count[] is complete (barrier above) and the pack reads the windows from it; the sort
+        // buffers (at least 2n >= M ints from the start of shared memory) are free and hold the
+        // rows' owners; the staged tokens are complete once every thread's copies have landed
+        // (the pack's first barrier comes before its first read of them)
         static_assert(kPackThreads == kThreads, "the pack body runs on the scheduler's CTA");
         if (tok_stage != nullptr) asm volatile("cp.async.wait_all;" ::: "memory");
         pack_block<false>(windows, pk.tokens, B, L + 1, pk.tiers, pk.n_tiers, pk.cu,
                           pk.packed_ids, pk.row_req, pk.row_pos, pk.packed_cap, pk.meta, status,
-                          count, &tier_pre, tok_stage);
+                          count, &tier_pre, tok_stage,
+                          reinterpret_cast<int*>(smem_raw));   // the sort buffers, free now
     }
 }
 
