@@ -10,23 +10,25 @@
 //   1. survivals -> fixed-point keys; request b's keys already descend along j (survivals
 //      never grow), so the array starts as B sorted runs in (request, position) order. The
 //      theta entries this thread will need are fetched in the same round trip;
-//   2. n <= 4096: stable merge-path merging of the runs, log2(B) rounds. Keys are 32-bit
-//      (2^32 itself, a survival of exactly 1, is stored as 2^32 - 1, which no other key can
-//      be), indices travel in a parallel array, and on equal keys the lower run goes first,
-//      so the result is ordered by key descending, then request, then position. Each thread
-//      finds the co-rank of its first output with one binary search and merges its outputs
-//      sequentially. Larger n: a bitonic sort of 64-bit words key << 31 | (2^31 - 1 - index);
+//   2. n <= 4096: a counting sort over 4096 order-preserving key buckets, then the exact place
+//      inside each (small) bucket by one 64-bit compare per pair, which orders by key
+//      descending, then request, then position; it also records every candidate's rank. When
+//      a bucket is too big (many equal keys), a stable merge of the runs instead. Larger n: a
+//      bitonic sort of 64-bit words key << 31 | (2^31 - 1 - index);
 //   3. block-wide inclusive scan of the keys (exact uint64 sums S(K));
 //   4. obj(K) = double(B*2^32 + S(K)) / T(K). FP64 throughput is scarce on this part, so an
 //      fp32 screen (theta read from its bits with integer operations, error < 1e-6 relative)
 //      finds the K within 1e-5 of the best and only those, plus any K the screen cannot
-//      judge (negative or extreme T), get the exact fp64 evaluation; the block argmax compares
-//      the objectives' bit patterns as integers (they are positive) and takes the smallest K
-//      among equal objectives;
-//   5. windows w_b = 1 + count of request b among the first K* candidates.
-// Latency-bound (microseconds); the grid is one CTA by construction of the problem.
+//      judge (negative or extreme T), get the exact fp64 evaluation, gathered onto as few
+//      lanes as possible; the argmax compares the objectives' bit patterns as integers (they
+//      are positive) and takes the smallest K among equal objectives;
+//   5. windows w_b = 1 + count of request b among the first K* candidates: with the ranks,
+//      the length of the prefix of its run ranked below K*.
+// Latency-bound (microseconds); the grid is one CTA by construction of the problem. Every
+// two-level reduction publishes per-warp totals behind one barrier and lets each warp combine
+// them itself. The kernel runs once per step from a cold instruction cache, so its loops stay
+// rolled: code size, not arithmetic, sets much of its time.
 #include "common.cuh"
-#include "pack_block.cuh"
 
 namespace dspark {
 namespace {
@@ -89,24 +91,26 @@ template <bool MERGE>
 __device__ __forceinline__ void write_run(const float* __restrict__ conf, int b, int L,
                                           uint64_t* word, uint32_t* key32, int* index)
 {
-    float c[DSPARK_MAX_GAMMA - 1];
-#pragma unroll
-    for (int j = 0; j < DSPARK_MAX_GAMMA - 1; ++j)
-        if (j < L) c[j] = __ldg(conf + static_cast<int64_t>(b) * L + j);
     float s = 1.0f;
+#pragma unroll 1
+    for (int j0 = 0; j0 < L; j0 += 8) {
+        float c[8];
 #pragma unroll
-    for (int j = 0; j < DSPARK_MAX_GAMMA - 1; ++j) {
-        if (j < L) {
-            s = __fmul_rn(s, fminf(fmaxf(c[j], 0.0f), 1.0f));   // NaN -> 0
-            const int idx = b * L + j;
-            // s < 1 gives at most 2^32 - 256; s == 1 gives 2^32, kept as 2^32 - 1 in 32 bits
-            const uint32_t k32 = s >= 1.0f ? 0xFFFFFFFFu : __float2uint_rn(__fmul_rn(s, 4294967296.0f));
-            if (MERGE) {
-                key32[idx] = k32;
-                index[idx] = idx;
-            } else {
-                const uint64_t key = s >= 1.0f ? (1ull << 32) : static_cast<uint64_t>(k32);
-                word[idx] = (key << 31) | static_cast<uint64_t>(0x7FFFFFFF - idx);
+        for (int j = 0; j < 8; ++j)
+            if (j0 + j < L) c[j] = __ldg(conf + static_cast<int64_t>(b) * L + j0 + j);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (j0 + j < L) {
+                s = __fmul_rn(s, fminf(fmaxf(c[j], 0.0f), 1.0f));   // NaN -> 0
+                const int idx = b * L + j0 + j;
+                const uint32_t k32 = s >= 1.0f ? 0xFFFFFFFFu : __float2uint_rn(__fmul_rn(s, 4294967296.0f));
+                if (MERGE) {
+                    key32[idx] = k32;
+                    index[idx] = idx;
+                } else {
+                    const uint64_t key = s >= 1.0f ? (1ull << 32) : static_cast<uint64_t>(k32);
+                    word[idx] = (key << 31) | static_cast<uint64_t>(0x7FFFFFFF - idx);
+                }
             }
         }
     }
@@ -134,7 +138,147 @@ __device__ __forceinline__ uint64_t key_value(uint32_t k32)
     return k32 == 0xFFFFFFFFu ? (1ull << 32) : static_cast<uint64_t>(k32);
 }
 
-// PACK: the same CTA then front-packs the windows it wrote (dspark_schedule_pack).
+// Bits of a double, exactly, from an integer below 2^53 (integer operations only).
+__device__ __forceinline__ double u53_to_double(uint64_t x)
+{
+    if (x == 0) return 0.0;
+    const int lz = __clzll(static_cast<long long>(x));          // >= 11
+    const uint64_t m = x << (lz - 11);                           // leading one at bit 52
+    const uint64_t e = static_cast<uint64_t>(1023 + 63 - lz);
+    return __longlong_as_double(static_cast<long long>((e << 52) | (m & ((1ull << 52) - 1))));
+}
+
+// The exact objective double(E) / T(K), T = t0 + theta: its bit pattern, or 0 (none) when T is
+// not positive and finite.
+__device__ __noinline__ uint64_t exact_objective(uint64_t E, double t0, uint64_t theta_bits)
+{
+    const double T = t0 + __longlong_as_double(static_cast<long long>(theta_bits));
+    const uint64_t tb = static_cast<uint64_t>(__double_as_longlong(T));
+    if ((tb >> 63) != 0 || tb == 0 || ((tb >> 52) & 0x7FF) == 0x7FF) return 0;
+    return static_cast<uint64_t>(__double_as_longlong(u53_to_double(E) / T));
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt()
+{
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Sum over the warps before this one of a per-warp total, read by every lane of the warp from
+// shared memory after the barrier that published the totals (no second barrier).
+template <typename T>
+__device__ __forceinline__ T warps_before(const T* total, int warp, int lane)
+{
+    T v = lane < warp ? total[lane] : T(0);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+// The front-pack on the scheduler's CTA (dspark_schedule_pack). The windows are valid by
+// construction (1 + a count of at most gamma - 1), so M = B + K* is known before any scan and
+// the tier is reduced in the same barrier as the scan of the windows. Then each warp writes
+// the rows of its own requests: the requests' rows form one contiguous range, which the warp
+// fills coalesced from a warp-private stretch of the row-owner map (request << 5 | position),
+// after a warp-level sync only. win(b) gives request b's window; owner holds M ints and may
+// overlay what win reads (every window is read before the block barrier).
+template <typename WinFn>
+__device__ __forceinline__ void pack_after_schedule(WinFn win, int B, int gamma, int K_star,
+                                                    PackArgs pk, int tier_pre,
+                                                    const int* tok_stage, int* owner,
+                                                    int* tier_s, int* pack_total, int* win_s,
+                                                    int32_t* __restrict__ windows,
+                                                    int32_t* __restrict__ status)
+{
+    // the output pointers as plain locals: no store below can be taken to change them
+    int32_t* const cu = pk.cu;
+    int32_t* const packed_ids = pk.packed_ids;
+    int32_t* const row_req = pk.row_req;
+    int32_t* const row_pos = pk.row_pos;
+    int32_t* const meta = pk.meta;
+    const int32_t* const tokens = pk.tokens;
+    const int packed_cap = pk.packed_cap;
+    const unsigned full = 0xffffffffu;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int M = B + K_star;
+
+    // tier: the smallest tier >= M (tier_pre is INT_MAX past n_tiers)
+    int best = tier_pre >= M ? tier_pre : INT_MAX;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) best = min(best, __shfl_xor_sync(full, best, off));
+    if (lane == 0 && best != INT_MAX) atomicMin(tier_s, best);
+
+    // windows of this thread's consecutive requests (kept in win_s), and their scan
+    const int items = (B + kThreads - 1) / kThreads;
+    const int b0 = tid * items;
+    int run = 0;
+#pragma unroll 1
+    for (int it = 0; it < items; ++it) {
+        const int b = b0 + it;
+        if (b >= B) break;
+        const int w = win(b);
+        windows[b] = w;
+        win_s[b] = w;
+        run += w;
+    }
+    int incl = run;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(full, incl, off);
+        if (lane >= off) incl += v;
+    }
+    if (lane == 31) pack_total[warp] = incl;
+    __syncthreads();
+    const int base = warps_before(pack_total, warp, lane);
+    const int warp_rows = __shfl_sync(full, incl, 31);
+    int acc = base + incl - run;
+#pragma unroll 1
+    for (int it = 0; it < items; ++it) {
+        const int b = b0 + it;
+        if (b >= B) break;
+        const int w = win_s[b];
+        cu[b] = acc;
+#pragma unroll 1
+        for (int i = 0; i < w; ++i) owner[acc + i] = (b << 5) | i;
+        acc += w;
+    }
+    if (tid == 0) cu[B] = M;
+    __syncwarp();
+    const int r_end = min(base + warp_rows, packed_cap);
+#pragma unroll 1
+    for (int r = base + lane; r < r_end; r += 32) {
+        const int e = owner[r];
+        const int b = e >> 5, i = e & 31;
+        const int64_t ti = static_cast<int64_t>(b) * gamma + i;
+        packed_ids[r] = tok_stage != nullptr ? tok_stage[ti] : __ldg(tokens + ti);
+        if (row_req) row_req[r] = b;
+        if (row_pos) row_pos[r] = i;
+    }
+    int tier = *tier_s;
+    int bad = 0;
+    if (tier == INT_MAX) {
+        tier = M;
+        bad |= DSPARK_STATUS_TIER_OVERFLOW;
+    }
+    if (tier > packed_cap) bad |= DSPARK_STATUS_PACK_CAPACITY;
+    const int rows_pad = min(tier, packed_cap);
+#pragma unroll 1
+    for (int r = M + tid; r < rows_pad; r += kThreads) {
+        packed_ids[r] = 0;
+        if (row_req) row_req[r] = -1;
+        if (row_pos) row_pos[r] = -1;
+    }
+    if (tid == 0) {
+        meta[0] = M;
+        meta[1] = tier;
+        raise_status(status, bad);      // the same bits in every thread
+    }
+}
+
+// PACK: the same CTA then front-packs the windows it computed (dspark_schedule_pack).
 template <bool MERGE, bool PACK>
 __global__ void __launch_bounds__(kThreads, 1)
 schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, double bias,
@@ -145,7 +289,7 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
     extern __shared__ __align__(16) unsigned char smem_raw[];
     // MERGE: keys ksrc [n] (u32), indices isrc [n], then the ping-pong pair kdst, idst (the
     // bucket path uses that second half as n 64-bit rank words); else words [n_pad] (u64).
-    // Then count [B].
+    // Then count [B]. The pack's row-owner map overlays the start (M <= B + n ints).
     uint64_t* word = reinterpret_cast<uint64_t*>(smem_raw);
     uint32_t* ksrc = reinterpret_cast<uint32_t*>(smem_raw);
     int* isrc = reinterpret_cast<int*>(ksrc + n);
@@ -157,14 +301,14 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
     __shared__ uint64_t red_obj[kWarps];
     __shared__ int red_k[kWarps];
     __shared__ float red_f[kWarps];
-    __shared__ int k_best;
-    __shared__ float f_best;
     __shared__ double t0_s;
     __shared__ __align__(16) int bucket_cnt[MERGE ? kBuckets : 4];
     __shared__ __align__(16) int bucket_start[MERGE ? kBuckets : 4];
     __shared__ int warp_int[kWarps];
+    __shared__ int tier_s;
 
     pdl_wait_and_trigger();
+    const unsigned full = 0xffffffffu;
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
@@ -174,15 +318,18 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
         // the pack's inputs are read only at the end: its tier now, and its tokens copied into
         // shared memory (cp.async, 16-byte pieces) while the scheduler works, when they fit
         if (tid < pk.n_tiers) tier_pre = __ldg(pk.tiers + tid);
+        if (tid == 0) tier_s = INT_MAX;
         if (tok_stage_off >= 0) {
             tok_stage = reinterpret_cast<int*>(smem_raw + tok_stage_off);
             const int nt = B * (L + 1);
             const int n16 = nt >> 2;
+#pragma unroll 1
             for (int c = tid; c < n16; c += kThreads) {
                 const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(tok_stage + 4 * c));
                 asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
                              "l"(pk.tokens + 4 * c) : "memory");
             }
+#pragma unroll 1
             for (int t = 4 * n16 + tid; t < nt; t += kThreads) tok_stage[t] = __ldg(pk.tokens + t);
             asm volatile("cp.async.commit_group;" ::: "memory");
         }
@@ -204,54 +351,50 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
         th0 = __ldg(theta_bits + B);
         t0_s = bias + __ldg(alpha + B);
     }
+#pragma unroll 1
     for (int b = tid; b < B; b += kThreads) {
         write_run<MERGE>(conf, b, L, word, ksrc, isrc);
-        count[b] = 0;
+        if (!MERGE) count[b] = 0;
     }
-    if (MERGE)
-        for (int j = tid; j < kBuckets; j += kThreads) bucket_cnt[j] = 0;
+    if (MERGE) {
+        static_assert(kBuckets % (4 * kThreads) == 0, "16-byte zeroing of the bucket counts");
+        for (int j = 4 * tid; j < kBuckets; j += 4 * kThreads)
+            *reinterpret_cast<int4*>(bucket_cnt + j) = make_int4(0, 0, 0, 0);
+    }
     if (!MERGE)
         for (int i = n + tid; i < n_pad; i += kThreads) word[i] = 0;   // sorts after all words
     __syncthreads();
 
-    // 2. sort descending
+    // 2. sort descending. MERGE also yields rank_of[i]: the sorted position of candidate i
+    int* rank_of = isrc;
     bool sorted = false;
     if (MERGE) {
         // 2a. counting sort by key bucket, when every bucket is small
+#pragma unroll 1
         for (int p = tid; p < n; p += kThreads) atomicAdd(&bucket_cnt[key_bucket(ksrc[p])], 1);
         __syncthreads();
-        int big = 0;
-        for (int j = tid; j < kBuckets; j += kThreads) big |= bucket_cnt[j] > kBucketMax;
+        // bucket starts in descending bucket order; thread t owns the reversed buckets
+        // kBuckets - 1 - (kBucketsPerThread * t + m), m = 0..kBucketsPerThread-1
+        static_assert(kBucketsPerThread == 4, "one 16-byte vector of counts per thread");
+        const int jv = kBuckets - 4 - 4 * tid;            // the thread's four buckets
+        const int4 cv = *reinterpret_cast<const int4*>(bucket_cnt + jv);
+        const int a[4] = {cv.w, cv.z, cv.y, cv.x};        // descending bucket order
+        const int own = (cv.x + cv.y) + (cv.z + cv.w);
+        const int big = max(max(cv.x, cv.y), max(cv.z, cv.w)) > kBucketMax;
+        int incl_b = own;
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(full, incl_b, off);
+            if (lane >= off) incl_b += v;
+        }
+        if (lane == 31) warp_int[warp] = incl_b;
         if (!__syncthreads_or(big)) {
-            // bucket starts in descending bucket order; thread t owns the reversed buckets
-            // kBuckets - 1 - (kBucketsPerThread * t + m), m = 0..kBucketsPerThread-1
-            static_assert(kBucketsPerThread == 4, "one 16-byte vector of counts per thread");
-            const int jv = kBuckets - 4 - 4 * tid;            // the thread's four buckets
-            const int4 cv = *reinterpret_cast<const int4*>(bucket_cnt + jv);
-            const int a[4] = {cv.w, cv.z, cv.y, cv.x};        // descending bucket order
-            const int own = (cv.x + cv.y) + (cv.z + cv.w);
-            int incl_b = own;
-            for (int off = 1; off < 32; off <<= 1) {
-                const int v = __shfl_up_sync(0xffffffffu, incl_b, off);
-                if (lane >= off) incl_b += v;
-            }
-            if (lane == 31) warp_int[warp] = incl_b;
-            __syncthreads();
-            if (warp == 0) {
-                int t = warp_int[lane];
-                for (int off = 1; off < 32; off <<= 1) {
-                    const int v = __shfl_up_sync(0xffffffffu, t, off);
-                    if (lane >= off) t += v;
-                }
-                warp_int[lane] = t;
-            }
-            __syncthreads();
-            const int ex = incl_b - own + (warp > 0 ? warp_int[warp - 1] : 0);
+            const int ex = incl_b - own + warps_before(warp_int, warp, lane);
             *reinterpret_cast<int4*>(bucket_start + jv) =
                 make_int4(ex + a[0] + a[1] + a[2], ex + a[0] + a[1], ex + a[0], ex);
             __syncthreads();
             // scatter rank words into the bucket ranges (any order inside a bucket); afterwards
             // bucket_start[j] holds the end of bucket j
+#pragma unroll 1
             for (int p = tid; p < n; p += kThreads) {
                 const uint32_t k = ksrc[p];
                 const int q = atomicAdd(&bucket_start[key_bucket(k)], 1);
@@ -259,14 +402,16 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
             }
             __syncthreads();
             // exact place inside the bucket: one unsigned compare orders (key desc, index asc)
+#pragma unroll 1
             for (int q = tid; q < n; q += kThreads) {
                 const uint64_t x = rword[q];
                 const int j = key_bucket(static_cast<uint32_t>(x >> 32));
                 const int c = bucket_cnt[j], s0 = bucket_start[j] - c;
                 int r = 0;
+#pragma unroll 4
                 for (int t = s0; t < s0 + c; ++t) r += rword[t] > x;
                 ksrc[s0 + r] = static_cast<uint32_t>(x >> 32);
-                isrc[s0 + r] = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(x));
+                rank_of[static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(x))] = s0 + r;
             }
             __syncthreads();
             sorted = true;
@@ -277,6 +422,7 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
         for (int R = L; R < n; R <<= 1) {          // run length: one request, two, four, ...
             int o = p0;
             const int o_end = min(p0 + items, n);
+#pragma unroll 1
             while (o < o_end) {
                 const int aS = o / (2 * R) * (2 * R);
                 const int aE = min(aS + R, n), bE = min(aS + 2 * R, n);
@@ -286,11 +432,13 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
                 // co-rank: how many of the first d merged outputs come from run A
                 const int d = o - aS;
                 int lo = max(0, d - lenB), hi = min(d, lenA);
+#pragma unroll 1
                 while (lo < hi) {
                     const int mid = (lo + hi) >> 1;
                     if (A[mid] >= Bk[d - mid - 1]) lo = mid + 1; else hi = mid;
                 }
                 int i = lo, j = d - lo;
+#pragma unroll 1
                 for (; o < o_end && o < bE; ++o) {
                     const bool takeA = i < lenA && (j >= lenB || A[i] >= Bk[j]);
                     if (takeA) {
@@ -308,6 +456,11 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
             uint32_t* tk = ksrc; ksrc = kdst; kdst = tk;
             int* ti = isrc; isrc = idst; idst = ti;
         }
+        // ranks into the free index buffer
+#pragma unroll 1
+        for (int p = tid; p < n; p += kThreads) idst[isrc[p]] = p;
+        rank_of = idst;
+        __syncthreads();
     } else if (!MERGE) {
         for (int k = 2; k <= n_pad; k <<= 1) {
             for (int j = k >> 1; j > 0; j >>= 1) {
@@ -328,38 +481,31 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
     auto key_at = [&](int p) -> uint64_t {
         return MERGE ? key_value(ksrc[p]) : (word[p] >> 31);
     };
-    auto index_at = [&](int p) -> int {
-        return MERGE ? isrc[p] : 0x7FFFFFFF - static_cast<int>(word[p] & 0x7FFFFFFFull);
+    auto theta_at = [&](int it, int p) -> uint64_t {
+        if (!MERGE) return __ldg(theta_bits + B + p + 1);
+        static_assert(kMergeItems == 4, "select chain over the thread's theta entries");
+        return it == 0 ? th[0] : it == 1 ? th[1] : it == 2 ? th[2] : th[3];
     };
 
     // 3. inclusive scan of keys over each thread's contiguous positions
     uint64_t run = 0;
-#pragma unroll
+#pragma unroll 1
     for (int it = 0; it < kMaxItems; ++it) {
         const int p = p0 + it;
         if (it < items && p < n) run += key_at(p);
     }
     uint64_t incl = run;
     for (int off = 1; off < 32; off <<= 1) {
-        const uint64_t v = __shfl_up_sync(0xffffffffu, incl, off);
+        const uint64_t v = __shfl_up_sync(full, incl, off);
         if (lane >= off) incl += v;
     }
     if (lane == 31) warp_total[warp] = incl;
     __syncthreads();
-    if (warp == 0) {
-        uint64_t t = warp_total[lane];
-        for (int off = 1; off < 32; off <<= 1) {
-            const uint64_t v = __shfl_up_sync(0xffffffffu, t, off);
-            if (lane >= off) t += v;
-        }
-        warp_total[lane] = t;   // inclusive over warps
-    }
-    __syncthreads();
-    const uint64_t S_excl = incl - run + (warp > 0 ? warp_total[warp - 1] : 0);
+    const uint64_t S_excl = incl - run + warps_before(warp_total, warp, lane);
     const uint64_t base_E = static_cast<uint64_t>(B) << 32;
     const double t0 = t0_s;
     bool t0_ok = true;
-    const float t0f = nonneg_double_to_float(__double_as_longlong(t0), t0_ok);
+    const float t0f = nonneg_double_to_float(static_cast<uint64_t>(__double_as_longlong(t0)), t0_ok);
 
     // 4a. fp32 screen over the K this thread owns
     float fb = -INFINITY;
@@ -369,64 +515,86 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
     }
     {
         uint64_t S = S_excl;
-#pragma unroll
+#pragma unroll 1
         for (int it = 0; it < kMaxItems; ++it) {
             const int p = p0 + it;
             if (it >= items || p >= n) break;
             S += key_at(p);
-            const uint64_t tb = MERGE ? th[it % kMergeItems] : __ldg(theta_bits + B + p + 1);
             float f;
-            if (!screen(base_E + S, t0f, t0_ok, tb, f)) fb = fmaxf(fb, f);
+            if (!screen(base_E + S, t0f, t0_ok, theta_at(it, p), f)) fb = fmaxf(fb, f);
         }
     }
-    for (int off = 16; off > 0; off >>= 1) fb = fmaxf(fb, __shfl_xor_sync(0xffffffffu, fb, off));
+    for (int off = 16; off > 0; off >>= 1) fb = fmaxf(fb, __shfl_xor_sync(full, fb, off));
     if (lane == 0) red_f[warp] = fb;
     __syncthreads();
-    if (warp == 0) {
-        float v = red_f[lane];
-        for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-        if (lane == 0) f_best = v;
-    }
-    __syncthreads();
+    float f_best = red_f[lane];
+    for (int off = 16; off > 0; off >>= 1) f_best = fmaxf(f_best, __shfl_xor_sync(full, f_best, off));
     const float thr = f_best * kScreen;
 
-    // 4b. exact objective for the candidates: near the screen's best, or not screenable
+    // 4b. exact objectives of the candidates (near the screen's best, or not screenable). The
+    // candidates of a warp are handed to its free lanes first, so that the warp runs its
+    // FP64 divisions in as few passes as possible (one while it has at most 32 candidates).
     uint64_t best_obj = 0;        // bit pattern of a positive double; 0 = none
     int best_k = -1;
+    uint64_t pend_E = 0, pend_t = 0;
+    int pend_k = -1;              // this lane's pending candidate
     if (tid == 0) {
         float f = 0.0f;
         if (screen(base_E, t0f, t0_ok, th0, f) || f >= thr) {
-            const double T = t0 + __longlong_as_double(th0);
-            if (T > 0.0 && T < INFINITY) {
-                best_obj = __double_as_longlong(static_cast<double>(base_E) / T);
-                best_k = 0;
-            }
+            pend_E = base_E;
+            pend_t = th0;
+            pend_k = 0;
         }
     }
+    auto evaluate_pending = [&]() {
+        if (pend_k >= 0) {
+            const uint64_t obj = exact_objective(pend_E, t0, pend_t);
+            if (obj != 0 && better(obj, pend_k, best_obj, best_k)) {
+                best_obj = obj;
+                best_k = pend_k;
+            }
+            pend_k = -1;
+        }
+    };
     {
         uint64_t S = S_excl;
-#pragma unroll
+#pragma unroll 1
         for (int it = 0; it < kMaxItems; ++it) {
+            if (it >= items) break;                   // uniform across the block
             const int p = p0 + it;
-            if (it >= items || p >= n) break;
-            S += key_at(p);
-            const uint64_t tb = MERGE ? th[it % kMergeItems] : __ldg(theta_bits + B + p + 1);
-            float f = 0.0f;
-            if (screen(base_E + S, t0f, t0_ok, tb, f) || f >= thr) {
-                const double T = t0 + __longlong_as_double(tb);
-                if (T > 0.0 && T < INFINITY) {
-                    const uint64_t obj = __double_as_longlong(static_cast<double>(base_E + S) / T);
-                    if (better(obj, p + 1, best_obj, best_k)) {
-                        best_obj = obj;
-                        best_k = p + 1;
-                    }
-                }
+            bool cand = false;
+            uint64_t tb = 0;
+            if (p < n) {
+                S += key_at(p);
+                tb = theta_at(it, p);
+                float f = 0.0f;
+                cand = screen(base_E + S, t0f, t0_ok, tb, f) || f >= thr;
+            }
+            const unsigned cm = __ballot_sync(full, cand);
+            if (cm == 0) continue;
+            unsigned fm = __ballot_sync(full, pend_k < 0);
+            if (__popc(cm) > __popc(fm)) {
+                evaluate_pending();
+                fm = full;
+            }
+            // the k-th candidate (in lane order) goes to the k-th free lane
+            const int fr = __popc(fm & lanemask_lt());
+            const bool take = pend_k < 0 && fr < __popc(cm);
+            const int src = take ? static_cast<int>(__fns(cm, 0, fr + 1)) : lane;
+            const uint64_t e = __shfl_sync(full, base_E + S, src);
+            const uint64_t t = __shfl_sync(full, tb, src);
+            const int k = __shfl_sync(full, p + 1, src);
+            if (take) {
+                pend_E = e;
+                pend_t = t;
+                pend_k = k;
             }
         }
     }
+    evaluate_pending();
     for (int off = 16; off > 0; off >>= 1) {
-        const uint64_t o = __shfl_xor_sync(0xffffffffu, best_obj, off);
-        const int kk = __shfl_xor_sync(0xffffffffu, best_k, off);
+        const uint64_t o = __shfl_xor_sync(full, best_obj, off);
+        const int kk = __shfl_xor_sync(full, best_k, off);
         if (better(o, kk, best_obj, best_k)) {
             best_obj = o;
             best_k = kk;
@@ -437,44 +605,54 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
         red_k[warp] = best_k;
     }
     __syncthreads();
-    if (warp == 0) {
-        best_obj = red_obj[lane];
-        best_k = red_k[lane];
-        for (int off = 16; off > 0; off >>= 1) {
-            const uint64_t o = __shfl_xor_sync(0xffffffffu, best_obj, off);
-            const int kk = __shfl_xor_sync(0xffffffffu, best_k, off);
-            if (better(o, kk, best_obj, best_k)) {
-                best_obj = o;
-                best_k = kk;
-            }
-        }
-        if (lane == 0) {
-            if (best_k < 0) {
-                raise_status(status, DSPARK_STATUS_BAD_COST);
-                best_k = 0;
-            }
-            k_best = best_k;
-            *k_star = best_k;
+    // every warp reduces the 32 warp results itself
+    best_obj = red_obj[lane];
+    best_k = red_k[lane];
+    for (int off = 16; off > 0; off >>= 1) {
+        const uint64_t o = __shfl_xor_sync(full, best_obj, off);
+        const int kk = __shfl_xor_sync(full, best_k, off);
+        if (better(o, kk, best_obj, best_k)) {
+            best_obj = o;
+            best_k = kk;
         }
     }
-    __syncthreads();
+    const bool none = best_k < 0;   // no K with a positive, finite step time
+    const int K_star = none ? 0 : best_k;
+    if (tid == 0) {
+        if (none) raise_status(status, DSPARK_STATUS_BAD_COST);
+        *k_star = K_star;
+    }
 
-    // 5. windows
-    const int K_star = k_best;
-    for (int p = tid; p < K_star; p += kThreads) atomicAdd(&count[index_at(p) / L], 1);
-    __syncthreads();
-    for (int b = tid; b < B; b += kThreads) windows[b] = 1 + count[b];
+    // 5. windows: w_b = 1 + the request's candidates among the first K*. Its candidates sit at
+    // increasing sorted positions along j, so they are a prefix of its run.
+    auto win_rank = [&](int b) -> int {
+        int c = 0;
+#pragma unroll 1
+        for (int j = 0; j < L; ++j) c += rank_of[b * L + j] < K_star;
+        return 1 + c;
+    };
+    if (!MERGE) {
+        for (int p = tid; p < K_star; p += kThreads) {
+            const int idx = 0x7FFFFFFF - static_cast<int>(word[p] & 0x7FFFFFFFull);
+            atomicAdd(&count[idx / L], 1);
+        }
+        __syncthreads();
+    }
+    auto win_count = [&](int b) -> int { return 1 + count[b]; };
     if (PACK) {
-        // count[] is complete (barrier above) and the pack reads the windows from it; the sort
-        // buffers (at least 2n >= M ints from the start of shared memory) are free and hold the
-        // rows' owners; the staged tokens are complete once every thread's copies have landed
-        // (the pack's first barrier comes before its first read of them)
-        static_assert(kPackThreads == kThreads, "the pack body runs on the scheduler's CTA");
+        // the staged tokens are complete once every thread's copies have landed (the pack's
+        // barrier comes before its first read of them)
         if (tok_stage != nullptr) asm volatile("cp.async.wait_all;" ::: "memory");
-        pack_block<false>(windows, pk.tokens, B, L + 1, pk.tiers, pk.n_tiers, pk.cu,
-                          pk.packed_ids, pk.row_req, pk.row_pos, pk.packed_cap, pk.meta, status,
-                          count, &tier_pre, tok_stage,
-                          reinterpret_cast<int*>(smem_raw));   // the sort buffers, free now
+        __shared__ int pack_total[kWarps];
+        int* owner = reinterpret_cast<int*>(smem_raw);   // sort buffers: at least B + n ints
+        if (MERGE)
+            pack_after_schedule(win_rank, B, L + 1, K_star, pk, tier_pre, tok_stage, owner,
+                                &tier_s, pack_total, count, windows, status);
+        else
+            pack_after_schedule(win_count, B, L + 1, K_star, pk, tier_pre, tok_stage, owner,
+                                &tier_s, pack_total, count, windows, status);
+    } else {
+        for (int b = tid; b < B; b += kThreads) windows[b] = MERGE ? win_rank(b) : win_count(b);
     }
 }
 
@@ -612,7 +790,7 @@ schedule_small_kernel(const float* __restrict__ conf, int B, int L, double bias,
     if (lane == 0) *k_star = K_star;
 
     if (PACK) {
-        // front-pack: cu by a warp scan of the windows, tier, rows, padding (as pack_block)
+        // front-pack: cu by a warp scan of the windows, tier, rows, padding (as the pack kernel)
         const int wv = lane < B ? 1 + cnt : 0;
         int incl = wv;
 #pragma unroll
