@@ -165,6 +165,19 @@ __device__ __forceinline__ uint32_t lanemask_lt()
     return m;
 }
 
+// Element i of a four-entry register array, by selects (no local memory under a rolled loop).
+__device__ __forceinline__ float get4(const float (&a)[4], int i)
+{
+    return i == 0 ? a[0] : i == 1 ? a[1] : i == 2 ? a[2] : a[3];
+}
+__device__ __forceinline__ void set4(float (&a)[4], int i, float v)
+{
+    a[0] = i == 0 ? v : a[0];
+    a[1] = i == 1 ? v : a[1];
+    a[2] = i == 2 ? v : a[2];
+    a[3] = i == 3 ? v : a[3];
+}
+
 // Sum over the warps before this one of a per-warp total, read by every lane of the warp from
 // shared memory after the barrier that published the totals (no second barrier).
 template <typename T>
@@ -205,57 +218,65 @@ __device__ __forceinline__ void pack_after_schedule(WinFn win, int B, int gamma,
     const int warp = tid >> 5;
     const int M = B + K_star;
 
-    // tier: the smallest tier >= M (tier_pre is INT_MAX past n_tiers)
-    int best = tier_pre >= M ? tier_pre : INT_MAX;
+    // tier: the smallest tier >= M (tier_pre is INT_MAX past n_tiers); warps without tiers skip
+    if (warp * 32 < pk.n_tiers) {
+        int best = tier_pre >= M ? tier_pre : INT_MAX;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) best = min(best, __shfl_xor_sync(full, best, off));
-    if (lane == 0 && best != INT_MAX) atomicMin(tier_s, best);
+        for (int off = 16; off > 0; off >>= 1) best = min(best, __shfl_xor_sync(full, best, off));
+        if (lane == 0 && best != INT_MAX) atomicMin(tier_s, best);
+    }
 
-    // windows of this thread's consecutive requests (kept in win_s), and their scan
+    // windows of this thread's consecutive requests (kept in win_s), and their scan; the warps
+    // past the last request only meet the barrier and write padding
     const int items = (B + kThreads - 1) / kThreads;
     const int b0 = tid * items;
-    int run = 0;
+    const bool active = warp * 32 * items < B;       // uniform across the warp
+    int run = 0, incl = 0;
+    if (active) {
 #pragma unroll 1
-    for (int it = 0; it < items; ++it) {
-        const int b = b0 + it;
-        if (b >= B) break;
-        const int w = win(b);
-        windows[b] = w;
-        win_s[b] = w;
-        run += w;
-    }
-    int incl = run;
+        for (int it = 0; it < items; ++it) {
+            const int b = b0 + it;
+            if (b >= B) break;
+            const int w = win(b);
+            windows[b] = w;
+            win_s[b] = w;
+            run += w;
+        }
+        incl = run;
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int v = __shfl_up_sync(full, incl, off);
-        if (lane >= off) incl += v;
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(full, incl, off);
+            if (lane >= off) incl += v;
+        }
+        if (lane == 31) pack_total[warp] = incl;
     }
-    if (lane == 31) pack_total[warp] = incl;
     __syncthreads();
-    const int base = warps_before(pack_total, warp, lane);
-    const int warp_rows = __shfl_sync(full, incl, 31);
-    int acc = base + incl - run;
+    if (active) {
+        const int base = warps_before(pack_total, warp, lane);   // all earlier warps are active
+        const int warp_rows = __shfl_sync(full, incl, 31);
+        int acc = base + incl - run;
 #pragma unroll 1
-    for (int it = 0; it < items; ++it) {
-        const int b = b0 + it;
-        if (b >= B) break;
-        const int w = win_s[b];
-        cu[b] = acc;
+        for (int it = 0; it < items; ++it) {
+            const int b = b0 + it;
+            if (b >= B) break;
+            const int w = win_s[b];
+            cu[b] = acc;
 #pragma unroll 1
-        for (int i = 0; i < w; ++i) owner[acc + i] = (b << 5) | i;
-        acc += w;
-    }
-    if (tid == 0) cu[B] = M;
-    __syncwarp();
-    const int r_end = min(base + warp_rows, packed_cap);
+            for (int i = 0; i < w; ++i) owner[acc + i] = (b << 5) | i;
+            acc += w;
+        }
+        if (tid == 0) cu[B] = M;
+        __syncwarp();
+        const int r_end = min(base + warp_rows, packed_cap);
 #pragma unroll 1
-    for (int r = base + lane; r < r_end; r += 32) {
-        const int e = owner[r];
-        const int b = e >> 5, i = e & 31;
-        const int64_t ti = static_cast<int64_t>(b) * gamma + i;
-        packed_ids[r] = tok_stage != nullptr ? tok_stage[ti] : __ldg(tokens + ti);
-        if (row_req) row_req[r] = b;
-        if (row_pos) row_pos[r] = i;
+        for (int r = base + lane; r < r_end; r += 32) {
+            const int e = owner[r];
+            const int b = e >> 5, i = e & 31;
+            const int64_t ti = static_cast<int64_t>(b) * gamma + i;
+            packed_ids[r] = tok_stage != nullptr ? tok_stage[ti] : __ldg(tokens + ti);
+            if (row_req) row_req[r] = b;
+            if (row_pos) row_pos[r] = i;
+        }
     }
     int tier = *tier_s;
     int bad = 0;
@@ -507,11 +528,16 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
     bool t0_ok = true;
     const float t0f = nonneg_double_to_float(static_cast<uint64_t>(__double_as_longlong(t0)), t0_ok);
 
-    // 4a. fp32 screen over the K this thread owns
+    // 4a. fp32 screen over the K this thread owns. MERGE keeps each K's screen value for the
+    // exact pass (+inf where the screen cannot judge, so that K is always evaluated exactly)
     float fb = -INFINITY;
+    float fv[kMergeItems] = {0.0f, 0.0f, 0.0f, 0.0f};
+    float f_k0 = 0.0f;
     if (tid == 0) {
-        float f;
-        if (!screen(base_E, t0f, t0_ok, th0, f)) fb = f;
+        float f = 0.0f;
+        const bool no = screen(base_E, t0f, t0_ok, th0, f);
+        if (!no) fb = f;
+        f_k0 = no ? INFINITY : f;
     }
     {
         uint64_t S = S_excl;
@@ -520,8 +546,10 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
             const int p = p0 + it;
             if (it >= items || p >= n) break;
             S += key_at(p);
-            float f;
-            if (!screen(base_E + S, t0f, t0_ok, theta_at(it, p), f)) fb = fmaxf(fb, f);
+            float f = 0.0f;
+            const bool no = screen(base_E + S, t0f, t0_ok, theta_at(it, p), f);
+            if (!no) fb = fmaxf(fb, f);
+            if (MERGE) set4(fv, it, no ? INFINITY : f);
         }
     }
     for (int off = 16; off > 0; off >>= 1) fb = fmaxf(fb, __shfl_xor_sync(full, fb, off));
@@ -538,13 +566,10 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
     int best_k = -1;
     uint64_t pend_E = 0, pend_t = 0;
     int pend_k = -1;              // this lane's pending candidate
-    if (tid == 0) {
-        float f = 0.0f;
-        if (screen(base_E, t0f, t0_ok, th0, f) || f >= thr) {
-            pend_E = base_E;
-            pend_t = th0;
-            pend_k = 0;
-        }
+    if (tid == 0 && f_k0 >= thr) {
+        pend_E = base_E;
+        pend_t = th0;
+        pend_k = 0;
     }
     auto evaluate_pending = [&]() {
         if (pend_k >= 0) {
@@ -567,8 +592,12 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
             if (p < n) {
                 S += key_at(p);
                 tb = theta_at(it, p);
-                float f = 0.0f;
-                cand = screen(base_E + S, t0f, t0_ok, tb, f) || f >= thr;
+                if (MERGE) {
+                    cand = get4(fv, it) >= thr;
+                } else {
+                    float f = 0.0f;
+                    cand = screen(base_E + S, t0f, t0_ok, tb, f) || f >= thr;
+                }
             }
             const unsigned cm = __ballot_sync(full, cand);
             if (cm == 0) continue;
@@ -592,28 +621,34 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
         }
     }
     evaluate_pending();
-    for (int off = 16; off > 0; off >>= 1) {
-        const uint64_t o = __shfl_xor_sync(full, best_obj, off);
-        const int kk = __shfl_xor_sync(full, best_k, off);
-        if (better(o, kk, best_obj, best_k)) {
-            best_obj = o;
-            best_k = kk;
+    // the best (objective, K) of a warp, then of the block (round 1: every warp combines the
+    // 32 warp results itself); a reduction runs only where more than one lane holds a result
+    // (candidates are few and sit in one or two warps)
+#pragma unroll 1
+    for (int round = 0; round < 2; ++round) {
+        if (round == 1) {
+            if (lane == 0) {
+                red_obj[warp] = best_obj;
+                red_k[warp] = best_k;
+            }
+            __syncthreads();
+            best_obj = red_obj[lane];
+            best_k = red_k[lane];
         }
-    }
-    if (lane == 0) {
-        red_obj[warp] = best_obj;
-        red_k[warp] = best_k;
-    }
-    __syncthreads();
-    // every warp reduces the 32 warp results itself
-    best_obj = red_obj[lane];
-    best_k = red_k[lane];
-    for (int off = 16; off > 0; off >>= 1) {
-        const uint64_t o = __shfl_xor_sync(full, best_obj, off);
-        const int kk = __shfl_xor_sync(full, best_k, off);
-        if (better(o, kk, best_obj, best_k)) {
-            best_obj = o;
-            best_k = kk;
+        const unsigned vm = __ballot_sync(full, best_k >= 0);
+        if (__popc(vm) > 1) {
+            for (int off = 16; off > 0; off >>= 1) {
+                const uint64_t o = __shfl_xor_sync(full, best_obj, off);
+                const int kk = __shfl_xor_sync(full, best_k, off);
+                if (better(o, kk, best_obj, best_k)) {
+                    best_obj = o;
+                    best_k = kk;
+                }
+            }
+        } else if (vm != 0) {
+            const int src = __ffs(vm) - 1;
+            best_obj = __shfl_sync(full, best_obj, src);
+            best_k = __shfl_sync(full, best_k, src);
         }
     }
     const bool none = best_k < 0;   // no K with a positive, finite step time
