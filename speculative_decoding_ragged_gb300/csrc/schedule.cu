@@ -299,6 +299,34 @@ __device__ __forceinline__ void pack_after_schedule(WinFn win, int B, int gamma,
     }
 }
 
+// Before the dependency wait, pull this call's inputs into L2: a prefetch returns no data, so
+// it is correct even while the previous kernel is still writing them, and once that kernel has
+// finished the loads below find them in L2 instead of DRAM. The inputs' 128-byte lines, laid
+// end to end, are dealt round-robin to the threads; every address lies inside its buffer.
+__device__ __forceinline__ void prefetch_inputs(int t, int nthreads, const float* conf, int B,
+                                                int L, const double* alpha,
+                                                const double* theta, const int32_t* tokens,
+                                                const int32_t* tiers, int n_tiers)
+{
+    const char* base[5] = {reinterpret_cast<const char*>(conf),
+                           reinterpret_cast<const char*>(theta + B),
+                           reinterpret_cast<const char*>(alpha + B),
+                           reinterpret_cast<const char*>(tokens),
+                           reinterpret_cast<const char*>(tiers)};
+    const int bytes[5] = {4 * B * L, 8 * (B * L + 1), 8, tokens != nullptr ? 4 * B * (L + 1) : 0,
+                          tiers != nullptr ? 4 * n_tiers : 0};
+    int first = 0;       // global index of the buffer's first line
+#pragma unroll 1
+    for (int k = 0; k < 5; ++k) {
+        const int lines = (bytes[k] + 127) / 128;
+        int l = (t - first) % nthreads;   // this thread's first line of the buffer
+        if (l < 0) l += nthreads;
+        for (; l < lines; l += nthreads)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(base[k] + 128 * static_cast<int64_t>(l)));
+        first += lines;
+    }
+}
+
 // PACK: the same CTA then front-packs the windows it computed (dspark_schedule_pack).
 template <bool MERGE, bool PACK>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -328,6 +356,8 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
     __shared__ int warp_int[kWarps];
     __shared__ int tier_s;
 
+    prefetch_inputs(threadIdx.x, kThreads, conf, B, L, alpha, theta, PACK ? pk.tokens : nullptr,
+                    PACK ? pk.tiers : nullptr, PACK ? pk.n_tiers : 0);
     pdl_wait_and_trigger();
     const unsigned full = 0xffffffffu;
     const int tid = threadIdx.x;
@@ -723,17 +753,13 @@ schedule_small_kernel(const float* __restrict__ conf, int B, int L, double bias,
                       int32_t* __restrict__ status, PackArgs pk)
 {
     __shared__ int cu_s[kSmallMax];
+    prefetch_inputs(threadIdx.x, 32, conf, B, L, alpha, theta, PACK ? pk.tokens : nullptr,
+                    PACK ? pk.tiers : nullptr, PACK ? pk.n_tiers : 0);
     pdl_wait_and_trigger();
     const unsigned full = 0xffffffffu;
     const int lane = threadIdx.x;
     const int n = B * L;
     const int gamma = L + 1;
-    if (PACK) {
-        const char* tp = reinterpret_cast<const char*>(pk.tokens);
-        const int tb = B * gamma * 4;
-        for (int off = lane * 128; off < tb; off += 32 * 128)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(tp + off));
-    }
     // inputs: this lane's confidences (its request's first j_own + 1), theta of K = lane + 1
     const uint64_t* theta_bits = reinterpret_cast<const uint64_t*>(theta);
     const bool mine = lane < n;
