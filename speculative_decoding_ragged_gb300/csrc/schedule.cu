@@ -303,28 +303,30 @@ __device__ __forceinline__ void pack_after_schedule(WinFn win, int B, int gamma,
 // it is correct even while the previous kernel is still writing them, and once that kernel has
 // finished the loads below find them in L2 instead of DRAM. The inputs' 128-byte lines, laid
 // end to end, are dealt round-robin to the threads; every address lies inside its buffer.
+__device__ __forceinline__ void prefetch_lines(const void* p, int bytes, int& first, int t,
+                                               int nthreads)
+{
+    const int lines = (bytes + 127) / 128;
+    int l = (t - first) % nthreads;       // this thread's first line of the buffer
+    if (l < 0) l += nthreads;
+#pragma unroll 1
+    for (; l < lines; l += nthreads)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const char*>(p) +
+                                                         128 * static_cast<int64_t>(l)));
+    first += lines;
+}
+
 __device__ __forceinline__ void prefetch_inputs(int t, int nthreads, const float* conf, int B,
                                                 int L, const double* alpha,
                                                 const double* theta, const int32_t* tokens,
                                                 const int32_t* tiers, int n_tiers)
 {
-    const char* base[5] = {reinterpret_cast<const char*>(conf),
-                           reinterpret_cast<const char*>(theta + B),
-                           reinterpret_cast<const char*>(alpha + B),
-                           reinterpret_cast<const char*>(tokens),
-                           reinterpret_cast<const char*>(tiers)};
-    const int bytes[5] = {4 * B * L, 8 * (B * L + 1), 8, tokens != nullptr ? 4 * B * (L + 1) : 0,
-                          tiers != nullptr ? 4 * n_tiers : 0};
-    int first = 0;       // global index of the buffer's first line
-#pragma unroll 1
-    for (int k = 0; k < 5; ++k) {
-        const int lines = (bytes[k] + 127) / 128;
-        int l = (t - first) % nthreads;   // this thread's first line of the buffer
-        if (l < 0) l += nthreads;
-        for (; l < lines; l += nthreads)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(base[k] + 128 * static_cast<int64_t>(l)));
-        first += lines;
-    }
+    int first = 0;
+    prefetch_lines(conf, 4 * B * L, first, t, nthreads);
+    prefetch_lines(theta + B, 8 * (B * L + 1), first, t, nthreads);
+    prefetch_lines(alpha + B, 8, first, t, nthreads);
+    if (tokens != nullptr) prefetch_lines(tokens, 4 * B * (L + 1), first, t, nthreads);
+    if (tiers != nullptr) prefetch_lines(tiers, 4 * n_tiers, first, t, nthreads);
 }
 
 // PACK: the same CTA then front-packs the windows it computed (dspark_schedule_pack).
@@ -589,37 +591,44 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
     for (int off = 16; off > 0; off >>= 1) f_best = fmaxf(f_best, __shfl_xor_sync(full, f_best, off));
     const float thr = f_best * kScreen;
 
-    // 4b. exact objectives of the candidates (near the screen's best, or not screenable). The
-    // candidates of a warp are handed to its free lanes first, so that the warp runs its
-    // FP64 divisions in as few passes as possible (one while it has at most 32 candidates).
+    // 4b. exact objectives of the candidates (near the screen's best, or not screenable). MERGE:
+    // each warp queues its candidates in 32 slots of the bucket tables (free after the sort), in
+    // ballot order, and evaluates a full queue 32 at a time, so that a warp with at most 32
+    // candidates runs its FP64 divisions in one pass. The larger kernel evaluates in place.
     uint64_t best_obj = 0;        // bit pattern of a positive double; 0 = none
     int best_k = -1;
-    uint64_t pend_E = 0, pend_t = 0;
-    int pend_k = -1;              // this lane's pending candidate
-    if (tid == 0 && f_k0 >= thr) {
-        pend_E = base_E;
-        pend_t = th0;
-        pend_k = 0;
-    }
-    auto evaluate_pending = [&]() {
-        if (pend_k >= 0) {
-            const uint64_t obj = exact_objective(pend_E, t0, pend_t);
-            if (obj != 0 && better(obj, pend_k, best_obj, best_k)) {
-                best_obj = obj;
-                best_k = pend_k;
-            }
-            pend_k = -1;
+    auto consider = [&](uint64_t E, uint64_t tb, int k) {
+        const uint64_t obj = exact_objective(E, t0, tb);
+        if (obj != 0 && better(obj, k, best_obj, best_k)) {
+            best_obj = obj;
+            best_k = k;
         }
     };
+    uint64_t* slot_e = reinterpret_cast<uint64_t*>(bucket_start) + 64 * warp;   // MERGE only
+    uint64_t* slot_t = slot_e + 32;
+    int* slot_k = bucket_cnt + 32 * warp;
+    int queued = 0;               // uniform across the warp
+    if (warp == 0 && __any_sync(full, tid == 0 && f_k0 >= thr)) {
+        if (!MERGE) {
+            if (tid == 0) consider(base_E, th0, 0);
+        } else {
+            if (lane == 0) {
+                slot_e[0] = base_E;
+                slot_t[0] = th0;
+                slot_k[0] = 0;
+            }
+            queued = 1;
+        }
+    }
     {
         uint64_t S = S_excl;
 #pragma unroll 1
-        for (int it = 0; it < kMaxItems; ++it) {
-            if (it >= items) break;                   // uniform across the block
+        for (int it = 0; it <= kMaxItems; ++it) {
+            const bool done = it >= items || it == kMaxItems;   // uniform across the block
             const int p = p0 + it;
             bool cand = false;
             uint64_t tb = 0;
-            if (p < n) {
+            if (!done && p < n) {
                 S += key_at(p);
                 tb = theta_at(it, p);
                 if (MERGE) {
@@ -629,28 +638,28 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
                     cand = screen(base_E + S, t0f, t0_ok, tb, f) || f >= thr;
                 }
             }
+            if (!MERGE) {
+                if (cand) consider(base_E + S, tb, p + 1);
+                if (done) break;
+                continue;
+            }
             const unsigned cm = __ballot_sync(full, cand);
-            if (cm == 0) continue;
-            unsigned fm = __ballot_sync(full, pend_k < 0);
-            if (__popc(cm) > __popc(fm)) {
-                evaluate_pending();
-                fm = full;
+            if (queued > 0 && (done || queued + __popc(cm) > 32)) {   // one drain site
+                __syncwarp();
+                if (lane < queued) consider(slot_e[lane], slot_t[lane], slot_k[lane]);
+                __syncwarp();
+                queued = 0;
             }
-            // the k-th candidate (in lane order) goes to the k-th free lane
-            const int fr = __popc(fm & lanemask_lt());
-            const bool take = pend_k < 0 && fr < __popc(cm);
-            const int src = take ? static_cast<int>(__fns(cm, 0, fr + 1)) : lane;
-            const uint64_t e = __shfl_sync(full, base_E + S, src);
-            const uint64_t t = __shfl_sync(full, tb, src);
-            const int k = __shfl_sync(full, p + 1, src);
-            if (take) {
-                pend_E = e;
-                pend_t = t;
-                pend_k = k;
+            if (done) break;
+            if (cand) {
+                const int r = queued + __popc(cm & lanemask_lt());
+                slot_e[r] = base_E + S;
+                slot_t[r] = tb;
+                slot_k[r] = p + 1;
             }
+            queued += __popc(cm);
         }
     }
-    evaluate_pending();
     // the best (objective, K) of a warp, then of the block (round 1: every warp combines the
     // 32 warp results itself); a reduction runs only where more than one lane holds a result
     // (candidates are few and sit in one or two warps)

@@ -321,8 +321,8 @@ verify_finalize_kernel(FinalArgs A)
     }
     __syncthreads();
 
-    // 2. accept tests, one thread per tested position
-    if (tid < nrows) {
+    // 2. accept tests, one thread per tested position (greedy: warp 0 does 2 and 3 alone)
+    if (STOCH && tid < nrows) {
         const int i = tid;
         int accepted = 0;
         const bool tested = i < ndec;
@@ -364,12 +364,25 @@ verify_finalize_kernel(FinalArgs A)
         }
         acc_s[i] = tested ? accepted : 0;
     }
-    __syncthreads();
+    if (STOCH) __syncthreads();
 
     // 3. walks (warp 0): the window's accept length (identical in compact and cap-accept) and
     //    the full block's; positions past the tested ones count as rejections
     if (warp == 0) {
-        const bool acc = lane < ndec && acc_s[lane] != 0;
+        bool acc;
+        if (!STOCH) {
+            // greedy accept test of lane i < ndec: the draft equals the row's argmax
+            const bool tested = lane < ndec;
+            const bool valid = d_mine >= 0 && d_mine < A.V;
+            if (tested && !valid) bits |= DSPARK_STATUS_BAD_TOKEN;
+            acc = tested && valid && d_mine == g_s[lane];
+            if (A.row_prob && lane < nrows) {
+                A.row_prob[(base + lane) * 2] = -1.0f;
+                A.row_prob[(base + lane) * 2 + 1] = -1.0f;
+            }
+        } else {
+            acc = lane < ndec && acc_s[lane] != 0;
+        }
         const unsigned rej = __ballot_sync(0xffffffffu, !acc);   // ndec <= 31: never zero
         const int lead = __ffs(rej) - 1;                          // leading accepted drafts
         const int Lc = 1 + min(lead, w - 1);
@@ -390,9 +403,9 @@ verify_finalize_kernel(FinalArgs A)
             if (lane == 0) bits |= sb;
         }
     }
-    __syncthreads();
-    const int Lc = walk_s[0];
     if (STOCH) {
+        __syncthreads();
+        const int Lc = walk_s[0];
         for (int k = tid; k < gamma; k += kFinalThreads)
             out[k] = (k < Lc - 1) ? A.tokens[static_cast<int64_t>(b) * gamma + k + 1] : -1;
         // 4. the bonus draw: the residual of the rejecting position, or p of the last verified
