@@ -564,12 +564,14 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
     // exact pass (+inf where the screen cannot judge, so that K is always evaluated exactly)
     float fb = -INFINITY;
     float fv[kMergeItems] = {0.0f, 0.0f, 0.0f, 0.0f};
-    float f_k0 = 0.0f;
+    float f_k0 = -INFINITY;
+    float f_hi = -INFINITY;      // the largest of this thread's screen values (+inf included)
     if (tid == 0) {
         float f = 0.0f;
         const bool no = screen(base_E, t0f, t0_ok, th0, f);
         if (!no) fb = f;
         f_k0 = no ? INFINITY : f;
+        f_hi = f_k0;              // a queued K = 0 makes warp 0 walk (and drain) as well
     }
     {
         uint64_t S = S_excl;
@@ -581,6 +583,7 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
             float f = 0.0f;
             const bool no = screen(base_E + S, t0f, t0_ok, theta_at(it, p), f);
             if (!no) fb = fmaxf(fb, f);
+            f_hi = fmaxf(f_hi, no ? INFINITY : f);
             if (MERGE) set4(fv, it, no ? INFINITY : f);
         }
     }
@@ -620,11 +623,13 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
             queued = 1;
         }
     }
-    {
+    // only warps with a candidate walk their items: at 32 warps the others' uniform work
+    // would take issue slots from the ones that divide
+    if (__any_sync(full, f_hi >= thr)) {
         uint64_t S = S_excl;
 #pragma unroll 1
         for (int it = 0; it <= kMaxItems; ++it) {
-            const bool done = it >= items || it == kMaxItems;   // uniform across the block
+            const bool done = it >= items || it == kMaxItems;   // uniform across the warp
             const int p = p0 + it;
             bool cand = false;
             uint64_t tb = 0;

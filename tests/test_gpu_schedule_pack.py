@@ -2,6 +2,7 @@
 status bits, cu_seqlens, tiers and packed rows, from tiny to the maximum sizes."""
 import numpy as np
 import pytest
+import torch
 
 from speculative_decoding_ragged_gb300 import synth
 import oracle
@@ -81,6 +82,38 @@ def test_schedule_invalid_cost_and_empty(dev):
     assert g["k_star"] == 0
     g = gpu_schedule(dev, np.zeros((6, 0), np.float32), 1.0, np.zeros(7), np.full(7, -1.0))
     assert g["status"] == 0x10 and (g["windows"] == 1).all()
+
+
+@pytest.mark.parametrize("B,gamma", [(64, 8), (256, 8), (600, 6), (2048, 9)])
+def test_schedule_k_star_at_and_near_zero(dev, B, gamma):
+    """Steep cost tables put the argmax at K = 0 or among the first few K, where the block
+    kernel's exact pass holds K = 0 in its first slot (with or without other candidates)."""
+    from speculative_decoding_ragged_gb300.step import DSparkStep
+    rng = np.random.default_rng(7 * B + gamma)
+    M = np.arange(B * gamma + 1, dtype=np.float64)
+    seen = set()
+    for trial in range(10):
+        conf = rng.uniform(0.05, 0.99, size=(B, gamma - 1)).astype(np.float32)
+        alpha = np.zeros(B + 1)
+        bias = float(rng.uniform(0.001, 0.1))
+        if trial == 0:
+            theta = np.where(M <= B, 0.0, 1e6)              # any candidate is ruinous: K* = 0
+        else:
+            # the first candidate's gain against its cost near break-even
+            step = float(np.exp(rng.uniform(np.log(0.5), np.log(2.0)))) * (bias + 1.0) / B
+            theta = np.where(M <= B, M / B, 1.0 + (M - B) * step)
+        g = gpu_schedule(dev, conf, bias, alpha, theta)
+        r = oracle.schedule(conf, bias, alpha, theta)
+        np.testing.assert_array_equal(g["windows"], r["windows"])
+        assert g["k_star"] == r["k_star"] and g["status"] == r["status"] == 0
+        st = DSparkStep(B, gamma, 64, [B * gamma], bias, alpha, theta, device=dev)
+        st.schedule_pack(torch.as_tensor(conf, device=dev),
+                         torch.zeros((B, gamma), dtype=torch.int32, device=dev))
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(st.windows.cpu().numpy(), r["windows"])
+        assert int(st.k_star.item()) == r["k_star"]
+        seen.add(min(r["k_star"], 10))
+    assert 0 in seen and len(seen - {0}) > 0, seen
 
 
 @pytest.mark.parametrize("B,gamma", [(0, 4), (1, 1), (2, 6), (33, 8), (1025, 4), (8192, 8),
