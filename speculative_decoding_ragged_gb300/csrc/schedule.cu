@@ -543,9 +543,10 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
     // 3. inclusive scan of keys over each thread's contiguous positions
     uint64_t run = 0;
 #pragma unroll 1
-    for (int it = 0; it < kMaxItems; ++it) {
+    for (int it = 0; it < items; ++it) {
         const int p = p0 + it;
-        if (it < items && p < n) run += key_at(p);
+        if (p >= n) break;
+        run += key_at(p);
     }
     uint64_t incl = run;
     for (int off = 1; off < 32; off <<= 1) {
