@@ -666,12 +666,12 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
             queued += __popc(cm);
         }
     }
-    // the best (objective, K) of a warp, then of the block (round 1: every warp combines the
-    // 32 warp results itself); a reduction runs only where more than one lane holds a result
+    // the best (objective, K) of a warp, then of the block (the second pass: every warp combines
+    // the 32 warp results itself); a reduction runs only where more than one lane holds a result
     // (candidates are few and sit in one or two warps)
 #pragma unroll 1
-    for (int round = 0; round < 2; ++round) {
-        if (round == 1) {
+    for (int pass = 0; pass < 2; ++pass) {
+        if (pass == 1) {
             if (lane == 0) {
                 red_obj[warp] = best_obj;
                 red_k[warp] = best_k;
