@@ -23,9 +23,9 @@ constexpr int kStreamWarps = kStreamThreads / 32;
 constexpr int kUnroll = DSPARK_UNROLL;  // 16-byte loads in flight per lane
 constexpr int kTargetUnits = 4096;    // aim: about one unit per resident warp
 #ifndef DSPARK_MAX_CHUNK
-#define DSPARK_MAX_CHUNK 4096
+#define DSPARK_MAX_CHUNK 12288
 #endif
-constexpr int kMaxChunk = DSPARK_MAX_CHUNK;   // elements per chunk, upper bound
+constexpr int kMaxChunk = DSPARK_MAX_CHUNK;   // elements per chunk, upper bound (24 KB of bf16)
 #ifndef DSPARK_MIN_CHUNK
 #define DSPARK_MIN_CHUNK 256
 #endif

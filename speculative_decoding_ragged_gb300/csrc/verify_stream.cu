@@ -100,16 +100,18 @@ verify_stream_kernel(StreamArgs A)
 // stage on its "empty" barrier and writes the unit's partial. Every wait is bounded (about a
 // second of SM clock); a wait that gives up sets DSPARK_STATUS_STALL and the producer still
 // waits, bounded, for every copy it started before the CTA exits.
-// Measured on GB300 (dspark_verify_scatter alone, L2 flushed): 4 consumer warps and a 48 KB
-// ring (four CTAs per SM, up to 16 chunks of 8 KB in flight per SM) beat 8 consumers with
-// 64-128 KB rings; one CTA per SM reached only 4 TB/s.
+// Measured on GB300 (whole steps of the large-vocab and high-load workloads): 4 consumer warps,
+// chunks of up to 12288 elements and a 96 KB ring (four stages of up to 24 KB, two CTAs per SM,
+// eight chunks in flight per SM) beat chunks of 2048-8192 elements in 32-80 KB rings (three or
+// four CTAs per SM), chunks of 14336-16384 elements, and 2 or 8 consumers; one CTA per SM
+// reached only 4 TB/s.
 #ifndef DSPARK_BULK_CONSUMERS
 #define DSPARK_BULK_CONSUMERS 4
 #endif
 constexpr int kBulkConsumers = DSPARK_BULK_CONSUMERS;
 constexpr int kBulkThreads = (kBulkConsumers + 1) * 32;
 #ifndef DSPARK_BULK_RING_BYTES
-#define DSPARK_BULK_RING_BYTES (48 * 1024)
+#define DSPARK_BULK_RING_BYTES (96 * 1024)
 #endif
 constexpr int kBulkRingBytes = DSPARK_BULK_RING_BYTES;   // stage ring per CTA
 // The bulk kernel serves launches whose full size (B*gamma rows of V logits) reaches this;
