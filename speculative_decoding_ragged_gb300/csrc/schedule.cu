@@ -194,8 +194,10 @@ __device__ __forceinline__ T warps_before(const T* total, int warp, int lane)
 // the tier is reduced in the same barrier as the scan of the windows. Then each warp writes
 // the rows of its own requests: the requests' rows form one contiguous range, which the warp
 // fills coalesced from a warp-private stretch of the row-owner map (request << 5 | position),
-// after a warp-level sync only. win(b) gives request b's window; owner holds M ints and may
-// overlay what win reads (every window is read before the block barrier).
+// after a warp-level sync only; warps past the last request only meet the barrier and write
+// padding. win(b) gives request b's window; owner holds M ints and may overlay what win reads
+// (every window is read before the block barrier), and win_s (B ints outside the owner map)
+// keeps each thread's windows for the pass after it.
 template <typename WinFn>
 __device__ __forceinline__ void pack_after_schedule(WinFn win, int B, int gamma, int K_star,
                                                     PackArgs pk, int tier_pre,
