@@ -46,7 +46,23 @@ def draw_case(rng):
 @pytest.mark.parametrize("case", range(N_CASES))
 def test_fused_step_matches_the_oracle(dev, case):
     rng = np.random.default_rng(9000 + case)
-    B, gamma, V, dtype, stochastic, mode, T, tiers, out_cap = draw_case(rng)
+    _check_fused_step(dev, case, rng, *draw_case(rng))
+
+
+@pytest.mark.parametrize("B,gamma,stochastic", [(1024, 5, False), (2049, 3, True),
+                                                (4096, 4, False), (8192, 2, True),
+                                                (4000, 5, False)])
+def test_fused_step_large_batches(dev, B, gamma, stochastic):
+    """Batches up to the limit (more requests than threads in the scheduler and the pack, the
+    bitonic scheduler past 4096 candidates), with a small vocabulary so that the oracle stays
+    quick."""
+    rng = np.random.default_rng(B + gamma)
+    tiers = sorted(set(int(t) for t in rng.integers(B, B * gamma + 1, size=6)))
+    _check_fused_step(dev, B, rng, B, gamma, 512, "bf16", stochastic, "compact", 1.0, tiers,
+                      2 * gamma)
+
+
+def _check_fused_step(dev, case, rng, B, gamma, V, dtype, stochastic, mode, T, tiers, out_cap):
     wl = synth.WORKLOADS["stochastic"].with_(B=B, gamma=gamma, V=V, dtype=dtype, temperature=T,
                                              tiers=tuple(tiers),
                                              theta_slope=float(rng.uniform(0.001, 0.05)))
