@@ -3,20 +3,27 @@
 
 One step = the whole hot path on one batch: schedule, pack, verify (compact, greedy) and the
 compact scatter, issued as the two fused calls dspark_schedule_pack and dspark_verify_scatter,
-on the large-vocab mixed-traffic workload (B=256
-requests, block gamma=8, V=151936 bf16 logits, three acceptance classes a = 0.9/0.65/0.35,
-theta(M) = 0.004 M, alpha(bs) = 0.01 bs, bias 2, tiers every 32 up to 2048). The packed
-target logits of the scheduled windows are produced off the clock (they stand in for the
-target model's forward) and stay resident; three seeded batches rotate so every step reads
-more than L2 holds.
+on the large-vocab mixed-traffic workload (B=256 requests, block gamma=8, V=151936 bf16
+logits, three acceptance classes a = 0.9/0.65/0.35, theta(M) = 0.004 M, alpha(bs) = 0.01 bs,
+bias 2, tiers every 32 up to 2048). The packed target logits of the scheduled windows are
+produced off the clock (they stand in for the target model's forward) and stay resident; three
+seeded batches rotate so every step reads more than L2 holds.
 
-Prints one JSON line. `value` is packed verify rows per second over the whole step with
-inputs resident in HBM; `e2e` repeats the measurement with the step's inputs copied from
-pinned host memory and the results read back inside the timed region; `roofline` reports the
-streaming kernel's algorithmic bytes (M * V * 2 per launch) over its CUDA-event time against
-the measured HBM copy bandwidth (and the whole verify call beside it); `latency_b1` times the
-batch-1 decode step; `verify_legs` the verify call on the other workloads; `cpu_baseline`
-times the CPU oracle on a bounded sample.
+Prints one JSON line.
+  value        packed verify rows per second over whole steps, inputs resident in HBM (events
+               around the K timed steps only, nothing recorded between a step's kernels);
+  e2e          the same rows/s with the step's inputs copied from pinned host memory and the
+               results read back inside the timed region;
+  legs         every workload timed alone: each of >= 30 launches after an L2 flush, events
+               around the whole verify call and (recorded by the library) around its streaming
+               kernel, plus the schedule-and-pack call; rows/s, GB/s and the fraction of the
+               measured and nominal HBM peaks, with p10/p90; the high-load workload at each
+               theta of its sweep in compact and cap-accept mode; the oracle timed per workload;
+  roofline     the large-vocab leg's streaming kernel: algorithmic bytes (M * V * 2 per launch)
+               over its mean event time, against the measured HBM copy bandwidth;
+  latency_b1   per-step time of the batch-1 workload over consecutive steps;
+  cpu_baseline the CPU oracle on a bounded sample of the headline workload;
+  clocks       nvidia-smi samples over the whole measured region (headline, e2e, legs).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 """
@@ -42,7 +49,7 @@ NOMINAL_HBM_GBS = 8000.0     # the GB300's nominal HBM3e bandwidth, for context 
 UNIT = "rows/s"
 WORKLOAD = "large_vocab_mixed"
 FALLBACK_HBM_GBS = 6800.0
-PROFILE = os.path.join(ROOT, "profiles", "verify_large_vocab_mixed.md")
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "verify_stream_traffic.json")
 N_BATCHES = 3
 
 
@@ -54,18 +61,17 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=100)
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="oracle time on the headline workload")
+    ap.add_argument("--cpu-seconds-leg", type=float, default=3.0,
+                    help="oracle time on each other workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batches", type=int, default=N_BATCHES)
     ap.add_argument("--latency-steps", type=int, default=10000)
     ap.add_argument("--stream-kernel", default="auto", choices=["auto", "register", "bulk"],
                     help="which logit-streaming kernel verify uses (results are identical)")
-    ap.add_argument("--config-reps", type=int, default=30,
-                    help="timed verify calls per extra workload leg (0: skip the legs)")
-    ap.add_argument("--event-every", type=int, default=100,
-                    help="record the per-kernel events on every n-th timed step only: an event "
-                         "between two kernels stops the second from launching early, so a "
-                         "sampled step runs about 10-15 us slower")
+    ap.add_argument("--config-reps", type=int, default=40,
+                    help="timed launches per workload leg (0: skip the legs)")
     return ap.parse_args()
 
 
@@ -117,36 +123,26 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def profile_traffic():
-    """DRAM bytes over algorithmic bytes of the captured verify-stream launch recorded in
-    profiles/, if the source files the record names still hash to the value recorded with it."""
+def traffic_ratio():
+    """DRAM bytes over algorithmic bytes of the captured full-size streaming launch (the JSON
+    record under profiles/), while the source files it names still hash to the value recorded
+    with it; None once the kernel has changed since the counters were taken."""
     try:
-        with open(PROFILE) as f:
-            text = f.read()
-    except OSError:
-        return None
-    rec = {}
-    for line in text.splitlines():
-        if ":" in line and line.strip().startswith("- "):
-            k, v = line.strip()[2:].split(":", 1)
-            rec[k.strip()] = v.strip().strip("`")
-    h = hashlib.sha256()
-    try:
-        for name in rec.get("sources", "").split():
+        with open(TRAFFIC_RECORD) as f:
+            rec = json.load(f)
+        h = hashlib.sha256()
+        for name in rec["sources"]:
             with open(os.path.join(ROOT, "speculative_decoding_ragged_gb300", "csrc", name), "rb") as f:
                 h.update(f.read())
-    except OSError:
-        return None
-    if not rec.get("sources") or rec.get("sources_sha256_16") != h.hexdigest()[:16]:
-        return None
-    try:
+        if h.hexdigest()[:16] != rec["sources_sha256_16"]:
+            return None
         return float(rec["traffic_over_algorithmic"])
-    except (KeyError, ValueError):
+    except (OSError, KeyError, ValueError, TypeError):
         return None
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    """nvidia-smi samples of SM clock and throttle reasons while the GPU is measured."""
     FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -169,7 +165,8 @@ class ClockSampler:
 
     def stop(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
         self.proc.terminate()
         try:
             out, _ = self.proc.communicate(timeout=5)
@@ -180,7 +177,7 @@ class ClockSampler:
         if self.uuid:
             mine = [r for r in rows if len(r) > 1 and self.uuid.replace("GPU-", "") in r[1]]
             rows = mine or rows
-        sm, mx, reasons = [], [], set()
+        sm, mx, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
             if len(r) < 10:
@@ -188,6 +185,7 @@ class ClockSampler:
             try:
                 sm.append(float(r[2]))
                 mx.append(float(r[3]))
+                pw.append(float(r[4]))
             except ValueError:
                 continue
             for name, val in zip(names, r[6:10]):
@@ -195,7 +193,18 @@ class ClockSampler:
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "sm_mhz_min": min(sm) if sm else None,
+                "power_w_max": max(pw) if pw else None,
+                "region": "headline steps, e2e steps, workload legs and the batch-1 leg"}
+
+
+def percentile(xs, q):
+    return float(np.percentile(np.asarray(xs, dtype=np.float64), q))
+
+
+def spread(xs):
+    return {"median": statistics.median(xs), "mean": statistics.mean(xs),
+            "p10": percentile(xs, 10), "p90": percentile(xs, 90), "n": len(xs)}
 
 
 def make_inputs(wl, seeds, dev, st):
@@ -211,17 +220,208 @@ def make_inputs(wl, seeds, dev, st):
         w = st.windows.cpu().numpy()
         M = int(w.sum())
         tier = min([t for t in wl.tiers if t >= M] or [M])
-        packed = synth.gather_packed(bt.target, bt.B, bt.gamma, w, rows_cap=tier)
+        target = bt.target.to(dev)
+        packed = synth.gather_packed(target, bt.B, bt.gamma, w, rows_cap=tier)
+        del target
         batches.append(dict(
             bt=bt, windows=w, M=M, conf=conf,
-            tokens=torch.as_tensor(bt.tokens, device=dev),
-            packed=packed.to(dev),
+            tokens=torch.as_tensor(bt.tokens, device=dev), packed=packed,
             conf_h=torch.as_tensor(bt.conf).pin_memory(),
             tokens_h=torch.as_tensor(bt.tokens).pin_memory(),
-            packed_h=packed.pin_memory()))
-        bt.target = None          # the full block is not needed any more
+            packed_h=packed.cpu().pin_memory()))
     st.status.zero_()
     return batches
+
+
+class LegTimer:
+    """Times calls one at a time: before each, `pre` (history reset) and an L2 flush (a 256 MB
+    read, long enough that the host has queued the call before the GPU reaches it); events
+    around the call, or (recorded by the library) around its logit-streaming kernel alone (an
+    event between two kernels costs the second its early launch, so the two are timed in
+    separate passes)."""
+
+    def __init__(self, dev):
+        from speculative_decoding_ragged_gb300 import _binding as bd
+        self.bd = bd
+        self.flush = torch.ones(64 << 20, dtype=torch.int32, device=dev)
+        self.stream = torch.cuda.current_stream()
+
+    def run(self, call, reps, pre=None, stream_events=True):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(reps)]
+        for e in ev:                      # torch creates events lazily: make them exist
+            for x in e:
+                x.record(self.stream)
+        torch.cuda.synchronize()
+        for e in ev:
+            if pre is not None:
+                pre()
+            torch.max(self.flush)         # a read: evicts the inputs without dirtying L2
+            e[0].record(self.stream)
+            if stream_events:
+                self.bd.set_stream_events(e[1], e[2])
+            call()
+            if stream_events:
+                self.bd.set_stream_events(None, None)
+            e[3].record(self.stream)
+        torch.cuda.synchronize()
+        call_us = [e[0].elapsed_time(e[3]) * 1e3 for e in ev]
+        stream_us = [e[1].elapsed_time(e[2]) * 1e3 for e in ev] if stream_events else None
+        return call_us, stream_us
+
+
+def leg_record(name, wl, mode, stochastic, M, rows_t, rows_d, bonus_rows, call_us, stream_us,
+               sp_us, step_us, peak, extra=None):
+    """One workload leg: algorithmic bytes (target rows the mode verifies, draft rows of the
+    tested drafts, bonus rows) per call, rows/s over the whole call, GB/s and fractions."""
+    e = 2 if wl.dtype == "bf16" else 4
+    algo = (rows_t + rows_d + bonus_rows) * wl.V * e
+    stream_bytes = (rows_t + rows_d) * wl.V * e
+    call = spread(call_us)
+    rec = {"workload": name, "B": wl.B, "gamma": wl.gamma, "V": wl.V, "dtype": wl.dtype,
+           "verify": "stochastic" if stochastic else "greedy", "mode": mode, "M": M,
+           "rows_streamed": rows_t + rows_d, "bonus_rows": bonus_rows,
+           "algorithmic_bytes": algo,
+           "call_us": call, "rows_per_s": M / (call["median"] * 1e-6),
+           "call_gbs": algo / (call["mean"] * 1e-6) / 1e9,
+           "call_frac": algo / (call["mean"] * 1e-6) / 1e9 / peak,
+           "call_frac_of_nominal_8tbs": algo / (call["mean"] * 1e-6) / 1e9 / NOMINAL_HBM_GBS}
+    if stream_us is not None:
+        s = spread(stream_us)
+        rec.update({"stream_us": s, "stream_bytes": stream_bytes,
+                    "stream_gbs": stream_bytes / (s["mean"] * 1e-6) / 1e9,
+                    "stream_frac": stream_bytes / (s["mean"] * 1e-6) / 1e9 / peak})
+    if sp_us is not None:
+        rec["sched_pack_us"] = spread(sp_us)
+    if step_us is not None:
+        rec["step_us"] = spread(step_us)
+    rec["l2"] = "flushed (256 MB read) before every timed call"
+    if extra:
+        rec.update(extra)
+    return rec
+
+
+def step_for(wl, bt, mode, stochastic, dev, out_cap):
+    from speculative_decoding_ragged_gb300.step import DSparkStep
+    return DSparkStep(wl.B, wl.gamma, wl.V, wl.tiers, bt.bias, bt.alpha, bt.theta, mode=mode,
+                      stochastic=stochastic, out_cap=out_cap, device=dev)
+
+
+def run_leg(timer, name, wl, bt, mode, stochastic, dev, reps, target_full, draft, peak,
+            extra=None, batches=None):
+    """One workload leg: windows from the library's own schedule (off the clock), packed rows
+    gathered on the device, then `reps` timed verify calls, schedule-and-pack calls and whole
+    steps. `batches` (the headline's) rotate instead of one batch when given."""
+    from speculative_decoding_ragged_gb300 import synth
+    B, g = wl.B, wl.gamma
+    st = step_for(wl, bt, mode, stochastic, dev, out_cap=4 * g)
+    kw = dict(temperature=wl.temperature, seed=5, step=0)
+    entries = []
+    for b in (batches or [None]):
+        conf = b["conf"] if b else torch.as_tensor(bt.conf, device=dev)
+        tokens = b["tokens"] if b else torch.as_tensor(bt.tokens, device=dev)
+        st.schedule_pack(conf, tokens)
+        torch.cuda.synchronize()
+        w = st.windows.cpu().numpy()
+        M = int(w.sum())
+        if b is not None:
+            target = b["packed"]
+        elif mode == "compact":
+            target = synth.gather_packed(target_full, B, g, w, rows_cap=int(st.meta[1].item()))
+        else:
+            target = target_full
+        entries.append(dict(conf=conf, tokens=tokens, target=target, M=M, w=w))
+    verify = [st.verify_scatter(e["target"], e["tokens"], draft, prepare=True, **kw)
+              for e in entries]
+    sched = [st.schedule_pack(e["conf"], e["tokens"], prepare=True) for e in entries]
+    steps = [st.prepare(e["conf"], e["tokens"], e["target"], draft, **kw) for e in entries]
+    n = len(entries)
+    reset = st.out_len.zero_
+    for k in range(3):
+        sched[k % n]()
+        verify[k % n]()
+        reset()
+    torch.cuda.synchronize()
+    # verify alone needs the windows and cu_seqlens of its own batch: one batch at a time;
+    # the whole call without events inside it, then the streaming kernel alone
+    call_us, stream_us = [], []
+    for k in range(n):
+        sched[k]()
+        r = (reps + n - 1 - k) // n
+        c, _ = timer.run(verify[k], r, pre=reset, stream_events=False)
+        _, s = timer.run(verify[k], r, pre=reset)
+        call_us += c
+        stream_us += s
+    st.out_len.zero_()
+    sp_us, _ = timer.run(lambda: sched[0](), reps, stream_events=False)
+    it = iter(range(10 ** 9))
+
+    def whole():
+        k = next(it) % n
+        for c in steps[k]:
+            c()
+    step_us, _ = timer.run(whole, reps, pre=reset, stream_events=False)
+    torch.cuda.synchronize()
+    Ms = [e["M"] for e in entries]
+    M = statistics.mean(Ms)
+    rows_t = M if mode == "compact" else B * g
+    rows_d = 0
+    bonus = 0
+    if stochastic:
+        rows_d = (M - B) if mode == "compact" else B * (g - 1)
+        # the bonus pass of the last batch: two rows per request that rejected a draft
+        # (residual of target and draft rows), one per request that accepted its whole window
+        sched[-1]()
+        verify[-1]()
+        torch.cuda.synchronize()
+        acc = st.accept_len.cpu().numpy()
+        bonus = int(np.sum(np.where(acc < entries[-1]["w"], 2, 1)))
+    ex = {"launches_per_call": st.launches_per_step - (1 if g > 1 else 2),
+          "launches_per_step": st.launches_per_step, "reps": len(call_us),
+          "batches_rotating": n, "status": int(st.status.item())}
+    if extra:
+        ex.update(extra)
+    return leg_record(name, wl, mode, stochastic, M, rows_t, rows_d, bonus, call_us, stream_us,
+                      sp_us, step_us, peak, ex)
+
+
+def workload_legs(dev, reps, headline_batches, args):
+    """Every workload of the benchmark, each verify call timed alone (see LegTimer)."""
+    from speculative_decoding_ragged_gb300 import synth
+    peak, _ = measured_peak()
+    timer = LegTimer(dev)
+    legs = {}
+    # large-vocab mixed (the headline workload): its own rotating batches
+    wl = synth.WORKLOADS["large_vocab_mixed"]
+    legs["large_vocab_mixed/compact"] = run_leg(
+        timer, "large_vocab_mixed", wl, headline_batches[0]["bt"], "compact", False, dev, reps,
+        None, None, peak, batches=headline_batches)
+    # tiny greedy, stochastic, batch-1 (greedy and stochastic T = 0.7)
+    for name, modes, samplers in (("tiny_greedy", ("compact",), (False,)),
+                                  ("stochastic", ("compact", "cap_accept"), (True,)),
+                                  ("latency_b1", ("compact",), (False, True))):
+        wl = synth.WORKLOADS[name]
+        for stochastic in samplers:
+            bt = synth.make_batch(wl, seed=77, stochastic=stochastic)
+            target = bt.target.to(dev)
+            draft = bt.draft.to(dev) if stochastic else None
+            for mode in modes:
+                key = f"{name}/{mode}" + ("/stochastic" if name == "latency_b1" and stochastic else "")
+                legs[key] = run_leg(timer, name, wl, bt, mode, stochastic, dev, reps, target,
+                                    draft, peak)
+            del target, draft
+    # high load: the theta sweep, compact and cap-accept, one logits block shared
+    wl = synth.WORKLOADS["high_load"]
+    bt = synth.make_batch(wl, seed=77)
+    target = bt.target.to(dev)
+    for theta in synth.HIGH_LOAD_THETAS:
+        bt.theta = theta * np.arange(wl.B * wl.gamma + 1, dtype=np.float64)
+        for mode in ("compact", "cap_accept"):
+            legs[f"high_load/theta{theta}/{mode}"] = run_leg(
+                timer, "high_load", wl, bt, mode, False, dev, reps, target, None, peak,
+                extra={"theta_slope": theta})
+    del target, timer
+    torch.cuda.empty_cache()
+    return legs
 
 
 def run_native(args, rank, world, local):
@@ -244,60 +444,34 @@ def run_native(args, rank, world, local):
     nb = len(batches)
     calls = [st.prepare(b["conf"], b["tokens"], b["packed"]) for b in batches]
 
-    def step(i, ev=None):
+    def step(i):
         # fused calls: dspark_schedule_pack, then dspark_verify_scatter (whose compact scatter
-        # runs inside the finaliser); on sampled steps the library also records ev[3], ev[4]
-        # around its streaming kernel
-        sched_pack, verify_scatter = calls[i % nb]
-        if ev is not None:
-            ev[0].record(stream)
-        sched_pack()
-        if ev is not None:
-            ev[1].record(stream)
-            bd.set_stream_events(ev[3], ev[4])
-        verify_scatter()
-        if ev is not None:
-            bd.set_stream_events(None, None)
-            ev[2].record(stream)
+        # runs inside the kernel that decides each request's tokens)
+        for c in calls[i % nb]:
+            c()
 
     for i in range(args.warmup):
         step(i)
         st.out_len.zero_()
     torch.cuda.synchronize()
 
-    # device-resident timed region: K steps, events around sched+pack and verify each step
+    # device-resident timed region: K whole steps, events around the loop only
     K = args.steps
-    sampled = [i for i in range(K) if i % max(1, args.event_every) == 0]
-    evs = {i: [torch.cuda.Event(enable_timing=True) for _ in range(5)] for i in sampled}
-    for ev in evs.values():           # torch creates events lazily: make them exist
-        for e in ev:
-            e.record(stream)
-    torch.cuda.synchronize()
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
+    clocks.start()
     barrier(world)
     torch.cuda.synchronize()
-    clocks.start()
     t_start.record(stream)
     for i in range(K):
-        step(i, evs.get(i))
+        step(i)
     t_end.record(stream)
     torch.cuda.synchronize()
-    clk = clocks.stop()
     barrier(world)
     ms = t_start.elapsed_time(t_end)
     ms = max_over_ranks(ms, world)
     rows = sum(batches[i % nb]["M"] for i in range(K))
     rows = sum_over_ranks(rows, world)
-    sched_us = [evs[i][0].elapsed_time(evs[i][1]) * 1e3 for i in sampled]
-    verify_us = [evs[i][1].elapsed_time(evs[i][2]) * 1e3 for i in sampled]
-    stream_us = [evs[i][3].elapsed_time(evs[i][4]) * 1e3 for i in sampled]
-    verify_bytes = [batches[i % nb]["M"] * wl.V * 2 for i in sampled]
-    ach_gbs = sum(verify_bytes) / (sum(verify_us) * 1e-6) / 1e9          # the whole verify call
-    kern_gbs = sum(verify_bytes) / (sum(stream_us) * 1e-6) / 1e9         # its streaming kernel
-    peak, peak_kind = measured_peak()
-    ratio = profile_traffic()     # DRAM bytes / algorithmic bytes of a captured launch
-    traffic = None if ratio is None else ratio * statistics.mean(verify_bytes)
     value = rows / (ms * 1e-3)
 
     # end to end through the C ABI with host buffers: every step copies its confidences,
@@ -345,17 +519,23 @@ def run_native(args, rank, world, local):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
     e2e_rows = sum_over_ranks(e2e_rows, world)
+    del inbuf
 
+    legs = None
+    if args.config_reps > 0 and rank == 0:
+        legs = workload_legs(dev, max(args.config_reps, 1), batches, args)
     latency = latency_leg(dev, args.latency_steps) if args.latency_steps > 0 else None
-    legs = config_legs(dev, args.config_reps) if args.config_reps > 0 and rank == 0 else None
+    clk = clocks.stop()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(batches, wl, args.cpu_seconds)
+        if legs is not None:
+            oracle_legs(legs, args.cpu_seconds_leg)
     if rank != 0:
         return None
-    verify_mean_us = statistics.mean(verify_us)
-    return {
+    peak, peak_kind = measured_peak()
+    out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -364,27 +544,9 @@ def run_native(args, rank, world, local):
                    "stream_kernel": args.stream_kernel,
                    "batches_rotating": nb, "rows_per_step_mean": rows / K / world,
                    "l2": "inputs larger than L2: each step reads >=300 MB of packed logits, "
-                         f"{nb} batches rotate",
+                         f"{nb} batches rotate; legs flush L2 before every timed call",
                    "parallelism": f"replicas{world}" if world > 1 else "single GPU"},
-        "logits_gbs": ach_gbs,
-        "sched_pack_us": statistics.median(sched_us),
-        "verify_us": statistics.median(verify_us),
         "step_us": ms / K * 1e3,
-        "events_sampled_steps": len(sampled),
-        "roofline": {"bound": "hbm",
-                     "kernel": f"verify streaming kernel ({stream_kernel_name(wl, args)})",
-                     "achieved": kern_gbs, "peak": peak, "peak_source": peak_kind,
-                     "unit": "GB/s", "frac": kern_gbs / peak, "traffic": traffic,
-                     "frac_of_nominal_8tbs": kern_gbs / NOMINAL_HBM_GBS,
-                     "algorithmic_bytes_per_launch": statistics.mean(verify_bytes),
-                     "launch_us_mean": statistics.mean(stream_us),
-                     "launch_us_p10_p90": [percentile(stream_us, 10), percentile(stream_us, 90)],
-                     "verify_call": {"what": "dspark_verify_scatter: streaming kernel, then "
-                                             "finaliser with the fused scatter",
-                                     "achieved": ach_gbs, "frac": ach_gbs / peak,
-                                     "us_mean": verify_mean_us,
-                                     "us_p10_p90": [percentile(verify_us, 10),
-                                                    percentile(verify_us, 90)]}},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_rows / (e2e_ms * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d // max(E, 1), "d2h_bytes_per_step": d2h // max(E, 1),
@@ -393,16 +555,44 @@ def run_native(args, rank, world, local):
         "gpu_launches": K * st.launches_per_step,
         "clocks": clk,
         "latency_b1": latency,
-        "verify_legs": legs,
+        "legs": legs,
     }
+    if legs is not None:
+        lv = legs["large_vocab_mixed/compact"]
+        ratio = traffic_ratio()
+        per_launch = lv["stream_bytes"]
+        s_mean = lv["stream_us"]["mean"]
+        achieved = per_launch / (s_mean * 1e-6) / 1e9
+        out["sched_pack_us"] = lv["sched_pack_us"]["median"]
+        out["verify_us"] = lv["call_us"]["median"]
+        out["logits_gbs"] = lv["call_gbs"]
+        out["roofline"] = {
+            "bound": "hbm", "kernel": f"verify streaming kernel ({stream_kernel_name(wl, args)})",
+            "achieved": achieved, "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
+            "frac": achieved / peak,
+            "traffic": None if ratio is None else ratio * per_launch,
+            "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
+            "algorithmic_bytes_per_launch": per_launch,
+            "launch_us_mean": s_mean, "launch_us_p10_p90": [lv["stream_us"]["p10"],
+                                                            lv["stream_us"]["p90"]],
+            "samples": lv["stream_us"]["n"],
+            "timing": "CUDA events on the launching stream around each launch, one launch "
+                      "at a time after an L2 flush; the 3 headline batches rotate",
+            "verify_call": {"what": "dspark_verify_scatter, the whole call",
+                            "achieved": lv["call_gbs"], "frac": lv["call_frac"],
+                            "us_mean": lv["call_us"]["mean"],
+                            "us_p10_p90": [lv["call_us"]["p10"], lv["call_us"]["p90"]]}}
+    return out
 
 
 def latency_leg(dev, steps, pool=64):
     """Per-step time of the batch-1 workload (B=1, gamma=16, V=129280 bf16, compact), greedy
     and stochastic (T = 0.7): `steps` consecutive steps cycling through `pool` seeded inputs
-    (the pool's logits exceed L2), launched eagerly (the fused calls: three kernels per greedy
-    step, four per stochastic step), as one CUDA graph replay per step, and as one graph
-    holding a whole pool cycle (the GPU-side step time)."""
+    (the pool's logits exceed L2), launched eagerly (the fused calls through ctypes), as one
+    CUDA graph replay per step (dspark_graph_launch), and as one graph holding a whole pool
+    cycle (the GPU-side step time). Host submission time per step is reported beside each: a
+    mode whose host time is at or above its step time is bound by the submitting thread."""
+    from speculative_decoding_ragged_gb300 import _binding as bd
     from speculative_decoding_ragged_gb300 import synth
     from speculative_decoding_ragged_gb300.step import DSparkGraph, DSparkStep
     wl = synth.WORKLOADS["latency_b1"]
@@ -423,11 +613,16 @@ def latency_leg(dev, steps, pool=64):
         kw = dict(temperature=wl.temperature, seed=7)
         calls = [st.prepare(*e, step=k, **kw) for k, e in enumerate(entries)]
         graphs = [DSparkGraph(st, *e, step_index=k, **kw) for k, e in enumerate(entries)]
-        cycle = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(cycle):
-            for k, e in enumerate(entries):
-                for c in st.prepare(*e, step=k, **kw):
+        # one graph holding a whole pool cycle, captured through the library's C ABI
+        capture = torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(capture):
+            cycle_calls = [st.prepare(*e, step=k, **kw) for k, e in enumerate(entries)]
+            cycle = bd.StepGraph(capture)
+            for cc in cycle_calls:
+                for c in cc:
                     c()
+            cycle.end()
+        cycle_launch = cycle.prepare_launch()
         stream = torch.cuda.current_stream()
         name = "stochastic" if stochastic else "greedy"
         out[f"{name}_launches_per_step"] = st.launches_per_step
@@ -439,21 +634,24 @@ def latency_leg(dev, steps, pool=64):
                 elif mode == "graph":
                     graphs[i % pool].replay()
                 elif i % pool == 0:
-                    cycle.replay()
+                    cycle_launch()
             n = steps - steps % pool
             for i in range(2 * pool):
                 one(i)
             torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0 = time.perf_counter()
             e0.record(stream)
             for i in range(n):
                 one(i)
             e1.record(stream)
+            t1 = time.perf_counter()
             torch.cuda.synchronize()
             out[f"{name}_step_us_{mode}"] = e0.elapsed_time(e1) * 1e3 / n
+            out[f"{name}_host_submit_us_{mode}"] = (t1 - t0) * 1e6 / n
         out["pool_mb"] = round(sum(sum(t.numel() * t.element_size() for t in e[2:] if t is not None)
                                    for e in entries) / 1e6, 1)
-        del graphs, cycle, calls, entries
+        del graphs, cycle, cycle_launch, cycle_calls, calls, entries
     return out
 
 
@@ -468,102 +666,31 @@ def stream_kernel_name(wl, args):
     return "TMA bulk-copy kernel" if full >= (64 << 20) else "register-streaming kernel"
 
 
-def percentile(xs, q):
-    return float(np.percentile(np.asarray(xs, dtype=np.float64), q))
+def _bits(t):
+    t = t.contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
 
 
-# (workload, mode, stochastic): the other workloads' verify launches, timed alone
-CONFIG_LEGS = [("stochastic", "compact", True), ("stochastic", "cap_accept", True),
-               ("high_load", "compact", False), ("high_load", "cap_accept", False)]
-
-
-def config_legs(dev, reps):
-    """Roofline of dspark_verify_scatter (stream + finalize with the fused scatter, + the bonus
-    kernel when stochastic) on the other workloads, each launch timed alone with CUDA events on
-    its stream after an L2 flush (a 256 MB buffer read between launches). Windows come from
-    the library's own schedule. Algorithmic bytes: the target rows the mode verifies (M
-    compact, B*gamma cap-accept), the draft rows of the tested drafts (stochastic: M - B
-    compact, B*(gamma-1) cap-accept) and the bonus pass (two rows per request that rejected,
-    one per request that accepted its whole window), each V*e bytes."""
-    from speculative_decoding_ragged_gb300 import synth
-    from speculative_decoding_ragged_gb300.step import DSparkStep
-    peak, _ = measured_peak()
-    flush = torch.ones(64 << 20, dtype=torch.int32, device=dev)     # 256 MB, read to evict L2
-    stream = torch.cuda.current_stream()
-    out = {}
-    cache = {}
-    for name, mode, stochastic in CONFIG_LEGS:
-        wl = synth.WORKLOADS[name]
-        if name not in cache:
-            cache.clear()
-            cache[name] = synth.make_batch(wl, seed=77, stochastic=stochastic)
-        bt = cache[name]
-        B, g, V = wl.B, wl.gamma, wl.V
-        e = 2 if wl.dtype == "bf16" else 4
-        st = DSparkStep(B, g, V, wl.tiers, bt.bias, bt.alpha, bt.theta, mode=mode,
-                        stochastic=stochastic, out_cap=g * (reps + 8), device=dev)
-        conf = torch.as_tensor(bt.conf, device=dev)
-        tokens = torch.as_tensor(bt.tokens, device=dev)
-        st.schedule_pack(conf, tokens)
-        torch.cuda.synchronize()
-        w = st.windows.cpu().numpy()
-        M = int(w.sum())
-        if mode == "compact":
-            tier = int(st.meta[1].item())
-            target = synth.gather_packed(bt.target, B, g, w, rows_cap=tier).to(dev)
-        else:
-            target = bt.target.to(dev)
-        draft = bt.draft.to(dev) if stochastic else None
-        call = st.verify_scatter(target, tokens, draft, temperature=wl.temperature, seed=5,
-                                 prepare=True)
-        for _ in range(3):
-            call()
-        torch.cuda.synchronize()
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(reps)]
-        for e0, e1 in evs:
-            torch.max(flush)      # a read: evicts the logits from L2 without leaving dirty lines
-            e0.record(stream)
-            call()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        us = [e0.elapsed_time(e1) * 1e3 for e0, e1 in evs]
-        rows_t = M if mode == "compact" else B * g
-        rows_d = 0
-        bonus = 0
-        if stochastic:
-            rows_d = (M - B) if mode == "compact" else B * (g - 1)
-            acc = st.accept_len.cpu().numpy()
-            bonus = int(np.sum(np.where(acc < w, 2, 1)))
-        algo = (rows_t + rows_d + bonus) * V * e
-        med = statistics.median(us)
-        out[f"{name}/{mode}"] = {
-            "B": B, "gamma": g, "V": V, "verify": "stochastic" if stochastic else "greedy",
-            "M": M, "algorithmic_bytes": algo, "us_median": med,
-            "us_p10_p90": [percentile(us, 10), percentile(us, 90)],
-            "gbs": algo / (med * 1e-6) / 1e9, "frac": algo / (med * 1e-6) / 1e9 / peak,
-            "frac_of_nominal_8tbs": algo / (med * 1e-6) / 1e9 / NOMINAL_HBM_GBS,
-            "launches": 3 if stochastic else 2, "reps": reps, "l2": "flushed between launches"}
-        del st, target, draft, call
-    del flush
-    return out
-
-
-def oracle_inputs(bt, n_req, packed_bits=None):
+def oracle_inputs(bt, n_req, mode="compact", stochastic=False):
     """Host inputs of the oracle's step on the first n_req requests as a batch of their own:
-    its confidences, tokens and cost tables, and the packed rows of its own schedule (the
-    stand-in for the target forward, prepared off the clock)."""
+    its confidences, tokens, cost tables, and the target rows its mode verifies (compact: the
+    packed rows of the oracle's own schedule), prepared off the clock as the stand-in for the
+    target forward."""
     import oracle
     from speculative_decoding_ragged_gb300 import synth
     B, g = n_req, bt.gamma
     inp = dict(conf=bt.conf[:B], tokens=bt.tokens[:B], alpha=bt.alpha[:B + 1],
                theta=bt.theta[:B * g + 1], bias=bt.bias, tiers=bt.tiers,
-               cap=int(max(int(bt.tiers.max()), B * g)))
-    if packed_bits is None:
+               cap=int(max(int(bt.tiers.max()), B * g)), mode=mode, stochastic=stochastic,
+               temperature=bt.wl.temperature)
+    if mode == "compact":
         w = oracle.schedule(inp["conf"], bt.bias, inp["alpha"], inp["theta"])["windows"]
-        packed = synth.gather_packed(bt.target, B, g, w)
-        packed_bits = packed.view(torch.int16).numpy().view(np.uint16)
-    inp["packed_bits"] = packed_bits
+        inp["target_bits"] = _bits(synth.gather_packed(bt.target, B, g, w))
+    else:
+        inp["target_bits"] = _bits(bt.target[:B * g])
+    inp["draft_bits"] = _bits(bt.draft[:B * (g - 1)]) if stochastic else None
     return inp
 
 
@@ -573,31 +700,60 @@ def oracle_step(inp):
     s = oracle.schedule(inp["conf"], inp["bias"], inp["alpha"], inp["theta"])
     w = s["windows"]
     p = oracle.pack(w, inp["tokens"], inp["tiers"], inp["cap"])
-    v = oracle.verify(oracle.COMPACT, False, inp["packed_bits"], inp["tokens"], cu=p["cu"],
-                      windows=w)
+    mode = oracle.COMPACT if inp["mode"] == "compact" else oracle.CAP_ACCEPT
+    v = oracle.verify(mode, inp["stochastic"], inp["target_bits"], inp["tokens"], cu=p["cu"],
+                      windows=w, draft=inp["draft_bits"], temperature=inp["temperature"],
+                      seed=5, step=0)
     B = w.shape[0]
     oracle.scatter(v["committed"], v["accept_len"], np.full((B, 64), -1, np.int32),
                    np.zeros(B, np.int32))
     return p["M"]
 
 
-def cpu_baseline(batches, wl, seconds):
-    """The oracle as it stands, single-threaded, on whole steps of the same batches until
-    `seconds` of CPU work have run (at least one step)."""
-    inputs = [oracle_inputs(b["bt"], b["bt"].B,
-                            b["packed_h"].view(torch.int16).numpy().view(np.uint16))
-              for b in batches]
+def time_oracle(inputs, seconds):
     rows, n, t0 = 0, 0, time.perf_counter()
     while True:
         rows += oracle_step(inputs[n % len(inputs)])
         n += 1
         if time.perf_counter() - t0 >= seconds:
             break
-    dt = time.perf_counter() - t0
+    return rows, n, time.perf_counter() - t0
+
+
+def cpu_baseline(batches, wl, seconds):
+    """The oracle as it stands, single-threaded, on whole steps of the same batches until
+    `seconds` of CPU work have run (at least one step)."""
+    inputs = [oracle_inputs(b["bt"], b["bt"].B) for b in batches]
+    rows, n, dt = time_oracle(inputs, seconds)
     return {"value": rows / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"{n} whole steps (schedule, pack, compact greedy verify, scatter) of the "
                       f"{wl.name} workload, {rows} packed rows, single thread",
             "cpu": cpu_model(), "host_cores": os.cpu_count()}
+
+
+def oracle_legs(legs, seconds):
+    """The oracle's rows/s beside each workload leg (single thread, bounded sample; the
+    high-load sweep at its middle theta in both modes)."""
+    from speculative_decoding_ragged_gb300 import synth
+    done = {}
+    for key, leg in legs.items():
+        name = leg["workload"]
+        if name == "large_vocab_mixed":
+            continue
+        theta = leg.get("theta_slope")
+        if theta is not None and theta != 0.004:
+            continue
+        wl = synth.WORKLOADS[name]
+        stochastic = leg["verify"] == "stochastic"
+        tag = (name, stochastic)
+        if tag not in done:
+            done[tag] = synth.make_batch(wl, seed=77, stochastic=stochastic)
+        bt = done[tag]
+        inp = oracle_inputs(bt, bt.B, leg["mode"], stochastic)
+        rows, n, dt = time_oracle([inp], seconds)
+        leg["oracle"] = {"rows_per_s": rows / dt, "cores": 1, "kind": "oracle",
+                         "sample": f"{n} whole steps of this workload and mode, single thread",
+                         "gpu_over_oracle": leg["rows_per_s"] / (rows / dt)}
 
 
 ARM_PARTS = {"0xd4f": "Arm Neoverse V2", "0xd40": "Arm Neoverse V1", "0xd0c": "Arm Neoverse N1",

@@ -33,7 +33,9 @@
  *     trap: the kernel ORs a DSPARK_STATUS_* bit into the caller's int32 `status` word, applies
  *     the documented clamp and carries on. The caller zeroes `status` when it wants a fresh
  *     report and reads it whenever convenient.
- *   - No kernel waits on another kernel, a flag or a peer; nothing can hang.
+ *   - No kernel waits on another kernel or a peer. The only waits are inside one CTA (the
+ *     bulk-copy verify kernel's shared-memory stages); each is bounded, and one that gives up
+ *     sets DSPARK_STATUS_STALL instead of hanging.
  */
 #ifndef DSPARK_H_
 #define DSPARK_H_
@@ -162,6 +164,7 @@ int dspark_schedule_pack(const float* conf, int B, int gamma, const dspark_cost*
  * Rows. Target row for (request b, block position i):
  *   COMPACT              row cu_seqlens[b] + i, i < w_b         (target_logits = packed [M, V])
  *   STATIC, CAP_ACCEPT   row b*gamma + i,       i < gamma       (target_logits = block [B*gamma, V])
+ * At most B*gamma target rows are read.
  * target row (b,i) is the target's distribution for block position i+1, which holds the draft
  * d_{i+1} = block_tokens[b, i+1]. Draft row (b,i) of draft_logits [B, gamma-1, V] is the draft
  * distribution that d_{i+1} was sampled from (stochastic only).
@@ -201,8 +204,11 @@ int dspark_schedule_pack(const float* conf, int B, int gamma, const dspark_cost*
  *   read (no clearing needed). Calls that share one workspace must not overlap on the GPU.
  * Limits: 0 <= B, 1 <= gamma <= DSPARK_MAX_GAMMA, V >= 1, temperature > 0 (stochastic).
  * Kernels: a persistent streaming kernel over fixed row chunks (register or TMA bulk-copy
- * streaming, see dspark_set_stream_kernel), then one CTA per request, and for stochastic calls
- * a bonus kernel spread over the grid.
+ * streaming, see dspark_set_stream_kernel), then, greedy: one CTA per request that combines
+ * the chunk results, walks and writes the outputs; stochastic: a bonus kernel spread over the
+ * grid whose CTAs each combine their request's chunk results and run its accept tests, sum
+ * the bonus row's weights over their tiles, and whose last CTA per request draws the bonus and
+ * writes the outputs.
  * ------------------------------------------------------------------------------------- */
 int dspark_verify(dspark_mode mode, int stochastic,
                   const void* target_logits, int target_rows, const void* draft_logits,
@@ -304,6 +310,32 @@ int dspark_observe(const float* conf, const int32_t* accept_len, const int32_t* 
                    int32_t* status, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * dspark_graph_begin / dspark_graph_end / dspark_graph_launch / dspark_graph_destroy — one or
+ * more whole decode steps captured once as a CUDA graph and replayed with a single launch
+ * ("A2 method details", ragged verify over full CUDA graphs, figure 2).
+ *
+ * dspark_graph_begin(stream) starts a stream capture (thread-local mode) on `stream`; every
+ * call of this library the caller then issues on that stream (and any other work on it) is
+ * recorded instead of run. dspark_graph_end(stream, &graph) ends the capture and instantiates
+ * it; *graph receives an opaque handle (host memory owned by the library until
+ * dspark_graph_destroy). dspark_graph_launch(graph, stream) replays the whole recording with
+ * one cudaGraphLaunch on any stream of the same device. Replays use the pointers and scalars
+ * of the captured calls: new inputs are written into the same buffers before a replay. The
+ * library's kernels read M, the windows and the tier on the device, so one graph serves every
+ * window allocation and every tier. Kernels keep their programmatic-dependent-launch edges in
+ * the graph. Make one eager call of each captured entry point on the device before the
+ * capture (per-device set-up such as shared-memory opt-ins happens on the first call).
+ * Errors: DSPARK_ERR_INVALID_ARG for the legacy default stream or NULL handles,
+ * DSPARK_ERR_CUDA when the runtime refuses the capture, its end, the instantiation or the
+ * launch (dspark_last_error names which). dspark_graph_destroy(NULL) does nothing.
+ * ------------------------------------------------------------------------------------- */
+typedef struct dspark_graph_s* dspark_graph;
+int dspark_graph_begin(cudaStream_t stream);
+int dspark_graph_end(cudaStream_t stream, dspark_graph* graph);
+int dspark_graph_launch(dspark_graph graph, cudaStream_t stream);
+int dspark_graph_destroy(dspark_graph graph);
+
+/* ---------------------------------------------------------------------------------------
  * dspark_verify_noalloc — the pages have no counterpart to this entry point; it exists for
  * callers that cannot hand the library scratch memory. Some hosts give a kernel library only
  * its input and output buffers (a plugin interface with no workspace argument), and some
@@ -316,8 +348,9 @@ int dspark_observe(const float* conf, const int32_t* accept_len, const int32_t* 
  * that loads the library keeps until the process exits. The call allocates nothing.
  *   - Sizes whose dspark_verify_workspace_bytes(B, gamma, V, stochastic) exceeds
  *     DSPARK_NOALLOC_SCRATCH_BYTES are rejected with DSPARK_ERR_UNSUPPORTED and a message.
- *   - The first call on each device looks up the array's device address (a one-time set-up,
- *     with that device current); make that first call before any stream capture.
+ *   - Each call looks up the array's device address in the current device's context
+ *     (cudaGetSymbolAddress: on the first call this loads the library's device code on that
+ *     device, so make that first call before any stream capture).
  *   - Every call on a device shares the one array and leaves its contents behind. Nothing in
  *     it needs to start at zero (each call rewrites what it reads), but calls that overlap on
  *     the GPU — on different streams, or from different host threads — race on it: order
@@ -336,7 +369,7 @@ int dspark_verify_noalloc(dspark_mode mode, int stochastic,
 /* Message of the last failed call on this host thread ("" if none). Never NULL. */
 const char* dspark_last_error(void);
 
-/* ABI version: 100 * major + minor. */
+/* ABI version: 100 * major + minor (1.1: the dspark_graph_* capture and replay calls). */
 int dspark_version(void);
 
 #ifdef __cplusplus

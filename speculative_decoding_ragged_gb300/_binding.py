@@ -70,6 +70,10 @@ SYMBOLS = {
     "dspark_verify_noalloc": ([_i, _i, _p, _i, _p, _i, _i, _p, _p, _p, _i, _i, ctypes.c_float,
                                _u64, _u64, _p, _p, _p, _p, _p, _p], _i),
     "dspark_observe": ([_p, _p, _p, _i, _i, _i, _p, _p, _p, _p], _i),
+    "dspark_graph_begin": ([_p], _i),
+    "dspark_graph_end": ([_p, ctypes.POINTER(_p)], _i),
+    "dspark_graph_launch": ([_p, _p], _i),
+    "dspark_graph_destroy": ([_p], _i),
     "dspark_set_stream_kernel": ([_i], _i),
     "dspark_set_stream_events": ([_p, _p], _i),
     "dspark_last_error": ([], ctypes.c_char_p),
@@ -171,6 +175,42 @@ def set_stream_events(start: Optional[torch.cuda.Event], stop: Optional[torch.cu
             raise ValueError("record the event once before handing it to the library")
         return ctypes.c_void_p(h)
     _check("dspark_set_stream_events", lib().dspark_set_stream_events(handle(start), handle(stop)))
+
+
+class StepGraph:
+    """Library calls captured once as a CUDA graph through the C ABI (dspark_graph_begin /
+    dspark_graph_end) and replayed with one cudaGraphLaunch (dspark_graph_launch).
+
+        s = torch.cuda.Stream()              # capture needs a stream other than the default
+        with torch.cuda.stream(s):
+            calls = [...]                    # prepared while s is current: bound to s
+            g = StepGraph(s)
+            for c in calls: c()
+            g.end()
+        g.launch()                           # replays on torch's current stream
+    """
+
+    def __init__(self, stream):
+        self._stream = _stream(stream)
+        self._h = ctypes.c_void_p()
+        _check("dspark_graph_begin", lib().dspark_graph_begin(self._stream))
+
+    def end(self):
+        _check("dspark_graph_end", lib().dspark_graph_end(self._stream, ctypes.byref(self._h)))
+        return self
+
+    def prepare_launch(self, stream=None) -> "Prepared":
+        """The replay as a prepared call bound to `stream` (torch's current by default)."""
+        return Prepared("dspark_graph_launch", (self._h, _stream(stream)))
+
+    def launch(self, stream=None):
+        _check("dspark_graph_launch", lib().dspark_graph_launch(self._h, _stream(stream)))
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value and _LIB is not None:
+            _LIB.dspark_graph_destroy(h)
+            self._h = ctypes.c_void_p()
 
 
 def version() -> int:

@@ -8,12 +8,13 @@
 //
 // Kernels of one call:
 // 1. the streaming kernel (verify_stream.cu): one partial per (row, chunk) unit;
-// 2. verify_finalize_kernel — one CTA per request: combines the chunk partials of its rows in
-//    a fixed order, runs the accept tests (Philox4x64-10 uniforms), walks to the first
-//    rejection, writes accept_len / committed / ceiling (and, fused, appends the committed
-//    tokens to the request's history);
-// 3. stochastic only, bonus_tiles_kernel — the bonus draw spread over the grid, finished by
-//    the last CTA of each request.
+// 2. greedy: verify_finalize_kernel — one CTA per request: combines the chunk partials of its
+//    rows, tests each draft against its row's argmax, walks to the first rejection, writes
+//    accept_len / committed / ceiling (and, fused, appends the committed tokens to the
+//    request's history);
+//    stochastic: bonus_final_kernel — spread over the grid: every CTA of a request combines its
+//    rows' partials and runs the accept tests (Philox4x64-10 uniforms), sums the bonus row's
+//    weights over its tiles, and the last CTA of the request draws the bonus token.
 #include <math.h>
 
 #include "verify_common.cuh"
@@ -21,8 +22,8 @@
 namespace dspark {
 namespace {
 
-// Finaliser CTA size: 256 threads for large batches; 1024 for small ones, where every row's
-// partials (target and draft rows each on a warp of their own) are combined at once.
+// Greedy finaliser CTA size: 256 threads for large batches; 1024 for small ones, where every
+// row's partials are combined at once (a warp per row).
 constexpr int kFinalThreadsLarge = 256;
 constexpr int kFinalThreadsSmall = 1024;
 constexpr int kFinalSmallBatch = 64;
@@ -167,8 +168,6 @@ __device__ __forceinline__ float sum8(const float (&w)[8])
     return ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
 }
 
-// Combined softmax statistics of one row from its nc chunk partials, by one warp, in a fixed
-// order (lane-strided, then a fixed shuffle tree): deterministic for a given nc.
 // Combined softmax statistics of one row from its nc chunk partials, by one warp: each lane
 // folds chunks lane, lane+32, ... in order (eight loads in flight at a time) with an online
 // rescale, then the lanes combine over a fixed shuffle tree — deterministic for a given nc.
@@ -226,19 +225,131 @@ __device__ __forceinline__ int combine_arg(const ArgPart* parts, int nc, int lan
     return idx == 0x7FFFFFFF ? 0 : idx;   // a row of -inf only: index 0
 }
 
-template <int DT, bool STOCH, int FT>
+// Softmax statistics (m, Z) of a request's rows j = first, first + step, ... < nrows + ndec:
+// target rows j < nrows (partials at part_t + (base + j) * nc), then draft rows (part_d +
+// (base + j - nrows) * nc). RB rows at a time with every partial load of the batch in flight
+// (CPL loads per lane and row, nc <= 32 * CPL); each row folds exactly as combine_soft does
+// (lane-strided, in chunk order, then the fixed shuffle tree), so every CTA that combines a
+// row gets the same bits. Lane 0 stores the results.
+template <int RB, int CPL>
+__device__ __forceinline__ void combine_soft_rows(const FinalArgs& A, int64_t base, int nrows,
+                                                  int ndec, int first, int step, int lane,
+                                                  float* m_t, float* z_t, float* m_d, float* z_d)
+{
+    const int n = nrows + ndec;
+    for (int j0 = first; j0 < n; j0 += step * RB) {
+        SoftPart p[RB][CPL];
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+            const int j = j0 + r * step;
+            const SoftPart* parts =
+                j < nrows ? static_cast<const SoftPart*>(A.part_t) + (base + j) * A.nc
+                          : static_cast<const SoftPart*>(A.part_d) + (base + j - nrows) * A.nc;
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) {
+                const int k = lane + 32 * c;
+                if (j < n && k < A.nc) {
+                    const float2 v = __ldcg(reinterpret_cast<const float2*>(parts + k));
+                    p[r][c].m = v.x;
+                    p[r][c].z = v.y;
+                } else {
+                    p[r][c].m = -INFINITY;
+                    p[r][c].z = 0.0f;
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+            const int j = j0 + r * step;
+            if (j >= n) break;
+            float m = -INFINITY, z = 0.0f;
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) {
+                if (p[r][c].m == -INFINITY) continue;
+                if (p[r][c].m > m) {
+                    z *= ex2_approx((m - p[r][c].m) * A.s);
+                    m = p[r][c].m;
+                }
+                z += p[r][c].z * ex2_approx((p[r][c].m - m) * A.s);
+            }
+            float M = m;
+            for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+            float zz = m != -INFINITY ? z * ex2_approx((m - M) * A.s) : 0.0f;
+            for (int off = 16; off > 0; off >>= 1) zz += __shfl_xor_sync(0xffffffffu, zz, off);
+            if (lane == 0) {
+                if (j < nrows) { m_t[j] = M; z_t[j] = zz; }
+                else { m_d[j - nrows] = M; z_d[j - nrows] = zz; }
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void combine_request_rows(const FinalArgs& A, int64_t base, int nrows,
+                                                     int ndec, int warp, int warps, int lane,
+                                                     float* m_t, float* z_t, float* m_d,
+                                                     float* z_d)
+{
+    if (A.nc <= 32) {
+        combine_soft_rows<4, 1>(A, base, nrows, ndec, warp, warps, lane, m_t, z_t, m_d, z_d);
+    } else if (A.nc <= 64) {
+        combine_soft_rows<4, 2>(A, base, nrows, ndec, warp, warps, lane, m_t, z_t, m_d, z_d);
+    } else if (A.nc <= 128) {
+        combine_soft_rows<2, 4>(A, base, nrows, ndec, warp, warps, lane, m_t, z_t, m_d, z_d);
+    } else {                                          // very wide rows: one at a time
+        for (int j = warp; j < nrows + ndec; j += warps) {
+            const SoftPart* parts =
+                j < nrows ? static_cast<const SoftPart*>(A.part_t) + (base + j) * A.nc
+                          : static_cast<const SoftPart*>(A.part_d) + (base + j - nrows) * A.nc;
+            float m, z;
+            combine_soft(parts, A.nc, A.s, lane, m, z);
+            if (lane == 0) {
+                if (j < nrows) { m_t[j] = m; z_t[j] = z; }
+                else { m_d[j - nrows] = m; z_d[j - nrows] = z; }
+            }
+        }
+    }
+}
+
+// Outputs of a request whose rows lie outside the buffer: nothing committed, (-1, -1) on its
+// rows that the buffer does hold, BAD_ROWS (with the caller's bits), and the fused scatter
+// checks the history length only. Threads tid < nthreads of one CTA; warp 0 scatters.
+__device__ __forceinline__ void bad_rows_outputs(const FinalArgs& A, int b, int64_t base,
+                                                 int nrows, int tid, int nthreads, int bits,
+                                                 int n_hist)
+{
+    int32_t* out = A.committed + static_cast<int64_t>(b) * A.gamma;
+    for (int k = tid; k < A.gamma; k += nthreads) out[k] = -1;
+    if (A.row_prob) {
+        for (int t = tid; t < nrows; t += nthreads) {
+            const int64_t r = base + t;
+            if (r >= 0 && r < A.target_rows) {
+                A.row_prob[r * 2] = -1.0f;
+                A.row_prob[r * 2 + 1] = -1.0f;
+            }
+        }
+    }
+    if (tid == 0) {
+        A.accept_len[b] = 0;
+        if (A.ceiling) A.ceiling[b] = (A.mode == DSPARK_COMPACT) ? -1 : 0;
+        raise_status(A.status, bits | DSPARK_STATUS_BAD_ROWS);
+    }
+    if (A.out_tokens && tid < 32) {
+        const int sb = scatter_request(b, 0, A.gamma, -1, tid, A.out_tokens, A.out_len,
+                                       A.out_cap, n_hist);
+        if (tid == 0) raise_status(A.status, sb);
+    }
+}
+
+// Greedy verify's finaliser: one CTA per request combines the argmax partials of its rows (one
+// warp per row), then warp 0 runs the accept tests, walks to the first rejection and writes the
+// request's outputs (and, fused, appends its tokens to the history).
+template <int DT, int FT>
 __global__ void __launch_bounds__(FT)
 verify_finalize_kernel(FinalArgs A)
 {
     constexpr int kFinalThreads = FT;
     constexpr int kFinalWarps = FT / 32;
-    constexpr int E = (DT == DSPARK_BF16) ? 2 : 4;
     __shared__ int g_s[DSPARK_MAX_GAMMA];
-    __shared__ float mp_s[DSPARK_MAX_GAMMA], mq_s[DSPARK_MAX_GAMMA];
-    __shared__ float zp_s[DSPARK_MAX_GAMMA], zq_s[DSPARK_MAX_GAMMA];
-    __shared__ uint64_t ub_s[DSPARK_MAX_GAMMA];
-    __shared__ int acc_s[DSPARK_MAX_GAMMA];
-    __shared__ int walk_s[4];                 // Lc, Lf, pos, rejected
 
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
@@ -266,172 +377,55 @@ verify_finalize_kernel(FinalArgs A)
     // kernel of this library triggers its dependents only after its own wait, so all kernels
     // before the streaming kernel have completed by the time this one starts
     const int n_hist = (A.out_tokens != nullptr && warp == 0) ? A.out_len[b] : 0;
-    // stochastic: the two logits of this thread's tested draft are inputs of the call as well
-    float lp_pre = 0.0f, lq_pre = 0.0f;
-    if (STOCH && tid < nrows - 1 && base >= 0 && base + nrows <= n_t && d_mine >= 0 &&
-        d_mine < A.V) {
-        lp_pre = load_logit<DT>(static_cast<const char*>(A.target) + (base + tid) * A.V * E, d_mine);
-        lq_pre = load_logit<DT>(static_cast<const char*>(A.draft) +
-                                    (static_cast<int64_t>(b) * L + tid) * A.V * E, d_mine);
-    }
     pdl_wait_and_trigger();
     int32_t* out = A.committed + static_cast<int64_t>(b) * gamma;
 
     if (base < 0 || base + nrows > n_t) {
-        for (int k = tid; k < gamma; k += kFinalThreads) out[k] = -1;
-        if (tid == 0) {
-            A.accept_len[b] = 0;
-            if (A.ceiling) A.ceiling[b] = (A.mode == DSPARK_COMPACT) ? -1 : 0;
-            raise_status(A.status, bits | DSPARK_STATUS_BAD_ROWS);
-            if (STOCH) {
-                BonusJob job = {};
-                job.slot = -1;
-                A.jobs[b] = job;
-                A.done[b] = 0u;
-            }
-        }
-        if (A.out_tokens && warp == 0) {         // nothing committed: lengths checked only
-            const int sb = scatter_request(b, 0, gamma, -1, lane, A.out_tokens, A.out_len,
-                                           A.out_cap, n_hist);
-            if (lane == 0) raise_status(A.status, sb);
-        }
+        bad_rows_outputs(A, b, base, nrows, tid, kFinalThreads, bits, n_hist);
         return;
     }
     const int ndec = nrows - 1;   // accept tests this mode runs
 
-    // 1. per-row statistics from the chunk partials; one warp per row: the target rows, then
-    //    (stochastic) the draft rows of the tested positions
-    const int row_jobs = STOCH ? nrows + ndec : nrows;
-    for (int t = warp; t < row_jobs; t += kFinalWarps) {
-        if (!STOCH) {
-            const int g = combine_arg(static_cast<const ArgPart*>(A.part_t) + (base + t) * A.nc,
-                                      A.nc, lane);
-            if (lane == 0) g_s[t] = g;
-        } else {
-            const bool target = t < nrows;
-            const int i = target ? t : t - nrows;
-            const SoftPart* parts = static_cast<const SoftPart*>(target ? A.part_t : A.part_d);
-            float m, z;
-            combine_soft(parts + (base + i) * A.nc, A.nc, A.s, lane, m, z);
-            if (lane == 0) {
-                if (target) { mp_s[i] = m; zp_s[i] = z; }
-                else { mq_s[i] = m; zq_s[i] = z; }
-            }
-        }
+    // 1. per-row argmax from the chunk partials, one warp per row
+    for (int t = warp; t < nrows; t += kFinalWarps) {
+        const int g = combine_arg(static_cast<const ArgPart*>(A.part_t) + (base + t) * A.nc,
+                                  A.nc, lane);
+        if (lane == 0) g_s[t] = g;
     }
     __syncthreads();
 
-    // 2. accept tests, one thread per tested position (greedy: warp 0 does 2 and 3 alone)
-    if (STOCH && tid < nrows) {
-        const int i = tid;
-        int accepted = 0;
-        const bool tested = i < ndec;
-        const int d = tested ? d_mine : -1;
-        const bool valid = d >= 0 && d < A.V;
-        if (tested && !valid) bits |= DSPARK_STATUS_BAD_TOKEN;
-        if (!STOCH) {
-            if (tested && valid) accepted = (d == g_s[i]);
-            if (A.row_prob) {
-                A.row_prob[(base + i) * 2] = -1.0f;
-                A.row_prob[(base + i) * 2 + 1] = -1.0f;
-            }
-        } else {
-            uint64_t rnd[4];
-            philox4x64_10(static_cast<uint64_t>(b), static_cast<uint64_t>(i), A.step, 0ull, A.seed, 0ull, rnd);
-            ub_s[i] = rnd[1] >> 11;                 // u' = ub_s[i] * 2^-53
-            float pp = -1.0f, qq = -1.0f;
-            if (tested && valid) {
-                const float lp = lp_pre;                // loaded before the wait
-                const float lq = lq_pre;
-                // fp32 (FP64 is scarce here): exponents relative to each row's maximum, and the
-                // ratio as one exp2 of their difference, so p/q neither under- nor overflows
-                const float ep = (lp - mp_s[i]) * A.s;
-                const float eq = (lq - mq_s[i]) * A.s;
-                const float u = static_cast<float>(rnd[0] >> 40) * 0x1p-24f;
-                if (lq == -INFINITY) {
-                    accepted = 1;                          // q(d) = 0
-                } else {
-                    const float ratio = exp2f(ep - eq) * (zq_s[i] / zp_s[i]);
-                    accepted = u < ratio;
-                }
-                pp = exp2f(ep) / zp_s[i];
-                qq = exp2f(eq) / zq_s[i];
-            }
-            if (A.row_prob) {
-                A.row_prob[(base + i) * 2] = pp;
-                A.row_prob[(base + i) * 2 + 1] = qq;
-            }
-        }
-        acc_s[i] = tested ? accepted : 0;
-    }
-    if (STOCH) __syncthreads();
-
-    // 3. walks (warp 0): the window's accept length (identical in compact and cap-accept) and
-    //    the full block's; positions past the tested ones count as rejections
+    // 2. warp 0: accept tests (lane i tests draft d_{i+1} against row i's argmax), the walk to
+    //    the first rejection, the outputs and the fused scatter
     if (warp == 0) {
-        bool acc;
-        if (!STOCH) {
-            // greedy accept test of lane i < ndec: the draft equals the row's argmax
-            const bool tested = lane < ndec;
-            const bool valid = d_mine >= 0 && d_mine < A.V;
-            if (tested && !valid) bits |= DSPARK_STATUS_BAD_TOKEN;
-            acc = tested && valid && d_mine == g_s[lane];
-            if (A.row_prob && lane < nrows) {
-                A.row_prob[(base + lane) * 2] = -1.0f;
-                A.row_prob[(base + lane) * 2 + 1] = -1.0f;
-            }
-        } else {
-            acc = lane < ndec && acc_s[lane] != 0;
+        const bool tested = lane < ndec;
+        const bool valid = d_mine >= 0 && d_mine < A.V;
+        if (tested && !valid) bits |= DSPARK_STATUS_BAD_TOKEN;
+        const bool acc = tested && valid && d_mine == g_s[lane];
+        if (A.row_prob && lane < nrows) {
+            A.row_prob[(base + lane) * 2] = -1.0f;
+            A.row_prob[(base + lane) * 2 + 1] = -1.0f;
         }
         const unsigned rej = __ballot_sync(0xffffffffu, !acc);   // ndec <= 31: never zero
         const int lead = __ffs(rej) - 1;                          // leading accepted drafts
         const int Lc = 1 + min(lead, w - 1);
         const int Lf = 1 + lead;
         if (lane == 0) {
-            walk_s[0] = Lc;
-            walk_s[1] = Lf;
-            walk_s[2] = Lc - 1;
-            walk_s[3] = (Lc - 1 < w - 1) ? 1 : 0;
             A.accept_len[b] = Lc;
             if (A.ceiling) A.ceiling[b] = (A.mode == DSPARK_COMPACT) ? -1 : Lf;
         }
-        if (!STOCH && lane < gamma) out[lane] = (lane < Lc) ? g_s[lane] : -1;
-        if (!STOCH && A.out_tokens) {
+        if (lane < gamma) out[lane] = (lane < Lc) ? g_s[lane] : -1;
+        if (A.out_tokens) {
             const int tok = lane < Lc ? g_s[lane] : -1;
             const int sb = scatter_request(b, Lc, gamma, tok, lane, A.out_tokens, A.out_len,
                                            A.out_cap, n_hist);
             if (lane == 0) bits |= sb;
         }
-    }
-    if (STOCH) {
-        __syncthreads();
-        const int Lc = walk_s[0];
-        for (int k = tid; k < gamma; k += kFinalThreads)
-            out[k] = (k < Lc - 1) ? A.tokens[static_cast<int64_t>(b) * gamma + k + 1] : -1;
-        // 4. the bonus draw: the residual of the rejecting position, or p of the last verified
-        //    position after full acceptance; carried out by the bonus kernel
-        if (tid == 0) {
-            const int pos = Lc - 1;
-            const bool residual = pos < w - 1;
-            BonusJob job;
-            job.trow = base + pos;
-            job.drow = residual ? static_cast<int64_t>(b) * L + pos : -1;
-            job.mp = mp_s[pos];
-            job.izp = 1.0f / zp_s[pos];
-            job.mq = residual ? mq_s[pos] : 0.0f;
-            job.izq = residual ? 1.0f / zq_s[pos] : 0.0f;
-            job.ubits = ub_s[pos];
-            job.slot = static_cast<int64_t>(b) * gamma + Lc - 1;
-            A.jobs[b] = job;
-            A.done[b] = 0u;
+        const unsigned any = __ballot_sync(0xffffffffu, bits != 0);
+        if (any) {
+            int all = bits;
+            for (int off = 16; off > 0; off >>= 1) all |= __shfl_xor_sync(0xffffffffu, all, off);
+            if (lane == 0) raise_status(A.status, all);
         }
-    }
-    // status bits of the CTA
-    const unsigned any = __ballot_sync(0xffffffffu, bits != 0);
-    if (any) {
-        int all = bits;
-        for (int off = 16; off > 0; off >>= 1) all |= __shfl_xor_sync(0xffffffffu, all, off);
-        if (lane == 0) raise_status(A.status, all);
     }
 }
 
@@ -590,27 +584,146 @@ __device__ void bonus_pick(const FinalArgs& A, int b, const BonusJob& job, int n
     }
 }
 
-// Stochastic bonus, step 1: weight sums of every 256-token tile of each request's bonus row(s),
-// spread over the whole grid (G tiles per warp, eight warps per CTA, all loads of a warp issued
-// before its exponentials; G = 1 spreads a small batch over more SMs). A residual draw also records p's sums, for the rare
-// fallback to p when rounding leaves a residual of zero. The last of a request's CTAs to finish
-// (a per-request counter the finaliser zeroed) then performs step 2.
+// Stochastic verify after the streaming kernel, in one launch spread over the grid: the CTAs
+// of request b (ctas_per_request of them, each with kTilesPerCta 256-token tiles) each
+//   1. combine the chunk partials of the request's target and draft rows into (m, Z) per row
+//      (rows spread over the CTA's warps; every CTA gets the same bits),
+//   2. run the accept tests of its drafts (Philox4x64-10 uniforms, the min(1, p/q) rule) and
+//      walk to the first rejection, which fixes the bonus row: the residual max(0, p - q) of
+//      the rejecting position, or p of the last verified position after full acceptance,
+//   3. sum the bonus weights over their own tiles (a residual draw also records p's sums, for
+//      the rare fallback to p when rounding leaves a residual of zero),
+// and the last of the request's CTAs to finish (a per-request counter that the streaming kernel
+// zeroed; no CTA waits for another) draws the bonus token by the inverse CDF over the tile sums
+// and appends the request's tokens when fused. CTA 0 of the request writes accept_len, the
+// ceiling, row_prob and every committed slot but the bonus one, which the drawing CTA writes.
 template <int DT, int G>
 __global__ void __launch_bounds__(kTileThreads)
-bonus_tiles_kernel(FinalArgs A, int ctas_per_request)
+bonus_final_kernel(FinalArgs A, int ctas_per_request)
 {
     constexpr int kBonusGroup = G;            // tiles a warp loads before reducing them
     constexpr int kTilesPerCta = kTileWarps * G;
     constexpr int E = (DT == DSPARK_BF16) ? 2 : 4;
+    __shared__ float mp_s[DSPARK_MAX_GAMMA], zp_s[DSPARK_MAX_GAMMA];
+    __shared__ float mq_s[DSPARK_MAX_GAMMA], zq_s[DSPARK_MAX_GAMMA];
+    __shared__ BonusJob job_s;
     const int b = blockIdx.x / ctas_per_request;
-    // the history length for the fused scatter, read before the wait (see the finaliser)
-    const int n_hist = (A.out_tokens != nullptr && threadIdx.x < 32) ? A.out_len[b] : 0;
-    pdl_wait_and_trigger();
     const int cta = blockIdx.x - b * ctas_per_request;
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const BonusJob job = A.jobs[b];
-    if (job.slot < 0) return;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int gamma = A.gamma;
+    const int L = gamma - 1;
+    int bits = 0;
+    // Inputs of the call (drafts, windows, cu_seqlens, the tested drafts' two logits, the
+    // history length) are fetched before waiting for the streaming kernel: no kernel of this
+    // call writes them, and the previous call's kernels have completed by then.
+    const int d_mine = (warp == 0 && lane < L)
+                           ? __ldg(A.tokens + static_cast<int64_t>(b) * gamma + lane + 1) : -1;
+    int w = gamma;
+    if (A.mode != DSPARK_STATIC) {
+        w = __ldg(A.windows + b);
+        if (w < 1 || w > gamma) {
+            if (tid == 0 && cta == 0) bits |= DSPARK_STATUS_BAD_WINDOW;
+            w = w < 1 ? 1 : gamma;
+        }
+    }
+    const int nrows = (A.mode == DSPARK_COMPACT) ? w : gamma;
+    const int ndec = nrows - 1;
+    const int64_t base = (A.mode == DSPARK_COMPACT) ? static_cast<int64_t>(__ldg(A.cu + b))
+                                                    : static_cast<int64_t>(b) * gamma;
+    const int64_t n_t = target_row_count(A.mode, A.cu, A.B, gamma, A.target_rows, A.rows_max);
+    const bool rows_ok = base >= 0 && base + nrows <= n_t;
+    const bool tested = warp == 0 && lane < ndec;
+    const bool valid = d_mine >= 0 && d_mine < A.V;
+    float lp = 0.0f, lq = 0.0f;
+    if (rows_ok && tested && valid) {
+        lp = load_logit<DT>(static_cast<const char*>(A.target) + (base + lane) * A.V * E, d_mine);
+        lq = load_logit<DT>(static_cast<const char*>(A.draft) +
+                                (static_cast<int64_t>(b) * L + lane) * A.V * E, d_mine);
+    }
+    const int n_hist = (A.out_tokens != nullptr && warp == 0) ? A.out_len[b] : 0;
+    pdl_wait_and_trigger();
+
+    if (!rows_ok) {
+        if (cta == 0) bad_rows_outputs(A, b, base, nrows, tid, kTileThreads, bits, n_hist);
+        return;
+    }
+
+    // 1. (m, Z) of the request's target rows and tested draft rows
+    combine_request_rows(A, base, nrows, ndec, warp, kTileWarps, lane, mp_s, zp_s, mq_s, zq_s);
+    __syncthreads();
+
+    // 2. accept tests, the walk and the bonus job (warp 0); CTA 0 writes the outputs
+    if (warp == 0) {
+        const bool writer = cta == 0;
+        if (tested && !valid) bits |= DSPARK_STATUS_BAD_TOKEN;
+        uint64_t ub = 0;
+        bool acc = false;
+        if (lane < nrows) {
+            uint64_t rnd[4];
+            philox4x64_10(static_cast<uint64_t>(b), static_cast<uint64_t>(lane), A.step, 0ull,
+                          A.seed, 0ull, rnd);
+            ub = rnd[1] >> 11;                      // u' = ub * 2^-53
+            float pp = -1.0f, qq = -1.0f;
+            if (tested && valid) {
+                // fp32 (FP64 is scarce here): exponents relative to each row's maximum, and the
+                // ratio as one exp2 of their difference, so p/q neither under- nor overflows
+                const float ep = (lp - mp_s[lane]) * A.s;
+                const float eq = (lq - mq_s[lane]) * A.s;
+                const float u = static_cast<float>(rnd[0] >> 40) * 0x1p-24f;
+                if (lq == -INFINITY) {
+                    acc = true;                     // q(d) = 0
+                } else {
+                    const float ratio = exp2f(ep - eq) * (zq_s[lane] / zp_s[lane]);
+                    acc = u < ratio;
+                }
+                pp = exp2f(ep) / zp_s[lane];
+                qq = exp2f(eq) / zq_s[lane];
+            }
+            if (writer && A.row_prob) {
+                A.row_prob[(base + lane) * 2] = pp;
+                A.row_prob[(base + lane) * 2 + 1] = qq;
+            }
+        }
+        const unsigned rej = __ballot_sync(0xffffffffu, !acc);   // ndec <= 31: never zero
+        const int lead = __ffs(rej) - 1;
+        const int Lc = 1 + min(lead, w - 1);
+        const int Lf = 1 + lead;
+        const int pos = Lc - 1;
+        const uint64_t jub = __shfl_sync(0xffffffffu, ub, pos);
+        if (lane == 0) {
+            const bool residual = pos < w - 1;
+            BonusJob job;
+            job.trow = base + pos;
+            job.drow = residual ? static_cast<int64_t>(b) * L + pos : -1;
+            job.mp = mp_s[pos];
+            job.izp = 1.0f / zp_s[pos];
+            job.mq = residual ? mq_s[pos] : 0.0f;
+            job.izq = residual ? 1.0f / zq_s[pos] : 0.0f;
+            job.ubits = jub;
+            job.slot = static_cast<int64_t>(b) * gamma + Lc - 1;
+            job_s = job;
+        }
+        if (writer) {
+            int32_t* out = A.committed + static_cast<int64_t>(b) * gamma;
+            if (lane < gamma && lane != Lc - 1) out[lane] = (lane < Lc - 1) ? d_mine : -1;
+            if (lane == 0) {
+                A.accept_len[b] = Lc;
+                if (A.ceiling) A.ceiling[b] = (A.mode == DSPARK_COMPACT) ? -1 : Lf;
+            }
+            const unsigned any = __ballot_sync(0xffffffffu, bits != 0);
+            if (any) {
+                int all = bits;
+                for (int off = 16; off > 0; off >>= 1) all |= __shfl_xor_sync(0xffffffffu, all, off);
+                if (lane == 0) raise_status(A.status, all);
+            }
+        }
+    }
+    __syncthreads();
+    const BonusJob job = job_s;
+
+    // 3. this CTA's tile sums of the bonus row(s)
     const bool residual = job.drow >= 0;
     const char* trow = static_cast<const char*>(A.target) + job.trow * A.V * E;
     const char* drow = static_cast<const char*>(A.draft) + (residual ? job.drow : 0) * A.V * E;
@@ -622,7 +735,7 @@ bonus_tiles_kernel(FinalArgs A, int ctas_per_request)
         load8<DT>(trow, v0, A.V, A.vec, xp[g]);
         if (residual) load8<DT>(drow, v0, A.V, A.vec, xq[g]);
     }
-    float* out = A.tiles + static_cast<int64_t>(b) * A.n_tiles * 2;
+    float* sums = A.tiles + static_cast<int64_t>(b) * A.n_tiles * 2;
 #pragma unroll
     for (int g = 0; g < kBonusGroup; ++g) {
         const int t = t0 + g;
@@ -646,17 +759,17 @@ bonus_tiles_kernel(FinalArgs A, int ctas_per_request)
             sr += __shfl_xor_sync(0xffffffffu, sr, off);
         }
         if (lane == 0 && t < A.n_tiles) {
-            out[2 * t] = sr;
-            out[2 * t + 1] = sp;
+            sums[2 * t] = sr;
+            sums[2 * t + 1] = sp;
         }
     }
-    // the request's last tile CTA to finish draws the token (no CTA ever waits for another):
-    // each lane that wrote tile sums publishes them at device scope, then one thread counts
-    // the CTA done; the pick reads the sums from L2 (ld.global.cg)
+    // the request's last CTA to finish draws the token: each lane that wrote tile sums
+    // publishes them at device scope, then one thread counts the CTA done; the pick reads the
+    // sums from L2 (ld.global.cg)
     __shared__ bool last_s;
     if (lane == 0) __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
         last_s = atomicAdd(A.done + b, 1u) == static_cast<unsigned>(ctas_per_request) - 1;
         if (last_s) __threadfence();
     }
@@ -696,6 +809,9 @@ int run_verify(const VerifyCall& c, const Plan& plan, void* part_t, void* part_d
     sa.target_rows = c.target_rows;
     sa.rows_max = plan.rows_max;
     sa.s = s;
+    // stochastic: the bonus kernel's per-request counters, zeroed by the streaming kernel
+    sa.zero = STOCH ? reinterpret_cast<unsigned*>(static_cast<BonusJob*>(jobs) + c.B) : nullptr;
+    sa.n_zero = STOCH ? c.B : 0;
 
     const int64_t max_units = (plan.rows_max + (STOCH ? static_cast<int64_t>(c.B) * L : 0)) * plan.nc;
     int rc = launch_verify_stream(DT, STOCH, sa, max_units, stream);
@@ -732,24 +848,24 @@ int run_verify(const VerifyCall& c, const Plan& plan, void* part_t, void* part_d
     fa.out_len = c.out_len;
     fa.out_cap = c.out_cap;
     fa.n_tiles = (c.V + 255) / 256;
-    if (c.B <= kFinalSmallBatch)
-        rc = launch_pdl("verify (finalize)", verify_finalize_kernel<DT, STOCH, kFinalThreadsSmall>,
-                        dim3(c.B), dim3(kFinalThreadsSmall), 0, stream, fa);
-    else
-        rc = launch_pdl("verify (finalize)", verify_finalize_kernel<DT, STOCH, kFinalThreadsLarge>,
-                        dim3(c.B), dim3(kFinalThreadsLarge), 0, stream, fa);
-    if (rc != DSPARK_OK || !STOCH) return rc;
+    if (!STOCH) {
+        if (c.B <= kFinalSmallBatch)
+            return launch_pdl("verify (finalize)", verify_finalize_kernel<DT, kFinalThreadsSmall>,
+                              dim3(c.B), dim3(kFinalThreadsSmall), 0, stream, fa);
+        return launch_pdl("verify (finalize)", verify_finalize_kernel<DT, kFinalThreadsLarge>,
+                          dim3(c.B), dim3(kFinalThreadsLarge), 0, stream, fa);
+    }
     // one tile per warp while the batch's bonus rows would not cover the SMs, four otherwise
     DeviceInfo dev;
     rc = current_device(&dev);
     if (rc != DSPARK_OK) return rc;
     const int64_t cpr4 = ceil_div(fa.n_tiles, kTileWarps * 4);
     if (static_cast<int64_t>(c.B) * cpr4 >= dev.sm_count)
-        return launch_pdl("verify (bonus)", bonus_tiles_kernel<DT, 4>,
+        return launch_pdl("verify (bonus)", bonus_final_kernel<DT, 4>,
                           dim3(static_cast<unsigned>(c.B * cpr4)), dim3(kTileThreads), 0, stream,
                           fa, static_cast<int>(cpr4));
     const int64_t cpr1 = ceil_div(fa.n_tiles, kTileWarps);
-    return launch_pdl("verify (bonus)", bonus_tiles_kernel<DT, 1>,
+    return launch_pdl("verify (bonus)", bonus_final_kernel<DT, 1>,
                       dim3(static_cast<unsigned>(c.B * cpr1)), dim3(kTileThreads), 0, stream, fa,
                       static_cast<int>(cpr1));
 }

@@ -76,10 +76,20 @@ struct StreamArgs {
     void* part_t;
     void* part_d;
     int32_t* status;
+    unsigned* zero;   // counters of the call's next kernel, zeroed here (nullptr: none)
+    int n_zero;
     int mode, V, nc, C, vec, B, gamma, target_rows;
     int64_t rows_max;
     float s;   // log2(e) / temperature
 };
+
+// Zeroes the counters the call's next kernel counts on: that kernel waits for this one to
+// complete before it reads them, and this one waited for the previous call's kernels.
+__device__ __forceinline__ void zero_next_counters(const StreamArgs& A)
+{
+    if (A.zero != nullptr && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < A.n_zero; i += blockDim.x) A.zero[i] = 0u;
+}
 
 // Rows this call verifies: compact M = cu[B] (bounded by the buffer), else B*gamma.
 __device__ __forceinline__ int64_t target_row_count(int mode, const int32_t* cu, int B, int gamma,

@@ -5,8 +5,6 @@
 // input and output buffers, and serving loops that reserve the device's memory up front and
 // must not call cudaMalloc mid-step. This file allocates nothing: the array below is part of
 // the library's device image, and each call forwards to dspark_verify with its address.
-#include <mutex>
-
 #include "common.cuh"
 
 namespace {
@@ -17,32 +15,21 @@ constexpr size_t kScratchBytes = DSPARK_NOALLOC_SCRATCH_BYTES;
 // this name is only a host-side stand-in: the device address comes from cudaGetSymbolAddress.
 static __device__ __align__(256) unsigned char g_verify_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mutex;
-void* g_scratch_address[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device, looked up once per device.
+// Device address of the scratch array in the current device's context. Looked up on every
+// call (after the module's first load this is a host-side table lookup), so a device reset or
+// another context current on the device never leaves a stale address behind.
 int scratch_address(void** out)
 {
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return dspark::fail(DSPARK_ERR_CUDA, "dspark_verify_noalloc: cudaGetDevice: %s",
-                            cudaGetErrorString(e));
-    if (dev < 0 || dev >= kMaxDevices)
-        return dspark::fail(DSPARK_ERR_UNSUPPORTED, "dspark_verify_noalloc: device %d beyond %d",
-                            dev, kMaxDevices);
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (g_scratch_address[dev] == nullptr) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_verify_scratch);
-        if (e != cudaSuccess || p == nullptr)
-            return dspark::fail(DSPARK_ERR_CUDA,
-                                "dspark_verify_noalloc: cudaGetSymbolAddress of the scratch "
-                                "array failed on device %d: %s", dev, cudaGetErrorString(e));
-        g_scratch_address[dev] = p;
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_verify_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+        int dev = -1;
+        cudaGetDevice(&dev);
+        return dspark::fail(DSPARK_ERR_CUDA,
+                            "dspark_verify_noalloc: cudaGetSymbolAddress of the scratch array "
+                            "failed on device %d: %s", dev, cudaGetErrorString(e));
     }
-    *out = g_scratch_address[dev];
+    *out = p;
     return DSPARK_OK;
 }
 

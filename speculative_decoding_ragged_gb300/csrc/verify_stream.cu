@@ -69,6 +69,7 @@ verify_stream_kernel(StreamArgs A)
 {
     constexpr int E = (DT == DSPARK_BF16) ? 2 : 4;
     pdl_wait_and_trigger();
+    zero_next_counters(A);
     const int lane = threadIdx.x & 31;
     const int64_t gw = static_cast<int64_t>(blockIdx.x) * kStreamWarps + (threadIdx.x >> 5);
     const int64_t GW = static_cast<int64_t>(gridDim.x) * kStreamWarps;
@@ -95,11 +96,12 @@ verify_stream_kernel(StreamArgs A)
 // A persistent grid (a few CTAs per SM) where each CTA owns a contiguous run of units. Warp
 // kBulkConsumers is the producer: its lane 0 walks the run and, for the k-th unit, waits until
 // stage k % S is free, arms that stage's "full" mbarrier with the unit's byte count and starts
-// one cp.async.bulk of the whole chunk into the stage. Consumer warp k % kBulkConsumers waits on the full barrier,
-// folds the staged chunk with the same per-lane order as the register kernel, releases the
-// stage on its "empty" barrier and writes the unit's partial. Every wait is bounded (about a
-// second of SM clock); a wait that gives up sets DSPARK_STATUS_STALL and the producer still
-// waits, bounded, for every copy it started before the CTA exits.
+// one cp.async.bulk of the whole chunk into the stage. Consumer warp k % kBulkConsumers waits
+// on the full barrier, folds the staged chunk with the same per-lane order as the register
+// kernel, releases the stage on its "empty" barrier and writes the unit's partial. Every wait
+// is bounded (about a second of SM clock from its own start); a wait that gives up sets
+// DSPARK_STATUS_STALL and the producer still waits, bounded, for every copy it started before
+// the CTA exits.
 // Measured on GB300 (whole steps of the large-vocab and high-load workloads): 4 consumer warps,
 // chunks of up to 12288 elements and a 96 KB ring (four stages of up to 24 KB, two CTAs per SM,
 // eight chunks in flight per SM) beat chunks of 2048-8192 elements in 32-80 KB rings (three or
@@ -141,10 +143,12 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// Waits for the completion of the barrier phase of this parity; false once the deadline (an
-// SM clock value) has passed.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long deadline)
+// Waits for the completion of the barrier phase of this parity; false once kWaitCycles of SM
+// clock have passed since this wait began (each wait has its own limit, so only one phase that
+// stalls that long trips it).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
 {
+    const long long deadline = clock64() + kWaitCycles;
     while (true) {
         uint32_t done;
         asm volatile(
@@ -229,12 +233,12 @@ verify_bulk_kernel(StreamArgs A, int stages, int stage_bytes)
     }
     __syncthreads();
     pdl_wait_and_trigger();
+    zero_next_counters(A);
     int64_t n_t;
     const int64_t U = unit_count<STOCH>(A, n_t);
     const int64_t u0 = static_cast<int64_t>(blockIdx.x) * U / gridDim.x;
     const int64_t u1 = static_cast<int64_t>(blockIdx.x + 1) * U / gridDim.x;
     const int64_t K = u1 - u0;
-    const long long deadline = clock64() + kWaitCycles;
 
     if (warp == kBulkConsumers) {                     // producer warp: lane 0 issues
         if (lane != 0) return;
@@ -247,7 +251,7 @@ verify_bulk_kernel(StreamArgs A, int stages, int stage_bytes)
         int64_t k = 0;
         for (; k < K; ++k) {
             const uint32_t full = smem_addr(&full_bar[s]);
-            if (k >= stages && !mbar_wait(smem_addr(&empty_bar[s]), ph ^ 1u, deadline)) {
+            if (k >= stages && !mbar_wait(smem_addr(&empty_bar[s]), ph ^ 1u)) {
                 ok = false;
                 break;
             }
@@ -267,10 +271,9 @@ verify_bulk_kernel(StreamArgs A, int stages, int stage_bytes)
         }
         // every started copy must land before this CTA may exit
         const int64_t issued = k;
-        const long long drain = clock64() + kWaitCycles;
         for (int s = 0; s < stages && s < issued; ++s) {
             const int64_t uses = (issued - s + stages - 1) / stages;
-            if (!mbar_wait(smem_addr(&full_bar[s]), static_cast<uint32_t>((uses - 1) & 1), drain))
+            if (!mbar_wait(smem_addr(&full_bar[s]), static_cast<uint32_t>((uses - 1) & 1)))
                 ok = false;
         }
         if (!ok) raise_status(A.status, DSPARK_STATUS_STALL);
@@ -282,7 +285,7 @@ verify_bulk_kernel(StreamArgs A, int stages, int stage_bytes)
     int s = warp;                                     // stages % kBulkConsumers == 0
     uint32_t ph = 0;
     for (int64_t k = warp; k < K; k += kBulkConsumers) {
-        bool ok = mbar_wait(smem_addr(&full_bar[s]), ph, deadline);
+        bool ok = mbar_wait(smem_addr(&full_bar[s]), ph);
         if (!__all_sync(0xffffffffu, ok)) {
             if (lane == 0) raise_status(A.status, DSPARK_STATUS_STALL);
             break;

@@ -3,8 +3,8 @@
 All buffers are allocated once, on the device, at construction; `run` only enqueues the
 library calls on the current stream and never synchronises, so it can be timed with CUDA
 events or captured into a CUDA graph. By default the step uses the two fused calls
-(dspark_schedule_pack, dspark_verify_scatter: three kernels greedy, four stochastic); with
-fused=False it issues the four single calls (five and six kernels). Both give identical
+(dspark_schedule_pack, dspark_verify_scatter: three kernels); with fused=False it issues the
+four single calls (five kernels). Both give identical
 results.
 """
 from __future__ import annotations
@@ -18,9 +18,9 @@ from . import _binding as bd
 
 
 def launches_per_step(gamma: int, stochastic: bool, fused: bool) -> int:
-    """Kernel launches of one step: schedule (+ pack), verify stream and finalize (+ the
-    stochastic bonus kernel), scatter unless fused."""
-    verify = 2 + (1 if stochastic else 0)
+    """Kernel launches of one step: schedule (+ pack), verify (the streaming kernel, then the
+    greedy finaliser or the stochastic bonus kernel), scatter unless fused."""
+    verify = 2
     if fused:
         return (1 if gamma > 1 else 2) + verify
     return 2 + verify + 1
@@ -135,29 +135,40 @@ class DSparkStep:
 
 
 class DSparkGraph:
-    """One decode step captured as a CUDA graph over fixed input buffers.
+    """One decode step captured as a CUDA graph over fixed input buffers, through the
+    library's own capture entry points (dspark_graph_begin / dspark_graph_end): replay() is one
+    dspark_graph_launch, a single cudaGraphLaunch from C.
 
     Every kernel sizes itself on the device (verify reads M from cu_seqlens), so a single
     graph serves every window allocation and every tier: replay() launches the whole step —
     schedule, pack, verify, scatter — with one call. New inputs are written into the same
     tensors (conf, block_tokens, target, draft) before a replay. The step's status word keeps
-    accumulating across replays until the caller zeroes it.
+    accumulating across replays until the caller zeroes it. `steps` > 1 captures that many
+    consecutive steps (Philox step counters step_index, step_index + 1, ...) in one graph.
     """
 
     def __init__(self, step: DSparkStep, conf, block_tokens, target, draft=None, *,
-                 temperature=1.0, seed=0, step_index=0, row_prob=None):
+                 temperature=1.0, seed=0, step_index=0, row_prob=None, steps=1):
         self.step = step
-        kw = dict(temperature=temperature, seed=seed, step=step_index, row_prob=row_prob)
+        kw = dict(temperature=temperature, seed=seed, row_prob=row_prob)
         # one eager run first: per-device set-up of the library happens outside the capture
-        for call in step.prepare(conf, block_tokens, target, draft, **kw):
+        for call in step.prepare(conf, block_tokens, target, draft, step=step_index, **kw):
             call()
         torch.cuda.synchronize()
-        self.graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(self.graph):
-            calls = step.prepare(conf, block_tokens, target, draft, **kw)
-            for call in calls:
-                call()
-        self._calls = calls
+        # capture on a side stream (the legacy default stream cannot be captured); the calls
+        # are prepared while it is current, so they are issued on it
+        capture = torch.cuda.Stream(device=step.device)
+        with torch.cuda.stream(capture):
+            self._calls = [step.prepare(conf, block_tokens, target, draft, step=step_index + k,
+                                        **kw) for k in range(steps)]
+            self.graph = bd.StepGraph(capture)
+            try:
+                for calls in self._calls:
+                    for call in calls:
+                        call()
+            finally:
+                self.graph.end()
+        self._replay = self.graph.prepare_launch()     # replays on the caller's stream
 
     def replay(self):
-        self.graph.replay()
+        self._replay()

@@ -34,7 +34,8 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_version(lib):
-    assert lib.dspark_version() == 100
+    # 1.1: the dspark_graph_* capture and replay calls
+    assert lib.dspark_version() == 101
 
 
 def test_argument_errors_are_reported_on_the_host(lib):

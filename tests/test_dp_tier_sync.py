@@ -1,9 +1,10 @@
 """DP tier agreement across ranks ("DSpark in SGLang", A2: under DP attention every rank replays
 the largest tier any rank needs and the ranks shrink together), on two gloo ranks on CPU.
 
-Each rank schedules its own requests with the oracle, packs, and agrees on the tier; the agreed
-tier must be the maximum of the ranks' own tiers at every step, identical on both ranks, and
-fall only when every rank's load falls."""
+Each rank schedules its own requests with the oracle and packs them; the ranks agree on the
+tier by an all-reduce(MAX) of meta[1] as the pack wrote it. The agreed tier must be the maximum
+of the ranks' own tiers at every step, identical on both ranks, fall only when every rank's load
+falls, and serve as the only tier of each rank's re-pack."""
 import os
 import socket
 
@@ -33,21 +34,26 @@ def _rank(rank, world, port, out):
     try:
         import oracle
         from speculative_decoding_ragged_gb300 import synth
-        from speculative_decoding_ragged_gb300.dp import TierSync, tier_for
+        from speculative_decoding_ragged_gb300.dp import TierSync
         wl = synth.WORKLOADS["high_load"].with_(B=64, V=64)
-        sync = TierSync(wl.tiers)
-        local = []
+        sync = TierSync()
+        local, agreed_hist = [], []
         for step, slope in enumerate(LOADS[rank]):
             bt = synth.make_batch(wl, seed=100 + rank, step=step, theta_slope=slope)
             w = oracle.schedule(bt.conf, bt.bias, bt.alpha, bt.theta)["windows"]
-            M = int(w.sum())
-            local.append(tier_for(M, wl.tiers))
-            agreed = sync.step(M)
+            pk = oracle.pack(w, bt.tokens, bt.tiers, int(max(bt.tiers)))
+            # meta = {M, tier} as the pack wrote it: the all-reduce runs on meta[1] in place
+            meta = torch.tensor([pk["M"], pk["tier"]], dtype=torch.int32)
+            local.append(pk["tier"])
+            tiers = sync.step(meta)
+            agreed = int(tiers.item())           # read by the test only
+            assert int(meta[1]) == agreed and int(meta[0]) == pk["M"]
+            agreed_hist.append(agreed)
             # re-pack with the agreed tier as the only tier: rows M..agreed are padding
-            pk = oracle.pack(w, bt.tokens, np.array([agreed], np.int32), agreed)
-            assert pk["tier"] == agreed and pk["status"] == 0
-            assert (pk["row_req"][M:agreed] == -1).all()
-        out[rank] = (local, sync.history)
+            re = oracle.pack(w, bt.tokens, tiers.numpy(), agreed)
+            assert re["tier"] == agreed and re["status"] == 0
+            assert (re["row_req"][pk["M"]:agreed] == -1).all()
+        out[rank] = (local, agreed_hist)
     finally:
         dist.destroy_process_group()
 
@@ -73,16 +79,23 @@ def test_two_ranks_agree_on_the_max_tier_and_shrink_together():
             assert local0[s] < agreed0[s - 1] and local1[s] < agreed0[s - 1]
 
 
-def test_tier_for_matches_pack_rounding():
-    from speculative_decoding_ragged_gb300.dp import tier_for
-    assert tier_for(8, [4, 8, 16]) == 8
-    assert tier_for(9, [16, 4, 12]) == 12
-    assert tier_for(40, [8, 16]) == 40
-
-
 def test_agree_tier_without_a_group_is_identity():
     from speculative_decoding_ragged_gb300.dp import agree_tier
     t = torch.tensor([96], dtype=torch.int32)
     assert int(agree_tier(t).item()) == 96
     with pytest.raises(ValueError):
         agree_tier(torch.tensor([1, 2], dtype=torch.int32))
+    with pytest.raises(ValueError):
+        agree_tier(torch.tensor([1], dtype=torch.int64))
+
+
+def test_tier_sync_writes_the_repack_tiers_without_a_group():
+    from speculative_decoding_ragged_gb300.dp import TierSync
+    sync = TierSync()
+    meta = torch.tensor([37, 64], dtype=torch.int32)
+    tiers = sync.step(meta)
+    assert tiers.dtype == torch.int32 and tiers.numel() == 1 and int(tiers) == 64
+    meta[1] = 0                              # the re-pack writes meta again: tiers stay put
+    assert int(tiers) == 64
+    with pytest.raises(ValueError):
+        sync.step(torch.tensor([1], dtype=torch.int32))

@@ -53,3 +53,78 @@ def test_graph_replay_matches_eager(dev, stochastic):
         Ms.add(int(graphed.windows.sum().item()))
     assert len(Ms) > 1          # the replays saw different packed totals
     assert int(graphed.status.item()) == int(eager.status.item())
+
+
+@pytest.mark.parametrize("mode", ["compact", "cap_accept"])
+@pytest.mark.parametrize("stochastic", [False, True])
+def test_graph_replay_matches_oracle_across_tiers(dev, mode, stochastic):
+    """The replayed step against the CPU oracle, step by step: windows, cu_seqlens, M and the
+    tier, accept lengths, committed tokens and the appended histories. The cost table's theta
+    changes between replays (the graph reads it from the same device buffer), so the packed
+    total and the tier change too; in compact mode the packed rows of the oracle's windows are
+    written into the captured logits buffer before each replay (the target forward's stand-in)."""
+    import oracle
+    from gpu_util import bits, compare_stochastic
+    wl = synth.WORKLOADS["stochastic"].with_(B=24, V=4096) if stochastic else \
+        synth.WORKLOADS["large_vocab_mixed"].with_(B=48, V=8192, tiers=tuple(range(48, 385, 48)))
+    B, g, V = wl.B, wl.gamma, wl.V
+    slopes = (0.001, 0.05, 0.004, 0.3, 0.0)
+    st = DSparkStep(B, g, V, wl.tiers, wl.bias, wl.alpha_slope * np.arange(B + 1),
+                    slopes[0] * np.arange(B * g + 1), mode=mode, stochastic=stochastic,
+                    out_cap=64, device=dev)
+    rows = st.packed_cap if mode == "compact" else B * g
+    conf = torch.zeros((B, g - 1), dtype=torch.float32, device=dev)
+    tokens = torch.zeros((B, g), dtype=torch.int32, device=dev)
+    target = torch.zeros((rows, V), dtype=torch.bfloat16, device=dev)
+    draft = torch.zeros((B * (g - 1), V), dtype=torch.bfloat16, device=dev) if stochastic else None
+    graph = DSparkGraph(st, conf, tokens, target, draft, seed=9, temperature=wl.temperature)
+    st.out_len.zero_()
+    st.out_tokens.fill_(-1)
+    st.status.zero_()
+    hist = np.full((B, 64), -1, np.int32)
+    hlen = np.zeros(B, np.int32)
+    tiers_seen, near = set(), 0
+    for k, slope in enumerate(slopes):
+        bt = synth.make_batch(wl, seed=40 + k, stochastic=stochastic, theta_slope=slope)
+        st.cost.theta.copy_(torch.as_tensor(bt.theta))
+        rs = oracle.schedule(bt.conf, bt.bias, bt.alpha, bt.theta)
+        w = rs["windows"]
+        rp = oracle.pack(w, bt.tokens, bt.tiers, st.packed_cap)
+        if mode == "compact":
+            tgt_host = synth.gather_packed(bt.target, B, g, w, rows_cap=rows)
+        else:
+            tgt_host = bt.target
+        conf.copy_(torch.as_tensor(bt.conf))
+        tokens.copy_(torch.as_tensor(bt.tokens))
+        target.copy_(tgt_host)
+        if stochastic:
+            draft.copy_(bt.draft)
+        graph.replay()
+        torch.cuda.synchronize()
+        rv = oracle.verify(oracle.COMPACT if mode == "compact" else oracle.CAP_ACCEPT,
+                           stochastic, bits(tgt_host), bt.tokens, cu=rp["cu"], windows=w,
+                           draft=bits(bt.draft) if stochastic else None,
+                           temperature=wl.temperature, seed=9, step=0)
+        np.testing.assert_array_equal(st.windows.cpu().numpy(), w)
+        assert int(st.k_star.item()) == rs["k_star"]
+        np.testing.assert_array_equal(st.cu.cpu().numpy(), rp["cu"])
+        np.testing.assert_array_equal(st.meta.cpu().numpy(), [rp["M"], rp["tier"]])
+        tiers_seen.add(rp["tier"])
+        got = dict(accept_len=st.accept_len.cpu().numpy(), committed=st.committed.cpu().numpy(),
+                   ceiling_len=st.ceiling.cpu().numpy(), status=rv["status"])
+        if stochastic:
+            got["row_prob"] = rv["row_prob"]          # the graph's step records none
+            n, _ = compare_stochastic(got, rv, rows_used=0)
+            near += n
+        else:
+            np.testing.assert_array_equal(got["accept_len"], rv["accept_len"])
+            np.testing.assert_array_equal(got["committed"], rv["committed"])
+        if mode == "cap_accept":
+            np.testing.assert_array_equal(got["ceiling_len"], rv["ceiling_len"])
+        sc = oracle.scatter(rv["committed"], rv["accept_len"], hist, hlen)
+        hist, hlen = sc["out_tokens"], sc["out_len"]
+    assert len(tiers_seen) >= 2, tiers_seen      # one captured graph served several tiers
+    if near == 0:
+        np.testing.assert_array_equal(st.out_len.cpu().numpy(), hlen)
+        np.testing.assert_array_equal(st.out_tokens.cpu().numpy(), hist)
+    assert int(st.status.item()) == 0

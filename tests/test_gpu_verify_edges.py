@@ -1,0 +1,191 @@
+"""Edge cases of verify against the oracle, with both streaming kernels: one workspace serving
+calls of every size and mode, requests whose rows the buffer does not hold (a short buffer, or
+none at all: bad rows, nothing committed, (-1, -1) on the rows the buffer does hold), rows before
+cu_seqlens[0], requests whose windows reach into the next request's rows, and batches of more
+than 4096 requests."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_decoding_ragged_gb300 import _binding as bd
+from speculative_decoding_ragged_gb300 import synth
+
+from gpu_util import MODE, bits, compare_stochastic, device, i32
+
+pytestmark = pytest.mark.gpu
+
+KERNELS = {"register": bd.STREAM_REGISTER, "bulk": bd.STREAM_BULK}
+
+
+@pytest.fixture(scope="module")
+def dev():
+    d = device()
+    yield d
+    bd.set_stream_kernel(bd.STREAM_AUTO)
+
+
+def run(dev, ws, mode, tgt, tokens, cu, windows, stochastic, draft=None, kernel="register",
+        **kw):
+    bd.set_stream_kernel(KERNELS[kernel])
+    try:
+        B, gamma = tokens.shape
+        rows = tgt.shape[0]
+        o = dict(accept_len=torch.full((B,), -7, dtype=torch.int32, device=dev),
+                 committed=torch.full((B, gamma), -7, dtype=torch.int32, device=dev),
+                 ceiling_len=torch.full((B,), -7, dtype=torch.int32, device=dev),
+                 row_prob=torch.full((max(rows, 1), 2), -7.0, dtype=torch.float32, device=dev),
+                 status=torch.zeros(1, dtype=torch.int32, device=dev))
+        # an empty buffer still needs a valid pointer: a one-row allocation passed with
+        # target_rows = 0 through the C ABI directly
+        tgt_d = tgt.to(dev) if rows else torch.zeros((1, tgt.shape[1]), dtype=tgt.dtype,
+                                                      device=dev)
+        args = list(bd._verify_args(
+            mode, tgt_d, i32(tokens, dev), o["accept_len"], o["committed"], ws, stochastic,
+            None if draft is None else draft.to(dev), None if cu is None else i32(cu, dev),
+            None if windows is None else i32(windows, dev), o["ceiling_len"], o["row_prob"],
+            kw.get("temperature", 1.0), kw.get("seed", 0), kw.get("step", 0)))
+        args[3] = rows
+        args += [bd._ptr(o["status"], "status"), bd._stream(None)]
+        bd._check("dspark_verify", bd.lib().dspark_verify(*args))
+        torch.cuda.synchronize()
+        out = {k: v.cpu().numpy() for k, v in o.items()}
+        out["status"] = int(out["status"][0])
+        out["row_prob"] = out["row_prob"][:rows]
+        return out
+    finally:
+        bd.set_stream_kernel(bd.STREAM_AUTO)
+
+
+def ref(mode, tgt, tokens, cu, windows, stochastic, draft=None, **kw):
+    return oracle.verify(MODE[mode], stochastic, bits(tgt), tokens, cu=cu, windows=windows,
+                         draft=None if draft is None else bits(draft), **kw)
+
+
+def check(g, r, stochastic, rows_used):
+    if stochastic:
+        near, _ = compare_stochastic(g, r, rows_used)
+        assert near == 0
+    else:
+        np.testing.assert_array_equal(g["accept_len"], r["accept_len"])
+        np.testing.assert_array_equal(g["committed"], r["committed"])
+        assert g["status"] == r["status"]
+    np.testing.assert_array_equal(g["ceiling_len"], r["ceiling_len"])
+
+
+@pytest.mark.parametrize("kernel", ["register", "bulk"])
+@pytest.mark.parametrize("stochastic", [False, True])
+def test_one_workspace_serves_calls_of_every_size_and_mode(dev, kernel, stochastic):
+    # the largest size's workspace, filled with garbage once, then calls of shrinking and
+    # growing sizes in every mode: each call rewrites what it reads
+    sizes = [(48, 8, 4096), (5, 6, 2056), (64, 4, 8192), (17, 8, 1024), (48, 8, 4096)]
+    need = max(bd.dspark_verify_workspace_bytes(B, g, V, stochastic) for B, g, V in sizes)
+    ws = torch.full((need,), 0xA5, dtype=torch.uint8, device=dev)
+    wl0 = synth.WORKLOADS["stochastic"] if stochastic else synth.WORKLOADS["large_vocab_mixed"]
+    for k, (B, g, V) in enumerate(sizes):
+        wl = wl0.with_(B=B, gamma=g, V=V, tiers=(B * g,))
+        bt = synth.make_batch(wl, seed=300 + k, stochastic=stochastic)
+        w = oracle.schedule(bt.conf, bt.bias, bt.alpha, bt.theta)["windows"]
+        cu = np.concatenate([[0], np.cumsum(w)]).astype(np.int32)
+        for mode in ("compact", "cap_accept", "static"):
+            tgt = synth.gather_packed(bt.target, B, g, w) if mode == "compact" else bt.target
+            win = None if mode == "static" else w
+            kw = dict(temperature=wl.temperature, seed=k, step=1) if stochastic else {}
+            gres = run(dev, ws, mode, tgt, bt.tokens, cu if mode == "compact" else None, win,
+                       stochastic, bt.draft if stochastic else None, kernel, **kw)
+            rres = ref(mode, tgt, bt.tokens, cu if mode == "compact" else None, win, stochastic,
+                       bt.draft if stochastic else None, **kw)
+            check(gres, rres, stochastic, tgt.shape[0])
+
+
+@pytest.mark.parametrize("kernel", ["register", "bulk"])
+@pytest.mark.parametrize("stochastic", [False, True])
+def test_requests_without_streamed_rows_are_still_finalised(dev, kernel, stochastic):
+    wl = (synth.WORKLOADS["stochastic"] if stochastic else synth.WORKLOADS["large_vocab_mixed"])
+    wl = wl.with_(B=12, V=2048, tiers=(96,))
+    bt = synth.make_batch(wl, seed=7, stochastic=stochastic)
+    B, g = bt.B, bt.gamma
+    w = oracle.schedule(bt.conf, bt.bias, bt.alpha, bt.theta)["windows"]
+    cu = np.concatenate([[0], np.cumsum(w)]).astype(np.int32)
+    packed = synth.gather_packed(bt.target, B, g, w)
+    kw = dict(temperature=1.0, seed=3, step=0) if stochastic else {}
+    drf = bt.draft if stochastic else None
+    ws = torch.zeros(bd.dspark_verify_workspace_bytes(B, g, wl.V, stochastic), dtype=torch.uint8,
+                     device=dev)
+    # the packed buffer cut to the first requests' rows: the later requests stream nothing
+    # (or only part of their rows) and must come out as bad rows, the earlier ones verified
+    for rows in (int(cu[B // 2]), int(cu[B // 2]) + 1, 0):
+        tgt = packed[:rows] if rows else packed[:0]
+        gres = run(dev, ws, "compact", tgt, bt.tokens, cu, w, stochastic, drf, kernel, **kw)
+        rres = ref("compact", tgt, bt.tokens, cu, w, stochastic, drf, **kw)
+        check(gres, rres, stochastic, rows)
+        assert gres["status"] & bd.STATUS_BAD_ROWS
+    # cap-accept with a block buffer short of the last requests' rows
+    tgt = bt.target[: (B - 3) * g + 2]
+    gres = run(dev, ws, "cap_accept", tgt, bt.tokens, None, w, stochastic, drf, kernel, **kw)
+    rres = ref("cap_accept", tgt, bt.tokens, None, w, stochastic, drf, **kw)
+    check(gres, rres, stochastic, tgt.shape[0])
+
+
+@pytest.mark.parametrize("kernel", ["register", "bulk"])
+def test_rows_before_the_first_request_are_skipped(dev, kernel):
+    wl = synth.WORKLOADS["large_vocab_mixed"].with_(B=9, V=1024, tiers=(80,))
+    bt = synth.make_batch(wl, seed=11)
+    B, g = bt.B, bt.gamma
+    # short windows (a steep theta): the rows with the leading gap still fit B * gamma rows
+    w = oracle.schedule(bt.conf, bt.bias, bt.alpha, 0.3 * np.arange(B * g + 1))["windows"]
+    lead = 5
+    assert lead + int(w.sum()) <= B * g
+    cu = (lead + np.concatenate([[0], np.cumsum(w)])).astype(np.int32)
+    body = synth.gather_packed(bt.target, B, g, w)
+    gap = torch.randn(lead, wl.V, generator=torch.Generator().manual_seed(1)).to(body.dtype)
+    tgt = torch.cat([gap, body])
+    ws = torch.zeros(bd.dspark_verify_workspace_bytes(B, g, wl.V, False), dtype=torch.uint8,
+                     device=dev)
+    gres = run(dev, ws, "compact", tgt, bt.tokens, cu, w, False, None, kernel)
+    rres = ref("compact", tgt, bt.tokens, cu, w, False)
+    check(gres, rres, False, tgt.shape[0])
+    assert gres["status"] == 0
+
+
+@pytest.mark.parametrize("kernel", ["register", "bulk"])
+@pytest.mark.parametrize("stochastic", [False, True])
+def test_a_window_reaching_into_the_next_request(dev, kernel, stochastic):
+    # request 3's window claims a row that cu_seqlens gives to request 4: every request reads
+    # its rows from cu_seqlens[b] on, as the oracle does (row_prob is not compared: the shared
+    # row holds either request's values, and the row after request 4 belongs to no request)
+    wl = (synth.WORKLOADS["stochastic"] if stochastic else synth.WORKLOADS["large_vocab_mixed"])
+    wl = wl.with_(B=8, V=2048, tiers=(64,))
+    bt = synth.make_batch(wl, seed=5, stochastic=stochastic)
+    B, g = bt.B, bt.gamma
+    w = oracle.schedule(bt.conf, bt.bias, bt.alpha, 0.0 * bt.theta)["windows"]   # all gamma
+    cu = np.concatenate([[0], np.cumsum(w)]).astype(np.int32)
+    cu_bad = cu.copy()
+    cu_bad[4] -= 1
+    tgt = synth.gather_packed(bt.target, B, g, w)
+    drf = bt.draft if stochastic else None
+    kw = dict(temperature=1.0, seed=2, step=4) if stochastic else {}
+    ws = torch.zeros(bd.dspark_verify_workspace_bytes(B, g, wl.V, stochastic), dtype=torch.uint8,
+                     device=dev)
+    gres = run(dev, ws, "compact", tgt, bt.tokens, cu_bad, w, stochastic, drf, kernel, **kw)
+    rres = ref("compact", tgt, bt.tokens, cu_bad, w, stochastic, drf, **kw)
+    check(gres, rres, stochastic, 0)
+
+
+@pytest.mark.parametrize("stochastic", [False, True])
+def test_more_than_4096_requests(dev, stochastic):
+    wl = (synth.WORKLOADS["stochastic"] if stochastic else synth.WORKLOADS["large_vocab_mixed"])
+    wl = wl.with_(B=4099, gamma=3, V=64, tiers=(3 * 4099,))
+    bt = synth.make_batch(wl, seed=21, stochastic=stochastic)
+    B, g = bt.B, bt.gamma
+    w = oracle.schedule(bt.conf, bt.bias, bt.alpha, bt.theta)["windows"]
+    cu = np.concatenate([[0], np.cumsum(w)]).astype(np.int32)
+    tgt = synth.gather_packed(bt.target, B, g, w)
+    drf = bt.draft if stochastic else None
+    kw = dict(temperature=1.0, seed=8, step=2) if stochastic else {}
+    ws = torch.zeros(bd.dspark_verify_workspace_bytes(B, g, wl.V, stochastic), dtype=torch.uint8,
+                     device=dev)
+    for kernel in ("register", "bulk"):
+        gres = run(dev, ws, "compact", tgt, bt.tokens, cu, w, stochastic, drf, kernel, **kw)
+        rres = ref("compact", tgt, bt.tokens, cu, w, stochastic, drf, **kw)
+        check(gres, rres, stochastic, tgt.shape[0])
