@@ -585,18 +585,45 @@ def run_native(args, rank, world, local):
     return out
 
 
+def host_and_device_us(fn, n, stream):
+    """(host submission us, device us) per call of fn: the host's time to enqueue n calls while
+    a sleep kernel holds the GPU (so no launch waits on the GPU), and the GPU's time for the n
+    calls back to back once the sleep ends (events after it)."""
+    for i in range(64):
+        fn(i)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(n):
+        fn(i)
+    rough = (time.perf_counter() - t0) / n
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(int(2.07e9 * (rough * n * 1.5 + 2e-3)))    # cycles at the maximum clock
+    t0 = time.perf_counter()
+    e0.record(stream)
+    for i in range(n):
+        fn(i)
+    e1.record(stream)
+    host = (time.perf_counter() - t0) / n * 1e6
+    torch.cuda.synchronize()
+    return host, e0.elapsed_time(e1) * 1e3 / n
+
+
 def latency_leg(dev, steps, pool=64):
     """Per-step time of the batch-1 workload (B=1, gamma=16, V=129280 bf16, compact), greedy
-    and stochastic (T = 0.7): `steps` consecutive steps cycling through `pool` seeded inputs
-    (the pool's logits exceed L2), launched eagerly (the fused calls through ctypes), as one
-    CUDA graph replay per step (dspark_graph_launch), and as one graph holding a whole pool
-    cycle (the GPU-side step time). Host submission time per step is reported beside each: a
-    mode whose host time is at or above its step time is bound by the submitting thread."""
+    and stochastic (T = 0.7), `steps` consecutive steps cycling through `pool` seeded inputs
+    (the pool's logits exceed L2): launched eagerly (the fused calls through ctypes) and as one
+    graph holding a whole pool cycle (the GPU-side step time). Beside them, host submission
+    and device time per step of each way to issue a step (host_and_device_us): eager, one
+    graph per pool entry (rotating), and one graph on fixed buffers replayed every step (how a
+    serving loop replays: new inputs land in the captured buffers; its logits stay in L2 at
+    this size, as do those of the eager step on the same buffers beside it)."""
     from speculative_decoding_ragged_gb300 import _binding as bd
     from speculative_decoding_ragged_gb300 import synth
     from speculative_decoding_ragged_gb300.step import DSparkGraph, DSparkStep
     wl = synth.WORKLOADS["latency_b1"]
     out = {"steps": steps, "pool_blocks": pool}
+    stream = torch.cuda.current_stream()
     for stochastic in (False, True):
         st = DSparkStep(wl.B, wl.gamma, wl.V, wl.tiers, wl.bias, wl.alpha_slope * np.arange(2),
                         wl.theta_slope * np.arange(wl.gamma + 1), out_cap=16,
@@ -623,32 +650,44 @@ def latency_leg(dev, steps, pool=64):
                     c()
             cycle.end()
         cycle_launch = cycle.prepare_launch()
-        stream = torch.cuda.current_stream()
         name = "stochastic" if stochastic else "greedy"
         out[f"{name}_launches_per_step"] = st.launches_per_step
-        for mode in ("eager", "graph", "graph_cycle"):
-            def one(i):
-                if mode == "eager":
-                    for c in calls[i % pool]:
-                        c()
-                elif mode == "graph":
-                    graphs[i % pool].replay()
-                elif i % pool == 0:
-                    cycle_launch()
-            n = steps - steps % pool
+
+        def eager(i):
+            for c in calls[i % pool]:
+                c()
+
+        def eager_static(i):
+            for c in calls[0]:
+                c()
+
+        def cycle_step(i):
+            if i % pool == 0:
+                cycle_launch()
+
+        # the consecutive-step timings of the workload: wall time per step on the device
+        n = steps - steps % pool
+        for mode, fn in (("eager", eager), ("graph_cycle", cycle_step)):
             for i in range(2 * pool):
-                one(i)
+                fn(i)
             torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            t0 = time.perf_counter()
             e0.record(stream)
             for i in range(n):
-                one(i)
+                fn(i)
             e1.record(stream)
-            t1 = time.perf_counter()
             torch.cuda.synchronize()
             out[f"{name}_step_us_{mode}"] = e0.elapsed_time(e1) * 1e3 / n
-            out[f"{name}_host_submit_us_{mode}"] = (t1 - t0) * 1e6 / n
+        # host submission against device time, each way of issuing a step
+        # (eager: 128 steps, 384 launches, stay under the launch queue's depth while the GPU
+        # is held; more would block the host and count the GPU's time as the host's)
+        for mode, fn, reps in (("eager", eager, 128), ("eager_static", eager_static, 128),
+                               ("graph_rotating", lambda i: graphs[i % pool].replay(), 384),
+                               ("graph_static", lambda i: graphs[0].replay(), 384),
+                               ("graph_cycle", lambda i: cycle_launch(), 16)):
+            host, devus = host_and_device_us(fn, reps, stream)
+            per = pool if mode == "graph_cycle" else 1
+            out[f"{name}_{mode}"] = {"host_us": host / per, "device_us": devus / per}
         out["pool_mb"] = round(sum(sum(t.numel() * t.element_size() for t in e[2:] if t is not None)
                                    for e in entries) / 1e6, 1)
         del graphs, cycle, cycle_launch, cycle_calls, calls, entries

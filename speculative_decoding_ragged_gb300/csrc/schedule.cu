@@ -360,9 +360,12 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
     __shared__ int warp_int[kWarps];
     __shared__ int tier_s;
 
+    // Step 1 reads only call inputs that no kernel of this library writes (confidences, the
+    // cost tables, block tokens) and writes only shared memory, so it runs before the wait for
+    // the previous kernel on the stream; tiers (a caller may hand in a tier that a pack wrote)
+    // and every global write come after it.
     prefetch_inputs(threadIdx.x, kThreads, conf, B, L, alpha, theta, PACK ? pk.tokens : nullptr,
                     PACK ? pk.tiers : nullptr, PACK ? pk.n_tiers : 0);
-    pdl_wait_and_trigger();
     const unsigned full = 0xffffffffu;
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -370,9 +373,8 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
     int tier_pre = INT_MAX;
     int* tok_stage = nullptr;
     if (PACK) {
-        // the pack's inputs are read only at the end: its tier now, and its tokens copied into
-        // shared memory (cp.async, 16-byte pieces) while the scheduler works, when they fit
-        if (tid < pk.n_tiers) tier_pre = __ldg(pk.tiers + tid);
+        // the pack's tokens are read only at the end: copied into shared memory (cp.async,
+        // 16-byte pieces) while the scheduler works, when they fit
         if (tid == 0) tier_s = INT_MAX;
         if (tok_stage_off >= 0) {
             tok_stage = reinterpret_cast<int*>(smem_raw + tok_stage_off);
@@ -418,6 +420,8 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
     }
     if (!MERGE)
         for (int i = n + tid; i < n_pad; i += kThreads) word[i] = 0;   // sorts after all words
+    pdl_wait_and_trigger();
+    if (PACK && tid < pk.n_tiers) tier_pre = __ldg(pk.tiers + tid);
     __syncthreads();
 
     // 2. sort descending. MERGE also yields rank_of[i]: the sorted position of candidate i
@@ -772,7 +776,6 @@ schedule_small_kernel(const float* __restrict__ conf, int B, int L, double bias,
     __shared__ int cu_s[kSmallMax];
     prefetch_inputs(threadIdx.x, 32, conf, B, L, alpha, theta, PACK ? pk.tokens : nullptr,
                     PACK ? pk.tiers : nullptr, PACK ? pk.n_tiers : 0);
-    pdl_wait_and_trigger();
     const unsigned full = 0xffffffffu;
     const int lane = threadIdx.x;
     const int n = B * L;
@@ -789,6 +792,13 @@ schedule_small_kernel(const float* __restrict__ conf, int B, int L, double bias,
     const uint64_t th_k = mine ? __ldg(theta_bits + B + lane + 1) : 0;
     const uint64_t th_0 = __ldg(theta_bits + B);
     const double t0 = bias + __ldg(alpha + B);
+    // the pack's block tokens, B * gamma <= 64 of them: lane l holds tokens l and l + 32
+    const int nt = B * gamma;
+    const int tok_lo = (PACK && lane < nt) ? __ldg(pk.tokens + lane) : 0;
+    const int tok_hi = (PACK && lane + 32 < nt) ? __ldg(pk.tokens + lane + 32) : 0;
+    // everything above reads call inputs that no kernel of this library writes; outputs and
+    // the tiers (which a pack of this library may have written) wait for the previous kernel
+    pdl_wait_and_trigger();
 
     // 1. survival key and rank word of the lane's candidate
     float sv = 1.0f;
@@ -898,13 +908,19 @@ schedule_small_kernel(const float* __restrict__ conf, int B, int L, double bias,
         if (tier > pk.packed_cap) bits |= DSPARK_STATUS_PACK_CAPACITY;
         __syncwarp();
         const int rows = min(M, pk.packed_cap);
-        for (int r = lane; r < rows; r += 32) {
+        for (int r0 = 0; r0 < rows; r0 += 32) {          // uniform trip count: shuffles inside
+            const int r = r0 + lane;
             int b = 0;
-            while (b + 1 < B && cu_s[b + 1] <= r) ++b;
+            while (b + 1 < B && r < rows && cu_s[b + 1] <= r) ++b;
             const int i = r - cu_s[b];
-            pk.packed_ids[r] = __ldg(pk.tokens + static_cast<int64_t>(b) * gamma + i);
-            if (pk.row_req) pk.row_req[r] = b;
-            if (pk.row_pos) pk.row_pos[r] = i;
+            const int q = b * gamma + i;                  // < B * gamma <= 64 for rows < M
+            const int t_lo = __shfl_sync(full, tok_lo, q & 31);
+            const int t_hi = __shfl_sync(full, tok_hi, q & 31);
+            if (r < rows) {
+                pk.packed_ids[r] = q < 32 ? t_lo : t_hi;
+                if (pk.row_req) pk.row_req[r] = b;
+                if (pk.row_pos) pk.row_pos[r] = i;
+            }
         }
         const int rows_pad = min(tier, pk.packed_cap);
         for (int r = M + lane; r < rows_pad; r += 32) {

@@ -763,15 +763,17 @@ bonus_final_kernel(FinalArgs A, int ctas_per_request)
             sums[2 * t + 1] = sp;
         }
     }
-    // the request's last CTA to finish draws the token: each lane that wrote tile sums
-    // publishes them at device scope, then one thread counts the CTA done; the pick reads the
-    // sums from L2 (ld.global.cg)
+    // the request's last CTA to finish draws the token: after the CTA barrier, one thread
+    // counts the CTA done with an acquire-release add at device scope (its release covers the
+    // tile sums every warp of the CTA stored before the barrier; its acquire, in the last CTA,
+    // every other CTA's); the pick reads the sums from L2 (ld.global.cg)
     __shared__ bool last_s;
-    if (lane == 0) __threadfence();
     __syncthreads();
     if (tid == 0) {
-        last_s = atomicAdd(A.done + b, 1u) == static_cast<unsigned>(ctas_per_request) - 1;
-        if (last_s) __threadfence();
+        unsigned old;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old)
+                     : "l"(A.done + b) : "memory");
+        last_s = old == static_cast<unsigned>(ctas_per_request) - 1;
     }
     __syncthreads();
     if (!last_s) return;

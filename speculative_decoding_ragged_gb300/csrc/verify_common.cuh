@@ -210,7 +210,8 @@ struct UnitSrc {
 };
 
 template <int E>
-__device__ __forceinline__ UnitSrc unit_source(const StreamArgs& A, int64_t job, int c, int64_t n_t)
+__device__ __forceinline__ UnitSrc unit_source(const StreamArgs& A, int64_t job, int c, int64_t n_t,
+                                               const int32_t* cu, const int32_t* windows)
 {
     UnitSrc s;
     s.c = c;
@@ -230,11 +231,11 @@ __device__ __forceinline__ UnitSrc unit_source(const StreamArgs& A, int64_t job,
         int lo = 0, hi = A.B;                    // largest b with cu[b] <= r
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
-            if (A.cu[mid] <= r) lo = mid; else hi = mid;
+            if (cu[mid] <= r) lo = mid; else hi = mid;
         }
         b = lo;
-        i = static_cast<int>(r - A.cu[b]);
-        int w = A.windows[b];
+        i = static_cast<int>(r - cu[b]);
+        int w = windows[b];
         w = w < 1 ? 1 : (w > A.gamma ? A.gamma : w);
         if (i < 0 || i >= w - 1 || i >= L) {     // last row of a request: no draft
             s.skip = true;
@@ -255,9 +256,9 @@ __device__ __forceinline__ UnitSrc unit_source(const StreamArgs& A, int64_t job,
 
 // Units this call streams: target rows, then (stochastic) the draft jobs.
 template <bool STOCH>
-__device__ __forceinline__ int64_t unit_count(const StreamArgs& A, int64_t& n_t)
+__device__ __forceinline__ int64_t unit_count(const StreamArgs& A, int64_t& n_t, const int32_t* cu)
 {
-    n_t = target_row_count(A.mode, A.cu, A.B, A.gamma, A.target_rows, A.rows_max);
+    n_t = target_row_count(A.mode, cu, A.B, A.gamma, A.target_rows, A.rows_max);
     int64_t n_d = 0;
     if (STOCH) n_d = (A.mode == DSPARK_COMPACT) ? n_t : static_cast<int64_t>(A.B) * (A.gamma - 1);
     return (n_t + n_d) * A.nc;

@@ -63,24 +63,40 @@ __device__ __forceinline__ void chunk_lane(const char* row, int v0, int v1, int 
 
 // Register-streaming variant: any alignment (scalar loads when the rows are not 16-byte
 // aligned or V % 8 != 0).
+// Compact batches of fewer requests than this keep cu_seqlens (and the windows) in shared
+// memory, so a draft job's owner search costs shared-memory latency, not L2 round trips.
+constexpr int kCuCache = 1024;
+
 template <int DT, bool STOCH>
 __global__ void __launch_bounds__(kStreamThreads)
 verify_stream_kernel(StreamArgs A)
 {
     constexpr int E = (DT == DSPARK_BF16) ? 2 : 4;
+    __shared__ int32_t cu_s[kCuCache];
+    __shared__ int32_t w_s[STOCH ? kCuCache : 1];
     pdl_wait_and_trigger();
     zero_next_counters(A);
+    const int32_t* cu = A.cu;
+    const int32_t* windows = A.windows;
+    if (A.mode == DSPARK_COMPACT && A.B < kCuCache) {      // uniform over the CTA
+        for (int i = threadIdx.x; i <= A.B; i += kStreamThreads) cu_s[i] = A.cu[i];
+        if (STOCH)
+            for (int i = threadIdx.x; i < A.B; i += kStreamThreads) w_s[i] = A.windows[i];
+        __syncthreads();
+        cu = cu_s;
+        if (STOCH) windows = w_s;
+    }
     const int lane = threadIdx.x & 31;
     const int64_t gw = static_cast<int64_t>(blockIdx.x) * kStreamWarps + (threadIdx.x >> 5);
     const int64_t GW = static_cast<int64_t>(gridDim.x) * kStreamWarps;
     int64_t n_t;
-    const int64_t U = unit_count<STOCH>(A, n_t);
+    const int64_t U = unit_count<STOCH>(A, n_t, cu);
     const int64_t u0 = gw * U / GW, u1 = (gw + 1) * U / GW;
 
     int64_t job = u0 / A.nc;
     int c = static_cast<int>(u0 - job * A.nc);
     for (int64_t u = u0; u < u1; ++u) {
-        const UnitSrc src = unit_source<E>(A, job, c, n_t);
+        const UnitSrc src = unit_source<E>(A, job, c, n_t, cu, windows);
         if (++c == A.nc) { c = 0; ++job; }
         if (src.skip) continue;
         const int v0 = src.c * A.C;
@@ -235,7 +251,7 @@ verify_bulk_kernel(StreamArgs A, int stages, int stage_bytes)
     pdl_wait_and_trigger();
     zero_next_counters(A);
     int64_t n_t;
-    const int64_t U = unit_count<STOCH>(A, n_t);
+    const int64_t U = unit_count<STOCH>(A, n_t, A.cu);
     const int64_t u0 = static_cast<int64_t>(blockIdx.x) * U / gridDim.x;
     const int64_t u1 = static_cast<int64_t>(blockIdx.x + 1) * U / gridDim.x;
     const int64_t K = u1 - u0;
@@ -290,7 +306,7 @@ verify_bulk_kernel(StreamArgs A, int stages, int stage_bytes)
             if (lane == 0) raise_status(A.status, DSPARK_STATUS_STALL);
             break;
         }
-        const UnitSrc src = unit_source<E>(A, job, c, n_t);
+        const UnitSrc src = unit_source<E>(A, job, c, n_t, A.cu, A.windows);
         float a = -INFINITY, bsum = 0.0f;
         int idx = 0x7FFFFFFF;
         if (!src.skip) {
