@@ -51,6 +51,7 @@ WORKLOAD = "large_vocab_mixed"
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "verify_stream_traffic.json")
 N_BATCHES = 3
+CHAINED_CALLS = 256      # back-to-back calls per chained timing in each workload leg
 
 
 def parse():
@@ -313,7 +314,8 @@ def run_leg(timer, name, wl, bt, mode, stochastic, dev, reps, target_full, draft
     steps. `batches` (the headline's) rotate instead of one batch when given."""
     from speculative_decoding_ragged_gb300 import synth
     B, g = wl.B, wl.gamma
-    st = step_for(wl, bt, mode, stochastic, dev, out_cap=4 * g)
+    # histories deep enough for every call of a chained timing (64 + 2 * CHAINED_CALLS)
+    st = step_for(wl, bt, mode, stochastic, dev, out_cap=g * 3 * CHAINED_CALLS)
     kw = dict(temperature=wl.temperature, seed=5, step=0)
     entries = []
     for b in (batches or [None]):
@@ -361,6 +363,21 @@ def run_leg(timer, name, wl, bt, mode, stochastic, dev, reps, target_full, draft
             c()
     step_us, _ = timer.run(whole, reps, pre=reset, stream_events=False)
     torch.cuda.synchronize()
+    # the same calls back to back, as a serving loop issues them (host held ahead of the GPU):
+    # device time per call of schedule-and-pack, of verify on the first batch's windows, and of
+    # whole steps with the batches rotating; inputs stay in L2 when they fit (below 129 MB)
+    stream = torch.cuda.current_stream()
+    chained = {}
+    st.out_len.zero_()
+    chained["sched_pack_us"] = host_and_device_us(lambda i: sched[i % n](), CHAINED_CALLS,
+                                                  stream)[1]
+    sched[0]()
+    st.out_len.zero_()
+    chained["verify_us"] = host_and_device_us(lambda i: verify[0](), CHAINED_CALLS, stream)[1]
+    st.out_len.zero_()
+    chained["step_us"] = host_and_device_us(lambda i: whole(), CHAINED_CALLS // 2, stream)[1]
+    st.out_len.zero_()
+    torch.cuda.synchronize()
     Ms = [e["M"] for e in entries]
     M = statistics.mean(Ms)
     rows_t = M if mode == "compact" else B * g
@@ -377,7 +394,7 @@ def run_leg(timer, name, wl, bt, mode, stochastic, dev, reps, target_full, draft
         bonus = int(np.sum(np.where(acc < entries[-1]["w"], 2, 1)))
     ex = {"launches_per_call": st.launches_per_step - (1 if g > 1 else 2),
           "launches_per_step": st.launches_per_step, "reps": len(call_us),
-          "batches_rotating": n, "status": int(st.status.item())}
+          "batches_rotating": n, "status": int(st.status.item()), "chained": chained}
     if extra:
         ex.update(extra)
     return leg_record(name, wl, mode, stochastic, M, rows_t, rows_d, bonus, call_us, stream_us,
