@@ -33,12 +33,17 @@
 namespace dspark {
 namespace {
 
-constexpr int kThreads = 1024;
+#ifndef DSPARK_SCHED_THREADS
+#define DSPARK_SCHED_THREADS 1024
+#endif
+constexpr int kThreads = DSPARK_SCHED_THREADS;   // the block kernel's CTA: 512 or 1024
+static_assert(kThreads == 512 || kThreads == 1024, "the block scheduler runs 512 or 1024 threads");
 constexpr int kWarps = kThreads / 32;
 constexpr int kMergeMax = 4096;          // ping-pong merge buffers up to this many words
 constexpr int kMergeItems = kMergeMax / kThreads;
 constexpr int kBuckets = 4096;           // 128 buckets per power of two of the key (keys 0, 1 share)
-constexpr int kBucketsPerThread = kBuckets / 1024;
+constexpr int kBucketsPerThread = kBuckets / kThreads;
+constexpr int kTiersPerThread = (DSPARK_MAX_TIERS + kThreads - 1) / kThreads;
 constexpr int kBucketMax = 64;           // larger buckets (many equal keys): merge instead
 constexpr float kScreen = 1.0f - 1e-5f;  // fp32 screen: candidates within 1e-5 of the best
 constexpr float kTmin = 1e-20f, kTmax = 1e20f;   // T range the fp32 screen judges
@@ -165,17 +170,20 @@ __device__ __forceinline__ uint32_t lanemask_lt()
     return m;
 }
 
-// Element i of a four-entry register array, by selects (no local memory under a rolled loop).
-__device__ __forceinline__ float get4(const float (&a)[4], int i)
+// Element i of a small register array, by selects (no local memory under a rolled loop).
+template <typename T, int N>
+__device__ __forceinline__ T get_n(const T (&a)[N], int i)
 {
-    return i == 0 ? a[0] : i == 1 ? a[1] : i == 2 ? a[2] : a[3];
+    T v = a[0];
+#pragma unroll
+    for (int k = 1; k < N; ++k) v = i == k ? a[k] : v;
+    return v;
 }
-__device__ __forceinline__ void set4(float (&a)[4], int i, float v)
+template <typename T, int N>
+__device__ __forceinline__ void set_n(T (&a)[N], int i, T v)
 {
-    a[0] = i == 0 ? v : a[0];
-    a[1] = i == 1 ? v : a[1];
-    a[2] = i == 2 ? v : a[2];
-    a[3] = i == 3 ? v : a[3];
+#pragma unroll
+    for (int k = 0; k < N; ++k) a[k] = i == k ? v : a[k];
 }
 
 // Sum over the warps before this one of a per-warp total, read by every lane of the warp from
@@ -200,7 +208,8 @@ __device__ __forceinline__ T warps_before(const T* total, int warp, int lane)
 // keeps each thread's windows for the pass after it.
 template <typename WinFn>
 __device__ __forceinline__ void pack_after_schedule(WinFn win, int B, int gamma, int K_star,
-                                                    PackArgs pk, int tier_pre,
+                                                    PackArgs pk,
+                                                    const int (&tier_pre)[kTiersPerThread],
                                                     const int* tok_stage, int* owner,
                                                     int* tier_s, int* pack_total, int* win_s,
                                                     int32_t* __restrict__ windows,
@@ -220,9 +229,13 @@ __device__ __forceinline__ void pack_after_schedule(WinFn win, int B, int gamma,
     const int warp = tid >> 5;
     const int M = B + K_star;
 
-    // tier: the smallest tier >= M (tier_pre is INT_MAX past n_tiers); warps without tiers skip
+    // tier: the smallest tier >= M (tier_pre: the thread's tiers, INT_MAX past n_tiers);
+    // warps without tiers skip
     if (warp * 32 < pk.n_tiers) {
-        int best = tier_pre >= M ? tier_pre : INT_MAX;
+        int best = INT_MAX;
+#pragma unroll
+        for (int k = 0; k < kTiersPerThread; ++k)
+            if (tier_pre[k] >= M && tier_pre[k] < best) best = tier_pre[k];
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) best = min(best, __shfl_xor_sync(full, best, off));
         if (lane == 0 && best != INT_MAX) atomicMin(tier_s, best);
@@ -370,7 +383,9 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
-    int tier_pre = INT_MAX;
+    int tier_pre[kTiersPerThread];
+#pragma unroll
+    for (int k = 0; k < kTiersPerThread; ++k) tier_pre[k] = INT_MAX;
     int* tok_stage = nullptr;
     if (PACK) {
         // the pack's tokens are read only at the end: copied into shared memory (cp.async,
@@ -421,7 +436,11 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
     if (!MERGE)
         for (int i = n + tid; i < n_pad; i += kThreads) word[i] = 0;   // sorts after all words
     pdl_wait_and_trigger();
-    if (PACK && tid < pk.n_tiers) tier_pre = __ldg(pk.tiers + tid);
+    if (PACK) {
+#pragma unroll
+        for (int k = 0; k < kTiersPerThread; ++k)
+            if (tid + k * kThreads < pk.n_tiers) tier_pre[k] = __ldg(pk.tiers + tid + k * kThreads);
+    }
     __syncthreads();
 
     // 2. sort descending. MERGE also yields rank_of[i]: the sorted position of candidate i
@@ -433,13 +452,27 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
         for (int p = tid; p < n; p += kThreads) atomicAdd(&bucket_cnt[key_bucket(ksrc[p])], 1);
         __syncthreads();
         // bucket starts in descending bucket order; thread t owns the reversed buckets
-        // kBuckets - 1 - (kBucketsPerThread * t + m), m = 0..kBucketsPerThread-1
-        static_assert(kBucketsPerThread == 4, "one 16-byte vector of counts per thread");
-        const int jv = kBuckets - 4 - 4 * tid;            // the thread's four buckets
-        const int4 cv = *reinterpret_cast<const int4*>(bucket_cnt + jv);
-        const int a[4] = {cv.w, cv.z, cv.y, cv.x};        // descending bucket order
-        const int own = (cv.x + cv.y) + (cv.z + cv.w);
-        const int big = max(max(cv.x, cv.y), max(cv.z, cv.w)) > kBucketMax;
+        // kBuckets - 1 - (kBucketsPerThread * t + m), m = 0..kBucketsPerThread-1, read and
+        // written as 16-byte vectors of four counts
+        constexpr int BPT = kBucketsPerThread;
+        static_assert(BPT % 4 == 0, "whole 16-byte vectors of counts per thread");
+        const int jv = kBuckets - BPT - BPT * tid;        // the thread's buckets [jv, jv + BPT)
+        int a[BPT];                                       // descending bucket order
+#pragma unroll
+        for (int v = 0; v < BPT / 4; ++v) {
+            const int4 cv = *reinterpret_cast<const int4*>(bucket_cnt + jv + 4 * v);
+            a[BPT - 1 - 4 * v] = cv.x;
+            a[BPT - 2 - 4 * v] = cv.y;
+            a[BPT - 3 - 4 * v] = cv.z;
+            a[BPT - 4 - 4 * v] = cv.w;
+        }
+        int own = 0, mx = 0;
+#pragma unroll
+        for (int m = 0; m < BPT; ++m) {
+            own += a[m];
+            mx = max(mx, a[m]);
+        }
+        const int big = mx > kBucketMax;
         int incl_b = own;
         for (int off = 1; off < 32; off <<= 1) {
             const int v = __shfl_up_sync(full, incl_b, off);
@@ -448,8 +481,18 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
         if (lane == 31) warp_int[warp] = incl_b;
         if (!__syncthreads_or(big)) {
             const int ex = incl_b - own + warps_before(warp_int, warp, lane);
-            *reinterpret_cast<int4*>(bucket_start + jv) =
-                make_int4(ex + a[0] + a[1] + a[2], ex + a[0] + a[1], ex + a[0], ex);
+            int st[BPT];                                  // start of the m-th bucket, descending
+            int acc = ex;
+#pragma unroll
+            for (int m = 0; m < BPT; ++m) {
+                st[m] = acc;
+                acc += a[m];
+            }
+#pragma unroll
+            for (int v = 0; v < BPT / 4; ++v)
+                *reinterpret_cast<int4*>(bucket_start + jv + 4 * v) =
+                    make_int4(st[BPT - 1 - 4 * v], st[BPT - 2 - 4 * v], st[BPT - 3 - 4 * v],
+                              st[BPT - 4 - 4 * v]);
             __syncthreads();
             // scatter rank words into the bucket ranges (any order inside a bucket); afterwards
             // bucket_start[j] holds the end of bucket j
@@ -542,8 +585,7 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
     };
     auto theta_at = [&](int it, int p) -> uint64_t {
         if (!MERGE) return __ldg(theta_bits + B + p + 1);
-        static_assert(kMergeItems == 4, "select chain over the thread's theta entries");
-        return it == 0 ? th[0] : it == 1 ? th[1] : it == 2 ? th[2] : th[3];
+        return get_n(th, it);
     };
 
     // 3. inclusive scan of keys over each thread's contiguous positions
@@ -570,7 +612,9 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
     // 4a. fp32 screen over the K this thread owns. MERGE keeps each K's screen value for the
     // exact pass (+inf where the screen cannot judge, so that K is always evaluated exactly)
     float fb = -INFINITY;
-    float fv[kMergeItems] = {0.0f, 0.0f, 0.0f, 0.0f};
+    float fv[kMergeItems];
+#pragma unroll
+    for (int k = 0; k < kMergeItems; ++k) fv[k] = 0.0f;
     float f_k0 = -INFINITY;
     float f_hi = -INFINITY;      // the largest of this thread's screen values (+inf included)
     if (tid == 0) {
@@ -591,13 +635,13 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
             const bool no = screen(base_E + S, t0f, t0_ok, theta_at(it, p), f);
             if (!no) fb = fmaxf(fb, f);
             f_hi = fmaxf(f_hi, no ? INFINITY : f);
-            if (MERGE) set4(fv, it, no ? INFINITY : f);
+            if (MERGE) set_n(fv, it, no ? INFINITY : f);
         }
     }
     for (int off = 16; off > 0; off >>= 1) fb = fmaxf(fb, __shfl_xor_sync(full, fb, off));
     if (lane == 0) red_f[warp] = fb;
     __syncthreads();
-    float f_best = red_f[lane];
+    float f_best = lane < kWarps ? red_f[lane] : -INFINITY;
     for (int off = 16; off > 0; off >>= 1) f_best = fmaxf(f_best, __shfl_xor_sync(full, f_best, off));
     const float thr = f_best * kScreen;
 
@@ -644,7 +688,7 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
                 S += key_at(p);
                 tb = theta_at(it, p);
                 if (MERGE) {
-                    cand = get4(fv, it) >= thr;
+                    cand = get_n(fv, it) >= thr;
                 } else {
                     float f = 0.0f;
                     cand = screen(base_E + S, t0f, t0_ok, tb, f) || f >= thr;
@@ -683,8 +727,8 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
                 red_k[warp] = best_k;
             }
             __syncthreads();
-            best_obj = red_obj[lane];
-            best_k = red_k[lane];
+            best_obj = lane < kWarps ? red_obj[lane] : 0;
+            best_k = lane < kWarps ? red_k[lane] : -1;
         }
         const unsigned vm = __ballot_sync(full, best_k >= 0);
         if (__popc(vm) > 1) {
