@@ -25,13 +25,16 @@
  *     two's complement; "bf16" is IEEE bfloat16 stored in 16 bits.
  *   - B = number of requests, gamma = block width (1 anchor + gamma-1 drafts), V = vocabulary.
  *   - All work is enqueued on `stream` (0 = legacy default stream); nothing synchronises the host.
- *   - Kernels are launched with programmatic dependent launch allowed and may read a call's
- *     read-only inputs that no call of this library writes (confidences, cost tables, block
- *     tokens, logits) while the previous kernel on the stream is still finishing; everything
- *     else (tiers, windows, cu_seqlens, histories) and every output waits for it. A kernel of
- *     the caller's that precedes a call on the stream and itself triggers its dependents early
- *     (griddepcontrol.launch_dependents) must have written those inputs before it triggers;
- *     kernels launched without that trigger need nothing.
+ *   - Kernels are launched with programmatic dependent launch allowed. A call may read, while
+ *     the previous kernel on the stream is still finishing, its read-only inputs that no
+ *     kernel of this library is writing at that moment: confidences, cost tables, block
+ *     tokens, logits and, in a verify call's second kernel, windows, cu_seqlens and the
+ *     history lengths out_len (that kernel starts early only after the call's first kernel,
+ *     which writes none of them, has itself waited for everything before it). Tiers and every
+ *     output wait for the previous kernel. A kernel of the caller's that precedes a call on
+ *     the stream and triggers its dependents early (griddepcontrol.launch_dependents) must
+ *     have written those inputs before it triggers; kernels launched without that trigger
+ *     need nothing.
  *   - Return value: DSPARK_OK, or a negative DSPARK_ERR_* code when the host-side argument check
  *     or the kernel launch failed. On error nothing was enqueued (argument errors) or the launch
  *     was refused (DSPARK_ERR_CUDA); dspark_last_error() then describes it.
