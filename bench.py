@@ -605,7 +605,10 @@ def run_native(args, rank, world, local):
 def host_and_device_us(fn, n, stream):
     """(host submission us, device us) per call of fn: the host's time to enqueue n calls while
     a sleep kernel holds the GPU (so no launch waits on the GPU), and the GPU's time for the n
-    calls back to back once the sleep ends (events after it)."""
+    calls back to back once the sleep ends (events after it). (None, None) where this torch
+    has no sleep kernel."""
+    if not hasattr(torch.cuda, "_sleep"):
+        return None, None
     for i in range(64):
         fn(i)
     torch.cuda.synchronize()
@@ -704,7 +707,8 @@ def latency_leg(dev, steps, pool=64):
                                ("graph_cycle", lambda i: cycle_launch(), 16)):
             host, devus = host_and_device_us(fn, reps, stream)
             per = pool if mode == "graph_cycle" else 1
-            out[f"{name}_{mode}"] = {"host_us": host / per, "device_us": devus / per}
+            out[f"{name}_{mode}"] = {"host_us": None if host is None else host / per,
+                                     "device_us": None if devus is None else devus / per}
         out["pool_mb"] = round(sum(sum(t.numel() * t.element_size() for t in e[2:] if t is not None)
                                    for e in entries) / 1e6, 1)
         del graphs, cycle, cycle_launch, cycle_calls, calls, entries
