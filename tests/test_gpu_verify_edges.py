@@ -189,3 +189,43 @@ def test_more_than_4096_requests(dev, stochastic):
         gres = run(dev, ws, "compact", tgt, bt.tokens, cu, w, stochastic, drf, kernel, **kw)
         rres = ref("compact", tgt, bt.tokens, cu, w, stochastic, drf, **kw)
         check(gres, rres, stochastic, tgt.shape[0])
+
+
+def chunks_per_row(V, B, gamma):
+    """Chunks per logits row of the streaming plan: about 4096 units per call (1024 when the
+    block holds at most 64 rows), chunks of 256 to 12288 elements in multiples of 8."""
+    rows = B * gamma
+    nc_min = -(-V // 12288)
+    nc_max = max(V // 256, 1)
+    want = -(-(1024 if rows <= 64 else 4096) // max(rows, 1))
+    nc = max(min(want, nc_max), nc_min)
+    C = -(-(-(-V // nc)) // 8) * 8
+    return -(-V // C)
+
+
+# (B, gamma, V): the bonus kernel combines a row's partials with 1, 2 or 4 per lane, or one row
+# at a time past 128 chunks
+COMBINE_CASES = [(40, 8, 4096), (3, 6, 20000), (2, 5, 40000), (1, 2, 131072)]
+
+
+@pytest.mark.parametrize("B,gamma,V", COMBINE_CASES)
+@pytest.mark.parametrize("mode", ["compact", "cap_accept"])
+def test_stochastic_every_combine_width(dev, B, gamma, V, mode):
+    nc = chunks_per_row(V, B, gamma)
+    wl = synth.WORKLOADS["stochastic"].with_(B=B, gamma=gamma, V=V, tiers=(B * gamma,))
+    bt = synth.make_batch(wl, seed=B + V, stochastic=True)
+    w = oracle.schedule(bt.conf, bt.bias, bt.alpha, 0.0 * bt.theta)["windows"]   # full windows
+    cu = np.concatenate([[0], np.cumsum(w)]).astype(np.int32)
+    tgt = synth.gather_packed(bt.target, B, gamma, w) if mode == "compact" else bt.target
+    kw = dict(temperature=0.8, seed=13, step=2)
+    ws = torch.empty(bd.dspark_verify_workspace_bytes(B, gamma, V, True), dtype=torch.uint8,
+                     device=dev)
+    for kernel in ("register", "bulk"):
+        gres = run(dev, ws, mode, tgt, bt.tokens, cu if mode == "compact" else None, w, True,
+                   bt.draft, kernel, **kw)
+        rres = ref(mode, tgt, bt.tokens, cu if mode == "compact" else None, w, True, bt.draft,
+                   **kw)
+        check(gres, rres, True, tgt.shape[0])
+    assert nc == chunks_per_row(V, B, gamma)
+    assert {(40, 8, 4096): nc <= 32, (3, 6, 20000): 32 < nc <= 64,
+            (2, 5, 40000): 64 < nc <= 128, (1, 2, 131072): nc > 128}[(B, gamma, V)], nc
