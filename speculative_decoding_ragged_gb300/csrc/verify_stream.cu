@@ -61,12 +61,12 @@ __device__ __forceinline__ void chunk_lane(const char* row, int v0, int v1, int 
     }
 }
 
-// Register-streaming variant: any alignment (scalar loads when the rows are not 16-byte
-// aligned or V % 8 != 0).
 // Compact batches of fewer requests than this keep cu_seqlens (and the windows) in shared
 // memory, so a draft job's owner search costs shared-memory latency, not L2 round trips.
 constexpr int kCuCache = 1024;
 
+// Register-streaming variant: any alignment (scalar loads when the rows are not 16-byte
+// aligned or V % 8 != 0).
 template <int DT, bool STOCH>
 __global__ void __launch_bounds__(kStreamThreads)
 verify_stream_kernel(StreamArgs A)
