@@ -210,8 +210,14 @@ int dspark_schedule_pack(const float* conf, int B, int gamma, const dspark_cost*
  *   of every target row that carries a stochastic accept test, (-1, -1) on the other rows of a
  *   request (always -1 in greedy mode).
  * workspace: device scratch of at least dspark_verify_workspace_bytes(B, gamma, V, stochastic)
- *   bytes, 16-byte aligned, owned by the caller, fully rewritten by every call before it is
- *   read (no clearing needed). Calls that share one workspace must not overlap on the GPU.
+ *   bytes, 16-byte aligned, owned by the caller; no clearing needed. Its first 256 bytes carry
+ *   state from one call to the next: the bulk-copy streaming kernel hands out the second half
+ *   of its work from a counter there, and each call leaves that counter at zero, with a 64-bit
+ *   tag beside it, for the next call. A call that finds no tag (a fresh or zeroed workspace)
+ *   splits its work evenly instead, with identical results. Between two calls that share a
+ *   workspace, leave those 256 bytes as the last call left them or zero them; the rest is
+ *   rewritten by every call before it is read. Calls that share one workspace must not overlap
+ *   on the GPU.
  * Limits: 0 <= B, 1 <= gamma <= DSPARK_MAX_GAMMA, V >= 1, temperature > 0 (stochastic).
  * Kernels: a persistent streaming kernel over fixed row chunks (register or TMA bulk-copy
  * streaming, see dspark_set_stream_kernel), then, greedy: one CTA per request that combines
@@ -379,7 +385,8 @@ int dspark_verify_noalloc(dspark_mode mode, int stochastic,
 /* Message of the last failed call on this host thread ("" if none). Never NULL. */
 const char* dspark_last_error(void);
 
-/* ABI version: 100 * major + minor (1.1: the dspark_graph_* capture and replay calls). */
+/* ABI version: 100 * major + minor (1.1: the dspark_graph_* capture and replay calls; 1.2: a
+ * 256-byte head in the verify workspace). */
 int dspark_version(void);
 
 #ifdef __cplusplus

@@ -362,6 +362,6 @@ int dspark_set_stream_events(cudaEvent_t start, cudaEvent_t stop)
 
 const char* dspark_last_error(void) { return dspark::last_error(); }
 
-int dspark_version(void) { return 101; }
+int dspark_version(void) { return 102; }
 
 }  // extern "C"

@@ -76,7 +76,8 @@ struct FinalArgs {
     int32_t* status;
     BonusJob* jobs;   // [B] (stochastic)
     float* tiles;     // [B][n_tiles][2]: residual and p weight sums per 256-token tile
-    unsigned* done;   // [B]: tile CTAs finished per request (zeroed by the finaliser)
+    unsigned* done;   // [B]: tile CTAs finished per request (zeroed by the streaming kernel)
+    WsHead* head;     // the workspace head, left ready for the next call
     int32_t* out_tokens;   // fused compact scatter (nullptr: none)
     int32_t* out_len;
     int out_cap;
@@ -378,6 +379,7 @@ verify_finalize_kernel(FinalArgs A)
     // before the streaming kernel have completed by the time this one starts
     const int n_hist = (A.out_tokens != nullptr && warp == 0) ? A.out_len[b] : 0;
     pdl_wait_and_trigger();
+    reset_ws_head(A.head);
     int32_t* out = A.committed + static_cast<int64_t>(b) * gamma;
 
     if (base < 0 || base + nrows > n_t) {
@@ -644,6 +646,7 @@ bonus_final_kernel(FinalArgs A, int ctas_per_request)
     }
     const int n_hist = (A.out_tokens != nullptr && warp == 0) ? A.out_len[b] : 0;
     pdl_wait_and_trigger();
+    reset_ws_head(A.head);
 
     if (!rows_ok) {
         if (cta == 0) bad_rows_outputs(A, b, base, nrows, tid, kTileThreads, bits, n_hist);
@@ -781,8 +784,8 @@ bonus_final_kernel(FinalArgs A, int ctas_per_request)
 }
 
 template <int DT, bool STOCH>
-int run_verify(const VerifyCall& c, const Plan& plan, void* part_t, void* part_d, void* jobs,
-               void* tiles, cudaStream_t stream)
+int run_verify(const VerifyCall& c, const Plan& plan, WsHead* head, void* part_t, void* part_d,
+               void* jobs, void* tiles, cudaStream_t stream)
 {
     const int L = c.gamma - 1;
     const double inv_t = STOCH ? 1.0 / static_cast<double>(c.temperature) : 1.0;
@@ -814,6 +817,7 @@ int run_verify(const VerifyCall& c, const Plan& plan, void* part_t, void* part_d
     // stochastic: the bonus kernel's per-request counters, zeroed by the streaming kernel
     sa.zero = STOCH ? reinterpret_cast<unsigned*>(static_cast<BonusJob*>(jobs) + c.B) : nullptr;
     sa.n_zero = STOCH ? c.B : 0;
+    sa.head = head;
 
     const int64_t max_units = (plan.rows_max + (STOCH ? static_cast<int64_t>(c.B) * L : 0)) * plan.nc;
     int rc = launch_verify_stream(DT, STOCH, sa, max_units, stream);
@@ -846,6 +850,7 @@ int run_verify(const VerifyCall& c, const Plan& plan, void* part_t, void* part_d
     fa.jobs = static_cast<BonusJob*>(jobs);
     fa.done = reinterpret_cast<unsigned*>(static_cast<BonusJob*>(jobs) + c.B);
     fa.tiles = static_cast<float*>(tiles);
+    fa.head = head;
     fa.out_tokens = c.out_tokens;
     fa.out_len = c.out_len;
     fa.out_cap = c.out_cap;
@@ -874,8 +879,9 @@ int run_verify(const VerifyCall& c, const Plan& plan, void* part_t, void* part_d
 
 }  // namespace
 
-// Workspace layout: target-row partials; then, stochastic only, draft-row partials, the bonus
-// jobs [B] and the bonus tile sums [B][n_tiles][2].
+// Workspace layout: the head (state handed from call to call); target-row partials; then,
+// stochastic only, draft-row partials, the bonus jobs [B] with their counters [B] and the bonus
+// tile sums [B][n_tiles][2].
 struct WsLayout {
     size_t part, jobs, tiles, total;
 };
@@ -888,12 +894,12 @@ WsLayout ws_layout(int B, int gamma, int V, int stochastic)
     const size_t per = stochastic ? sizeof(SoftPart) : sizeof(ArgPart);
     l.part = align_up(static_cast<size_t>(plan.rows_max) * plan.nc * per, 256);
     if (!stochastic) {
-        l.total = l.part;
+        l.total = kWsHeadBytes + l.part;
         return l;
     }
     l.jobs = align_up((sizeof(BonusJob) + sizeof(unsigned)) * static_cast<size_t>(B), 256);
     l.tiles = align_up(sizeof(float) * 2 * static_cast<size_t>(B) * ((V + 255) / 256), 256);
-    l.total = 2 * l.part + l.jobs + l.tiles;
+    l.total = kWsHeadBytes + 2 * l.part + l.jobs + l.tiles;
     return l;
 }
 
@@ -915,16 +921,19 @@ int launch_verify(const VerifyCall& c, cudaStream_t stream)
     if (need > 0 && (c.ws == nullptr || reinterpret_cast<uintptr_t>(c.ws) % 16 != 0))
         return fail(DSPARK_ERR_INVALID_ARG, "dspark_verify: workspace must be a 16-byte aligned device pointer");
     const WsLayout lay = ws_layout(c.B, c.gamma, c.V, c.stochastic);
-    char* ws = static_cast<char*>(c.ws);
+    WsHead* head = static_cast<WsHead*>(c.ws);
+    char* ws = static_cast<char*>(c.ws) + kWsHeadBytes;
     void* part_t = ws;
     void* part_d = c.stochastic ? ws + lay.part : nullptr;
     void* jobs = c.stochastic ? ws + 2 * lay.part : nullptr;
     void* tiles = c.stochastic ? ws + 2 * lay.part + lay.jobs : nullptr;
     if (c.dtype == DSPARK_BF16)
-        return c.stochastic ? run_verify<DSPARK_BF16, true>(c, plan, part_t, part_d, jobs, tiles, stream)
-                            : run_verify<DSPARK_BF16, false>(c, plan, part_t, part_d, jobs, tiles, stream);
-    return c.stochastic ? run_verify<DSPARK_F32, true>(c, plan, part_t, part_d, jobs, tiles, stream)
-                        : run_verify<DSPARK_F32, false>(c, plan, part_t, part_d, jobs, tiles, stream);
+        return c.stochastic
+                   ? run_verify<DSPARK_BF16, true>(c, plan, head, part_t, part_d, jobs, tiles, stream)
+                   : run_verify<DSPARK_BF16, false>(c, plan, head, part_t, part_d, jobs, tiles, stream);
+    return c.stochastic
+               ? run_verify<DSPARK_F32, true>(c, plan, head, part_t, part_d, jobs, tiles, stream)
+               : run_verify<DSPARK_F32, false>(c, plan, head, part_t, part_d, jobs, tiles, stream);
 }
 
 }  // namespace dspark

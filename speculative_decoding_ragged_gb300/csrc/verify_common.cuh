@@ -68,6 +68,31 @@ inline Plan make_plan(int V, int B, int gamma)
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// The first kWsHeadBytes of a verify workspace: state that one call hands to the next. The
+// bulk-copy streaming kernel splits half of its units evenly over its CTAs and hands out the
+// other half one at a time from `next_unit`, so CTAs that stream faster take more of the tail.
+// The call's last kernel, which starts only after the streaming kernel has completed, leaves
+// next_unit = 0 and tag = kWsHeadTag for the next call. A streaming kernel that finds any other
+// tag (a fresh or cleared workspace) splits all of its units evenly instead: the same partials,
+// only the balance of the tail differs.
+struct WsHead {
+    unsigned next_unit;            // units of the dynamic half handed out so far
+    unsigned pad;
+    unsigned long long tag;
+};
+constexpr size_t kWsHeadBytes = 256;
+constexpr unsigned long long kWsHeadTag = 0x7c3a91e4d2b8f605ull;
+
+// Leaves the workspace head ready for the next call (one thread of the call's last kernel,
+// after that kernel's wait for the streaming kernel).
+__device__ __forceinline__ void reset_ws_head(WsHead* h)
+{
+    if (h != nullptr && blockIdx.x == 0 && threadIdx.x == 0) {
+        h->next_unit = 0u;
+        h->tag = kWsHeadTag;
+    }
+}
+
 struct StreamArgs {
     const void* target;
     const void* draft;
@@ -78,6 +103,7 @@ struct StreamArgs {
     int32_t* status;
     unsigned* zero;   // counters of the call's next kernel, zeroed here (nullptr: none)
     int n_zero;
+    WsHead* head;     // the workspace head (bulk kernel's unit counter)
     int mode, V, nc, C, vec, B, gamma, target_rows;
     int64_t rows_max;
     float s;   // log2(e) / temperature

@@ -109,15 +109,28 @@ verify_stream_kernel(StreamArgs A)
 }
 
 // ---- bulk-copy streaming -----------------------------------------------------------------
-// A persistent grid (a few CTAs per SM) where each CTA owns a contiguous run of units. Warp
-// kBulkConsumers is the producer: its lane 0 walks the run and, for the k-th unit, waits until
-// stage k % S is free, arms that stage's "full" mbarrier with the unit's byte count and starts
-// one cp.async.bulk of the whole chunk into the stage. Consumer warp k % kBulkConsumers waits
-// on the full barrier, folds the staged chunk with the same per-lane order as the register
-// kernel, releases the stage on its "empty" barrier and writes the unit's partial. Every wait
-// is bounded (about a second of SM clock from its own start); a wait that gives up sets
-// DSPARK_STATUS_STALL and the producer still waits, bounded, for every copy it started before
-// the CTA exits.
+// A persistent grid (a few CTAs per SM). CTA i streams unit i first; of the remaining units
+// the first half is split into one contiguous run per CTA and the second half is handed out one
+// unit at a time from the counter in the workspace head (an atomic ticket, fetched while the
+// previous copy lands), so CTAs on SMs that stream faster take more of the tail. Without a
+// valid head every remaining unit is in the runs. Warp kBulkConsumers is the producer: its
+// lane 0, for its k-th unit, waits until stage
+// k % S is free, records the unit in the stage's slot, arms the stage's "full" mbarrier with
+// the unit's byte count (the arrive publishes the slot) and starts one cp.async.bulk of the
+// whole chunk into the stage; after its last unit it posts one end marker per consumer.
+// Consumer warp k % kBulkConsumers waits on the full barrier, reads the slot, folds the staged
+// chunk with the same per-lane order as the register kernel, releases the stage on its "empty"
+// barrier and writes the unit's partial. Every wait is bounded (about a second of SM clock from
+// its own start); a wait that gives up sets DSPARK_STATUS_STALL and the producer still waits,
+// bounded, for every copy it started before the CTA exits.
+// Per-CTA stamps of the large-vocab launch (instrumented copy, L2 flushed) showed why the tail
+// is dynamic: with even runs the CTA bodies spanned 46.4 us (the copy peak's rate) but CTAs
+// ended between 40.9 and 46.4 us, since SMs stream at rates a few per cent apart. Handing out
+// the second half by ticket took the launch from 51.1 to 49.6 us and the high-load cap-accept
+// launch from 178 to 170.5 us; a fifth, a third or all of the units by ticket landed within a
+// microsecond of that, a tenth or a twentieth gained less (172-174 us at high load). Each
+// CTA's first unit is fixed so that the head's tag, one L2 or DRAM round trip, is read while
+// that unit's copy is in flight instead of before it.
 // Measured on GB300 (whole steps of the large-vocab and high-load workloads): 4 consumer warps,
 // chunks of up to 12288 elements and a 96 KB ring (four stages of up to 24 KB, two CTAs per SM,
 // eight chunks in flight per SM) beat chunks of 2048-8192 elements in 32-80 KB rings (three or
@@ -238,6 +251,8 @@ verify_bulk_kernel(StreamArgs A, int stages, int stage_bytes)
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) uint64_t full_bar[kBulkMaxStages];
     __shared__ __align__(8) uint64_t empty_bar[kBulkMaxStages];
+    __shared__ int64_t stage_job[kBulkMaxStages];     // the unit each stage holds (row job,
+    __shared__ int stage_c[kBulkMaxStages];           // chunk), or job -1: no more units
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
@@ -252,25 +267,65 @@ verify_bulk_kernel(StreamArgs A, int stages, int stage_bytes)
     zero_next_counters(A);
     int64_t n_t;
     const int64_t U = unit_count<STOCH>(A, n_t, A.cu);
-    const int64_t u0 = static_cast<int64_t>(blockIdx.x) * U / gridDim.x;
-    const int64_t u1 = static_cast<int64_t>(blockIdx.x + 1) * U / gridDim.x;
-    const int64_t K = u1 - u0;
 
     if (warp == kBulkConsumers) {                     // producer warp: lane 0 issues
         if (lane != 0) return;
+        // Units: first unit blockIdx.x, whatever the head says, so the first copy is in flight
+        // before the head's tag arrives; then of the rest [G, U) a contiguous run per CTA over
+        // the first half and tickets for the second half when the head is valid, else runs over
+        // all of it. No kernel writes the head while this one runs: every CTA reads one tag.
+        const int64_t G = gridDim.x;
+        const unsigned long long tag =
+            A.head != nullptr ? *static_cast<volatile unsigned long long*>(&A.head->tag) : 0ull;
+        bool tickets = false;
+        int phase = 0;                                // 0: the first unit, 1: the run, 2: tickets
+        int64_t u = blockIdx.x, u1 = 0, S = 0;
+        unsigned tk = 0;                              // the ticket in flight
+        // the next unit into u; false when this CTA has no more
+        auto advance = [&]() -> bool {
+            if (phase == 0) {
+                tickets = tag == kWsHeadTag;
+                const int64_t R = U > G ? U - G : 0;
+                S = tickets ? R - R / 2 : R;
+                u = G + static_cast<int64_t>(blockIdx.x) * S / G;
+                u1 = G + static_cast<int64_t>(blockIdx.x + 1) * S / G;
+                if (tickets) tk = atomicAdd(&A.head->next_unit, 1u);   // used after the run
+                phase = 1;
+                if (u < u1) return true;
+            } else if (phase == 1) {
+                if (++u < u1) return true;
+            }
+            phase = 2;
+            if (!tickets) return false;
+            u = G + S + tk;
+            if (u >= U) return false;
+            tk = atomicAdd(&A.head->next_unit, 1u);   // travels while this unit's copy lands
+            return true;
+        };
         bool ok = true;
         DraftCursor cur;
-        int64_t job = u0 / A.nc;
-        int c = static_cast<int>(u0 - job * A.nc);
         int s = 0;
         uint32_t ph = 0;                              // parity of this use of stage s
         int64_t k = 0;
-        for (; k < K; ++k) {
+        bool more = u < U || advance();
+        for (; more; ++k, more = advance()) {
+            int64_t job;
+            int c;
+            if (u <= 0x7fffffff) {                    // 32-bit division where it fits
+                const int q = static_cast<int>(u) / A.nc;
+                job = q;
+                c = static_cast<int>(u) - q * A.nc;
+            } else {
+                job = u / A.nc;
+                c = static_cast<int>(u - job * A.nc);
+            }
             const uint32_t full = smem_addr(&full_bar[s]);
             if (k >= stages && !mbar_wait(smem_addr(&empty_bar[s]), ph ^ 1u)) {
                 ok = false;
                 break;
             }
+            stage_job[s] = job;                       // published by the arrive below
+            stage_c[s] = c;
             const char* row = bulk_source<E>(A, job, n_t, cur);
             if (row == nullptr) {
                 mbar_arrive(full);                    // a skipped unit: complete the phase
@@ -282,7 +337,16 @@ verify_bulk_kernel(StreamArgs A, int stages, int stage_bytes)
                 bulk_load(smem_addr(ring + static_cast<size_t>(s) * stage_bytes),
                           row + static_cast<int64_t>(v0) * E, bytes, full);
             }
-            if (++c == A.nc) { c = 0; ++job; }
+            if (++s == stages) { s = 0; ph ^= 1u; }
+        }
+        // one end marker per consumer warp (consecutive slots: one for each of them)
+        for (int e = 0; ok && e < kBulkConsumers; ++e, ++k) {
+            if (k >= stages && !mbar_wait(smem_addr(&empty_bar[s]), ph ^ 1u)) {
+                ok = false;
+                break;
+            }
+            stage_job[s] = -1;
+            mbar_arrive(smem_addr(&full_bar[s]));
             if (++s == stages) { s = 0; ph ^= 1u; }
         }
         // every started copy must land before this CTA may exit
@@ -296,16 +360,17 @@ verify_bulk_kernel(StreamArgs A, int stages, int stage_bytes)
         return;
     }
 
-    int64_t job = (u0 + warp) / A.nc;
-    int c = static_cast<int>(u0 + warp - job * A.nc);
     int s = warp;                                     // stages % kBulkConsumers == 0
     uint32_t ph = 0;
-    for (int64_t k = warp; k < K; k += kBulkConsumers) {
-        bool ok = mbar_wait(smem_addr(&full_bar[s]), ph);
+    while (true) {
+        const bool ok = mbar_wait(smem_addr(&full_bar[s]), ph);
         if (!__all_sync(0xffffffffu, ok)) {
             if (lane == 0) raise_status(A.status, DSPARK_STATUS_STALL);
             break;
         }
+        const int64_t job = stage_job[s];
+        const int c = stage_c[s];
+        if (job < 0) break;                           // the producer's end marker
         const UnitSrc src = unit_source<E>(A, job, c, n_t, A.cu, A.windows);
         float a = -INFINITY, bsum = 0.0f;
         int idx = 0x7FFFFFFF;
@@ -325,8 +390,6 @@ verify_bulk_kernel(StreamArgs A, int stages, int stage_bytes)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&empty_bar[s]));
         if (!src.skip) write_partial<STOCH>(A, src, lane, a, bsum, idx);
-        c += kBulkConsumers;
-        while (c >= A.nc) { c -= A.nc; ++job; }
         s += kBulkConsumers;
         if (s >= stages) { s -= stages; ph ^= 1u; }
     }

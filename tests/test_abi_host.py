@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_version(lib):
     # 1.1: the dspark_graph_* capture and replay calls
-    assert lib.dspark_version() == 101
+    assert lib.dspark_version() == 102
 
 
 def test_argument_errors_are_reported_on_the_host(lib):
@@ -93,11 +93,13 @@ def test_workspace_size_is_a_function_of_sizes(lib):
     assert bd.dspark_verify_workspace_bytes(0, 8, 1000, False) == 0
     g = bd.dspark_verify_workspace_bytes(256, 8, 151936, False)
     s = bd.dspark_verify_workspace_bytes(256, 8, 151936, True)
-    # stochastic: target and draft partials (8 B each, like greedy's), a 48-byte bonus job and
-    # a 4-byte counter per request, and two fp32 sums per 256-token tile per request
+    # a 256-byte head, then the target partials (8 B per chunk of each of the B*gamma rows);
+    # stochastic adds the draft partials (as many, 8 B each), a 48-byte bonus job and a 4-byte
+    # counter per request, and two fp32 sums per 256-token tile per request
     align = lambda x: (x + 255) // 256 * 256
-    assert g > 0 and s == 2 * g + align(52 * 256) + align(8 * 256 * ((151936 + 255) // 256))
-    assert g % 256 == 0
+    part = g - 256
+    assert part > 0 and part % 256 == 0
+    assert s == 256 + 2 * part + align(52 * 256) + align(8 * 256 * ((151936 + 255) // 256))
     assert bd.dspark_verify_workspace_bytes(-1, 8, 10, False) == 0
     assert "bad sizes" in bd.last_error()
 

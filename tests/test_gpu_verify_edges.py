@@ -1,5 +1,6 @@
 """Edge cases of verify against the oracle, with both streaming kernels: one workspace serving
-calls of every size and mode, requests whose rows the buffer does not hold (a short buffer, or
+calls of every size and mode, the workspace head in each of its states (garbage, left by a
+call, zeroed), requests whose rows the buffer does not hold (a short buffer, or
 none at all: bad rows, nothing committed, (-1, -1) on the rows the buffer does hold), rows before
 cu_seqlens[0], requests whose windows reach into the next request's rows, and batches of more
 than 4096 requests."""
@@ -77,7 +78,8 @@ def check(g, r, stochastic, rows_used):
 @pytest.mark.parametrize("stochastic", [False, True])
 def test_one_workspace_serves_calls_of_every_size_and_mode(dev, kernel, stochastic):
     # the largest size's workspace, filled with garbage once, then calls of shrinking and
-    # growing sizes in every mode: each call rewrites what it reads
+    # growing sizes in every mode: each call rewrites what it reads (the first call finds no
+    # valid head and splits the bulk kernel's units evenly; the later ones hand out tickets)
     sizes = [(48, 8, 4096), (5, 6, 2056), (64, 4, 8192), (17, 8, 1024), (48, 8, 4096)]
     need = max(bd.dspark_verify_workspace_bytes(B, g, V, stochastic) for B, g, V in sizes)
     ws = torch.full((need,), 0xA5, dtype=torch.uint8, device=dev)
@@ -96,6 +98,42 @@ def test_one_workspace_serves_calls_of_every_size_and_mode(dev, kernel, stochast
             rres = ref(mode, tgt, bt.tokens, cu if mode == "compact" else None, win, stochastic,
                        bt.draft if stochastic else None, **kw)
             check(gres, rres, stochastic, tgt.shape[0])
+
+
+def head_words(ws):
+    """(unit counter, tag) of the workspace head: its first 4 and its bytes 8..16."""
+    h = ws[:16].cpu().numpy()
+    return int(h[:4].view(np.uint32)[0]), int(h[8:16].view(np.uint64)[0])
+
+
+@pytest.mark.parametrize("stochastic", [False, True])
+def test_workspace_head_in_every_state(dev, stochastic):
+    # the bulk kernel hands out half of its units by ticket from the workspace head when the
+    # previous call left it valid, else splits them evenly: the results must not depend on it
+    wl0 = synth.WORKLOADS["stochastic"] if stochastic else synth.WORKLOADS["large_vocab_mixed"]
+    sizes = [(40, 8, 16384), (7, 5, 30000)]
+    need = max(bd.dspark_verify_workspace_bytes(B, g, V, stochastic) for B, g, V in sizes)
+    gen = torch.Generator(device="cpu").manual_seed(5)
+    ws = torch.randint(0, 256, (need,), dtype=torch.uint8, generator=gen).to(dev)
+    tags = set()
+    for k, state in enumerate(["garbage", "left", "left", "zeroed", "left"]):
+        if state == "zeroed":
+            ws[:256].zero_()
+        B, g, V = sizes[k % 2]
+        wl = wl0.with_(B=B, gamma=g, V=V, tiers=(B * g,))
+        bt = synth.make_batch(wl, seed=500 + k, stochastic=stochastic)
+        w = oracle.schedule(bt.conf, bt.bias, bt.alpha, bt.theta)["windows"]
+        cu = np.concatenate([[0], np.cumsum(w)]).astype(np.int32)
+        tgt = synth.gather_packed(bt.target, B, g, w)
+        kw = dict(temperature=wl.temperature, seed=k, step=2) if stochastic else {}
+        drf = bt.draft if stochastic else None
+        gres = run(dev, ws, "compact", tgt, bt.tokens, cu, w, stochastic, drf, "bulk", **kw)
+        rres = ref("compact", tgt, bt.tokens, cu, w, stochastic, drf, **kw)
+        check(gres, rres, stochastic, tgt.shape[0])
+        counter, tag = head_words(ws)
+        assert counter == 0            # left ready for the next call
+        tags.add(tag)
+    assert len(tags) == 1 and 0 not in tags
 
 
 @pytest.mark.parametrize("kernel", ["register", "bulk"])
