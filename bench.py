@@ -11,7 +11,9 @@ seeded batches rotate so every step reads more than L2 holds.
 
 Prints one JSON line.
   value        packed verify rows per second over whole steps, inputs resident in HBM (events
-               around the K timed steps only, nothing recorded between a step's kernels);
+               around the K timed steps only, nothing recorded between a step's kernels; a
+               sleep kernel holds the GPU while the host enqueues them, so host speed does not
+               enter; the host's cost per step is reported under `timing`);
   e2e          the same rows/s with the step's inputs copied from pinned host memory and the
                results read back inside the timed region;
   legs         every workload timed alone: each of >= 30 launches after an L2 flush, events
@@ -471,14 +473,27 @@ def run_native(args, rank, world, local):
         step(i)
         st.out_len.zero_()
     torch.cuda.synchronize()
+    # the host's time to enqueue one step (a few more untimed steps)
+    t0 = time.perf_counter()
+    for i in range(8):
+        step(i)
+    host_step_s = (time.perf_counter() - t0) / 8
+    torch.cuda.synchronize()
+    st.out_len.zero_()
 
-    # device-resident timed region: K whole steps, events around the loop only
+    # device-resident timed region: K whole steps, events around the loop only. A sleep kernel
+    # holds the GPU while the host enqueues the steps, so the events time the GPU running them
+    # back to back (with their programmatic-dependent-launch overlap) whatever the host's speed:
+    # a slow or contended host would otherwise leave the GPU idle between launches and count
+    # the gaps. The host's own cost per step is reported beside it, and the end-to-end leg
+    # below includes it.
     K = args.steps
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     clocks.start()
     barrier(world)
     torch.cuda.synchronize()
+    held = hold_gpu(host_step_s * K)
     t_start.record(stream)
     for i in range(K):
         step(i)
@@ -564,6 +579,12 @@ def run_native(args, rank, world, local):
                          f"{nb} batches rotate; legs flush L2 before every timed call",
                    "parallelism": f"replicas{world}" if world > 1 else "single GPU"},
         "step_us": ms / K * 1e3,
+        "timing": {"what": "CUDA events around the K timed steps on the launching stream",
+                   "host_held": held,
+                   "how": "a sleep kernel held the GPU while the host enqueued the steps, so "
+                          "the events time the GPU running them back to back" if held else
+                          "steps enqueued as the GPU ran them",
+                   "host_us_per_step": host_step_s * 1e6},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_rows / (e2e_ms * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d // max(E, 1), "d2h_bytes_per_step": d2h // max(E, 1),
@@ -600,6 +621,15 @@ def run_native(args, rank, world, local):
                             "us_mean": lv["call_us"]["mean"],
                             "us_p10_p90": [lv["call_us"]["p10"], lv["call_us"]["p90"]]}}
     return out
+
+
+def hold_gpu(host_seconds):
+    """Enqueues a sleep kernel long enough for the host to enqueue work that takes it about
+    host_seconds (capped at 0.25 s); False where this torch has no sleep kernel."""
+    if not hasattr(torch.cuda, "_sleep"):
+        return False
+    torch.cuda._sleep(int(2.07e9 * min(host_seconds * 1.5 + 2e-3, 0.25)))   # cycles at max clock
+    return True
 
 
 def host_and_device_us(fn, n, stream):
