@@ -5,7 +5,10 @@ Its scratch is a static device array inside the library.
 
 The test calls it through the C ABI twice in a row with different inputs and checks each
 result against the ordinary dspark_verify with a caller workspace (bit for bit: both run the
-same kernels in the same order), then checks that sizes beyond the array are refused. The file
+same kernels in the same order), then checks that sizes beyond the array are refused. The
+greedy case is large enough for the bulk-copy streaming kernel, whose unit counter then sits in
+the static array's head: the first call finds it zeroed (no tag: units split evenly), the second
+hands out tickets. The file
 is named to be collected last, so a run that stops at the first failure has run everything else;
 it also passes alone in a fresh process."""
 import numpy as np
