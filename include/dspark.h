@@ -70,7 +70,7 @@ extern "C" {
 #define DSPARK_STATUS_BAD_WINDOW     0x04 /* a window outside [1,gamma]: clamped into it        */
 #define DSPARK_STATUS_OUT_OVERFLOW   0x08 /* a history reached out_cap: tokens past it dropped   */
 #define DSPARK_STATUS_BAD_COST       0x10 /* no K had a finite positive T: K* := 0               */
-#define DSPARK_STATUS_BAD_ROWS       0x20 /* a request's logits rows lie outside the buffer      */
+#define DSPARK_STATUS_BAD_ROWS       0x20 /* a request's rows lie outside the verified rows      */
 #define DSPARK_STATUS_BAD_TOKEN      0x40 /* a draft id outside [0,V): treated as rejected       */
 #define DSPARK_STATUS_BAD_LENGTH     0x80 /* accept_len / out_len outside range: clamped         */
 #define DSPARK_STATUS_STALL         0x100 /* a bounded in-kernel wait gave up: this call's verify
@@ -174,12 +174,18 @@ int dspark_schedule_pack(const float* conf, int B, int gamma, const dspark_cost*
  * Rows. Target row for (request b, block position i):
  *   COMPACT              row cu_seqlens[b] + i, i < w_b         (target_logits = packed [M, V])
  *   STATIC, CAP_ACCEPT   row b*gamma + i,       i < gamma       (target_logits = block [B*gamma, V])
- * At most B*gamma target rows are read.
+ * The call verifies rows [0, N): N = cu_seqlens[B] (COMPACT: the packed total M) or B*gamma
+ * (STATIC, CAP_ACCEPT), capped at target_rows and at B*gamma; no other row is read.
  * target row (b,i) is the target's distribution for block position i+1, which holds the draft
  * d_{i+1} = block_tokens[b, i+1]. Draft row (b,i) of draft_logits [B, gamma-1, V] is the draft
  * distribution that d_{i+1} was sampled from (stochastic only).
- * Any row index outside [0, target_rows) flags DSPARK_STATUS_BAD_ROWS and the request commits
- * nothing (accept_len 0, committed all -1).
+ * A request with a row outside [0, N) (outside the buffer, or, COMPACT, at or past
+ * cu_seqlens[B]) flags DSPARK_STATUS_BAD_ROWS and commits nothing (accept_len 0, committed
+ * all -1). So does, COMPACT, a request whose rows that carry its accept tests reach into the
+ * next request's rows (cu_seqlens[b+1] < cu_seqlens[b] + w_b - 1): each packed row is one
+ * request's, although a request's last row may be shared. The exclusive scan of the windows
+ * that dspark_pack writes meets both rules; with rows shared otherwise, row_prob of a shared
+ * row holds either request's values.
  *
  * Greedy (stochastic == 0): g[b,i] = argmax_v target[row(b,i), v] (lowest v on ties; NaN
  *   unsupported). d_{i+1} is accepted iff d_{i+1} == g[b,i]; L = 1 + number of leading accepts;

@@ -380,6 +380,15 @@ int oracle_verify(int mode, int stochastic, const void* target, int target_rows,
     double* zq = (double*)malloc(sizeof(double) * (size_t)gamma);
     double* work = stochastic ? (double*)malloc(sizeof(double) * (size_t)V) : NULL;
 
+    /* The rows a call verifies: [0, N) with N = cu[B], the packed total M (COMPACT: the windows
+       are packed to the front of the buffer and nothing past M is read, "DSpark in SGLang", A2
+       ragged verify over full CUDA graphs, figure 2), or B * gamma (the block); never more than
+       the buffer holds, nor more than B * gamma. */
+    int64_t n_rows = (mode == OR_COMPACT) ? (int64_t)cu[B] : (int64_t)B * gamma;
+    if (n_rows < 0) n_rows = 0;
+    if (n_rows > (int64_t)target_rows) n_rows = target_rows;
+    if (n_rows > (int64_t)B * gamma) n_rows = (int64_t)B * gamma;
+
     for (int b = 0; b < B; ++b) {
         int w = gamma;
         if (mode != OR_STATIC) {
@@ -388,9 +397,14 @@ int oracle_verify(int mode, int stochastic, const void* target, int target_rows,
         }
         const int nrows = (mode == OR_COMPACT) ? w : gamma;
         const int64_t base = (mode == OR_COMPACT) ? (int64_t)cu[b] : (int64_t)b * gamma;
+        /* COMPACT: each packed row is one request's (the last b with cu[b] <= row), so the
+           rows that carry this request's accept tests, cu[b] .. cu[b] + w - 2, must lie before
+           the next request's first row; its last row may be shared */
+        const int shared = mode == OR_COMPACT && b + 1 < B && nrows >= 2 &&
+                           (int64_t)cu[b + 1] < base + nrows - 1;
         int32_t* out = committed + (size_t)b * gamma;
         for (int k = 0; k < gamma; ++k) out[k] = -1;
-        if (base < 0 || base + nrows > (int64_t)target_rows) {
+        if (base < 0 || base + nrows > n_rows || shared) {
             st |= OR_BAD_ROWS;
             accept_len[b] = 0;
             if (ceiling) ceiling[b] = (mode == OR_COMPACT) ? -1 : 0;

@@ -311,9 +311,22 @@ __device__ __forceinline__ void combine_request_rows(const FinalArgs& A, int64_t
     }
 }
 
-// Outputs of a request whose rows lie outside the buffer: nothing committed, (-1, -1) on its
-// rows that the buffer does hold, BAD_ROWS (with the caller's bits), and the fused scatter
-// checks the history length only. Threads tid < nthreads of one CTA; warp 0 scatters.
+// Whether request b's rows can be verified: they lie in [0, n_t), the rows the streaming
+// kernel covered, and (compact) the rows that carry its accept tests, base .. base + nrows - 2,
+// lie before the next request's first row. Each packed row is one request's (the streaming
+// kernel files a compact draft under the last b with cu[b] <= row); the last row may be shared.
+__device__ __forceinline__ bool request_rows_ok(const FinalArgs& A, int b, int64_t base,
+                                                int nrows, int64_t n_t)
+{
+    if (base < 0 || base + nrows > n_t) return false;
+    return !(A.mode == DSPARK_COMPACT && b + 1 < A.B && nrows >= 2 &&
+             static_cast<int64_t>(__ldg(A.cu + b + 1)) < base + nrows - 1);
+}
+
+// Outputs of a request whose rows cannot be verified (outside the verified rows, or sharing
+// tested rows with the next request): nothing committed, (-1, -1) on its rows that the buffer
+// does hold, BAD_ROWS (with the caller's bits), and the fused scatter checks the history
+// length only. Threads tid < nthreads of one CTA; warp 0 scatters.
 __device__ __forceinline__ void bad_rows_outputs(const FinalArgs& A, int b, int64_t base,
                                                  int nrows, int tid, int nthreads, int bits,
                                                  int n_hist)
@@ -374,6 +387,7 @@ verify_finalize_kernel(FinalArgs A)
     const int64_t base = (A.mode == DSPARK_COMPACT) ? static_cast<int64_t>(__ldg(A.cu + b))
                                                     : static_cast<int64_t>(b) * gamma;
     const int64_t n_t = target_row_count(A.mode, A.cu, A.B, gamma, A.target_rows, A.rows_max);
+    const bool rows_ok = request_rows_ok(A, b, base, nrows, n_t);
     // the history length the fused scatter appends at: the previous call wrote it, and every
     // kernel of this library triggers its dependents only after its own wait, so all kernels
     // before the streaming kernel have completed by the time this one starts
@@ -382,7 +396,7 @@ verify_finalize_kernel(FinalArgs A)
     reset_ws_head(A.head);
     int32_t* out = A.committed + static_cast<int64_t>(b) * gamma;
 
-    if (base < 0 || base + nrows > n_t) {
+    if (!rows_ok) {
         bad_rows_outputs(A, b, base, nrows, tid, kFinalThreads, bits, n_hist);
         return;
     }
@@ -635,7 +649,7 @@ bonus_final_kernel(FinalArgs A, int ctas_per_request)
     const int64_t base = (A.mode == DSPARK_COMPACT) ? static_cast<int64_t>(__ldg(A.cu + b))
                                                     : static_cast<int64_t>(b) * gamma;
     const int64_t n_t = target_row_count(A.mode, A.cu, A.B, gamma, A.target_rows, A.rows_max);
-    const bool rows_ok = base >= 0 && base + nrows <= n_t;
+    const bool rows_ok = request_rows_ok(A, b, base, nrows, n_t);
     const bool tested = warp == 0 && lane < ndec;
     const bool valid = d_mine >= 0 && d_mine < A.V;
     float lp = 0.0f, lq = 0.0f;

@@ -127,6 +127,43 @@ def test_verify_flags_and_bad_rows(oracle_mod):
     assert out["committed"][1].tolist() == [-1, -1, -1, -1]
 
 
+def test_compact_rows_end_at_the_packed_total(oracle_mod):
+    # compact verifies the packed rows [0, cu[B]) only: a request whose window reaches past
+    # cu[B] commits nothing, although the buffer holds the row (the rows of the others are
+    # verified as usual); the same request with cu[B] covering its rows is verified
+    x = np.zeros((8, 8), np.float32)
+    x[:, 3] = 1.0
+    tokens = np.array([[0, 3, 3], [0, 3, 3], [0, 3, 3]], np.int32)
+    w = np.array([2, 2, 2], np.int32)
+    short = oracle_mod.verify(oracle_mod.COMPACT, False, x, tokens, cu=np.array([0, 2, 4, 5]),
+                              windows=w)
+    assert short["status"] == 0x20
+    assert short["accept_len"].tolist() == [2, 2, 0]
+    assert short["committed"][2].tolist() == [-1, -1, -1]
+    full = oracle_mod.verify(oracle_mod.COMPACT, False, x, tokens, cu=np.array([0, 2, 4, 6]),
+                             windows=w)
+    assert full["status"] == 0
+    assert full["accept_len"].tolist() == [2, 2, 2]
+    assert full["committed"][2].tolist() == [3, 3, -1]
+
+
+def test_compact_tested_rows_belong_to_one_request(oracle_mod):
+    # each packed row is one request's: request 0's tested row 0 is also request 1's first row
+    # (cu[1] = 0) -> nothing committed; sharing only a last row (cu = 0, 1, 3) is fine
+    x = np.zeros((8, 8), np.float32)
+    x[:, 3] = 1.0
+    tokens = np.array([[0, 3, 3], [0, 3, 3], [0, 3, 3]], np.int32)
+    w = np.array([2, 2, 2], np.int32)
+    out = oracle_mod.verify(oracle_mod.COMPACT, False, x, tokens, cu=np.array([0, 0, 2, 4]),
+                            windows=w)
+    assert out["status"] == 0x20
+    assert out["accept_len"].tolist() == [0, 2, 2]
+    ok = oracle_mod.verify(oracle_mod.COMPACT, False, x, tokens, cu=np.array([0, 1, 3, 5]),
+                           windows=w)
+    assert ok["status"] == 0
+    assert ok["accept_len"].tolist() == [2, 2, 2]
+
+
 def make_stochastic(oracle_mod, B, gamma, V, rng, T=1.0, same=False):
     target = (rng.standard_normal((B * gamma, V)) * 2).astype(np.float32)
     draft = target[np.arange(B * (gamma - 1)) // (gamma - 1) * gamma
