@@ -2,8 +2,8 @@
 calls of every size and mode, the workspace head in each of its states (garbage, left by a
 call, zeroed), requests whose rows the buffer does not hold (a short buffer, or
 none at all: bad rows, nothing committed, (-1, -1) on the rows the buffer does hold), rows before
-cu_seqlens[0], requests whose windows reach into the next request's rows, and batches of more
-than 4096 requests."""
+cu_seqlens[0], requests whose windows reach into the next request's rows, fewer rows than
+requests, and batches of more than 4096 requests."""
 import numpy as np
 import pytest
 import torch
@@ -208,6 +208,33 @@ def test_a_window_reaching_into_the_next_request(dev, kernel, stochastic):
     gres = run(dev, ws, "compact", tgt, bt.tokens, cu_bad, w, stochastic, drf, kernel, **kw)
     rres = ref("compact", tgt, bt.tokens, cu_bad, w, stochastic, drf, **kw)
     check(gres, rres, stochastic, 0)
+
+
+@pytest.mark.parametrize("kernel", ["register", "bulk"])
+@pytest.mark.parametrize("stochastic", [False, True])
+def test_fewer_rows_than_requests(dev, kernel, stochastic):
+    # cu_seqlens puts two requests on each row, so its total (32) is below B (64): the bulk
+    # kernel starts its first copy before the wait when that unit's row is below B, and must
+    # discard the copies of rows 32..63 (units that are no target rows after all); the
+    # even requests share their tested row with the next request (bad rows, as the oracle has
+    # it), the odd ones share only their last row and are verified
+    wl = (synth.WORKLOADS["stochastic"] if stochastic else synth.WORKLOADS["large_vocab_mixed"])
+    wl = wl.with_(B=64, V=4096, tiers=(512,))
+    bt = synth.make_batch(wl, seed=9, stochastic=stochastic)
+    B, g = bt.B, bt.gamma
+    w = np.full(B, 2, dtype=np.int32)
+    cu = (np.arange(B + 1) // 2).astype(np.int32)
+    # a 128-row buffer of which cu_seqlens names 32; the last request's second row lies past
+    # them (bad rows, as the oracle has it)
+    tgt = synth.gather_packed(bt.target, B, g, w)
+    drf = bt.draft if stochastic else None
+    kw = dict(temperature=1.0, seed=6, step=1) if stochastic else {}
+    ws = torch.zeros(bd.dspark_verify_workspace_bytes(B, g, wl.V, stochastic), dtype=torch.uint8,
+                     device=dev)
+    for _ in range(2):          # the second call hands out the bulk kernel's tail by ticket
+        gres = run(dev, ws, "compact", tgt, bt.tokens, cu, w, stochastic, drf, kernel, **kw)
+        rres = ref("compact", tgt, bt.tokens, cu, w, stochastic, drf, **kw)
+        check(gres, rres, stochastic, 0)
 
 
 @pytest.mark.parametrize("stochastic", [False, True])
