@@ -218,12 +218,13 @@ int dspark_schedule_pack(const float* conf, int B, int gamma, const dspark_cost*
  * workspace: device scratch of at least dspark_verify_workspace_bytes(B, gamma, V, stochastic)
  *   bytes, 16-byte aligned, owned by the caller; no clearing needed. Its first 256 bytes carry
  *   state from one call to the next: the bulk-copy streaming kernel hands out the second half
- *   of its work from a counter there, and each call leaves that counter at zero, with a 64-bit
- *   tag beside it, for the next call. A call that finds no tag (a fresh or zeroed workspace)
- *   splits its work evenly instead, with identical results. Between two calls that share a
- *   workspace, leave those 256 bytes as the last call left them or zero them; the rest is
- *   rewritten by every call before it is read. Calls that share one workspace must not overlap
- *   on the GPU.
+ *   of its work from a counter there (bytes 4-7), and each call leaves that counter at zero,
+ *   between a 32-bit tag (bytes 0-3) and a 64-bit tag (bytes 8-15), for the next call. A call
+ *   that finds either tag missing (a fresh or zeroed workspace, or one whose first bytes were
+ *   written since) splits its work evenly instead, with identical results. Between two calls
+ *   that share a workspace, leave those 256 bytes as the last call left them or zero them;
+ *   the rest is rewritten by every call before it is read. Calls that share one workspace must
+ *   not overlap on the GPU.
  * Limits: 0 <= B, 1 <= gamma <= DSPARK_MAX_GAMMA, V >= 1, temperature > 0 (stochastic).
  * Kernels: a persistent streaming kernel over fixed row chunks (register or TMA bulk-copy
  * streaming, see dspark_set_stream_kernel), then, greedy: one CTA per request that combines

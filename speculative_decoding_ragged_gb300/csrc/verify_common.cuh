@@ -70,26 +70,52 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // The first kWsHeadBytes of a verify workspace: state that one call hands to the next. The
 // bulk-copy streaming kernel splits half of its units evenly over its CTAs and hands out the
-// other half one at a time from `next_unit`, so CTAs that stream faster take more of the tail.
-// The call's last kernel, which starts only after the streaming kernel has completed, leaves
-// next_unit = 0 and tag = kWsHeadTag for the next call. A streaming kernel that finds any other
-// tag (a fresh or cleared workspace) splits all of its units evenly instead: the same partials,
-// only the balance of the tail differs.
+// other half one at a time from a counter here, so CTAs that stream faster take more of the
+// tail. The counter is the high half of the head's first 8-byte word; its low half and the
+// second word hold tags. The call's last kernel, which starts only after the streaming kernel
+// has completed, leaves the counter at 0 with both tags for the next call. A streaming kernel
+// that finds either tag missing (a fresh or cleared workspace, or a former workspace whose
+// first bytes another tensor has since written) splits all of its units evenly instead: the
+// same partials, only the balance of the tail differs. Tickets add 2^32 to the first word, so
+// the low tag never changes while a kernel runs and every CTA reads the same verdict.
 struct WsHead {
-    unsigned next_unit;            // units of the dynamic half handed out so far
-    unsigned pad;
-    unsigned long long tag;
+    unsigned long long word;       // low 32 bits: kWsHeadTag32; high 32 bits: units handed out
+    unsigned long long tag;        // kWsHeadTag64
 };
 constexpr size_t kWsHeadBytes = 256;
-constexpr unsigned long long kWsHeadTag = 0x7c3a91e4d2b8f605ull;
+constexpr unsigned long long kWsHeadTag32 = 0xd2b8f605ull;
+constexpr unsigned long long kWsHeadTag64 = 0x7c3a91e44e1f63a9ull;
+
+// The head's two words (read once per CTA after its wait; volatile: another call wrote them),
+// and whether they carry both tags, i.e. were left by a call.
+__device__ __forceinline__ void ws_head_read(const WsHead* h, unsigned long long& w,
+                                             unsigned long long& t)
+{
+    w = 0;
+    t = 0;
+    if (h != nullptr) {
+        w = *reinterpret_cast<const volatile unsigned long long*>(&h->word);
+        t = *reinterpret_cast<const volatile unsigned long long*>(&h->tag);
+    }
+}
+__device__ __forceinline__ bool ws_head_tags_ok(unsigned long long w, unsigned long long t)
+{
+    return (w & 0xffffffffull) == kWsHeadTag32 && t == kWsHeadTag64;
+}
+
+// The next unit ticket of the dynamic half (a relaxed add of one to the counter).
+__device__ __forceinline__ unsigned ws_head_ticket(WsHead* h)
+{
+    return static_cast<unsigned>(atomicAdd(&h->word, 1ull << 32) >> 32);
+}
 
 // Leaves the workspace head ready for the next call (one thread of the call's last kernel,
 // after that kernel's wait for the streaming kernel).
 __device__ __forceinline__ void reset_ws_head(WsHead* h)
 {
     if (h != nullptr && blockIdx.x == 0 && threadIdx.x == 0) {
-        h->next_unit = 0u;
-        h->tag = kWsHeadTag;
+        h->word = kWsHeadTag32;
+        h->tag = kWsHeadTag64;
     }
 }
 

@@ -308,8 +308,8 @@ verify_bulk_kernel(StreamArgs A, int stages, int stage_bytes)
         // the first half and tickets for the second half when the head is valid, else runs over
         // all of it. No kernel writes the head while this one runs: every CTA reads one tag.
         const int64_t G = gridDim.x;
-        const unsigned long long tag =
-            A.head != nullptr ? *static_cast<volatile unsigned long long*>(&A.head->tag) : 0ull;
+        unsigned long long head_w, head_t;            // compared only when first needed
+        ws_head_read(A.head, head_w, head_t);
         bool tickets = false;
         int phase = 0;                                // 0: the first unit, 1: the run, 2: tickets
         int64_t u = blockIdx.x, u1 = 0, S = 0;
@@ -317,12 +317,12 @@ verify_bulk_kernel(StreamArgs A, int stages, int stage_bytes)
         // the next unit into u; false when this CTA has no more
         auto advance = [&]() -> bool {
             if (phase == 0) {
-                tickets = tag == kWsHeadTag;
+                tickets = ws_head_tags_ok(head_w, head_t);
                 const int64_t R = U > G ? U - G : 0;
                 S = tickets ? R - R / 2 : R;
                 u = G + static_cast<int64_t>(blockIdx.x) * S / G;
                 u1 = G + static_cast<int64_t>(blockIdx.x + 1) * S / G;
-                if (tickets) tk = atomicAdd(&A.head->next_unit, 1u);   // used after the run
+                if (tickets) tk = ws_head_ticket(A.head);  // used after the run
                 phase = 1;
                 if (u < u1) return true;
             } else if (phase == 1) {
@@ -332,7 +332,7 @@ verify_bulk_kernel(StreamArgs A, int stages, int stage_bytes)
             if (!tickets) return false;
             u = G + S + tk;
             if (u >= U) return false;
-            tk = atomicAdd(&A.head->next_unit, 1u);   // travels while this unit's copy lands
+            tk = ws_head_ticket(A.head);              // travels while this unit's copy lands
             return true;
         };
         bool ok = true;

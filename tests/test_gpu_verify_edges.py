@@ -1,6 +1,6 @@
 """Edge cases of verify against the oracle, with both streaming kernels: one workspace serving
 calls of every size and mode, the workspace head in each of its states (garbage, left by a
-call, zeroed), requests whose rows the buffer does not hold (a short buffer, or
+call, zeroed, its first bytes overwritten), requests whose rows the buffer does not hold (a short buffer, or
 none at all: bad rows, nothing committed, (-1, -1) on the rows the buffer does hold), rows before
 cu_seqlens[0], requests whose windows reach into the next request's rows, fewer rows than
 requests, and batches of more than 4096 requests."""
@@ -101,9 +101,10 @@ def test_one_workspace_serves_calls_of_every_size_and_mode(dev, kernel, stochast
 
 
 def head_words(ws):
-    """(unit counter, tag) of the workspace head: its first 4 and its bytes 8..16."""
+    """(unit counter, tags) of the workspace head: its bytes 4..8, and bytes 0..4 and 8..16."""
     h = ws[:16].cpu().numpy()
-    return int(h[:4].view(np.uint32)[0]), int(h[8:16].view(np.uint64)[0])
+    return int(h[4:8].view(np.uint32)[0]), (int(h[:4].view(np.uint32)[0]),
+                                             int(h[8:16].view(np.uint64)[0]))
 
 
 @pytest.mark.parametrize("stochastic", [False, True])
@@ -116,9 +117,14 @@ def test_workspace_head_in_every_state(dev, stochastic):
     gen = torch.Generator(device="cpu").manual_seed(5)
     ws = torch.randint(0, 256, (need,), dtype=torch.uint8, generator=gen).to(dev)
     tags = set()
-    for k, state in enumerate(["garbage", "left", "left", "zeroed", "left"]):
+    states = ["garbage", "left", "left", "zeroed", "left", "overwritten", "left"]
+    for k, state in enumerate(states):
         if state == "zeroed":
             ws[:256].zero_()
+        if state == "overwritten":
+            # another tensor's write over the first bytes (a caching allocator reuses freed
+            # blocks): the low tag and the counter garbage, the 64-bit tag intact
+            ws[:8].copy_(torch.tensor([7, 0, 0, 0, 9, 9, 9, 9], dtype=torch.uint8))
         B, g, V = sizes[k % 2]
         wl = wl0.with_(B=B, gamma=g, V=V, tiers=(B * g,))
         bt = synth.make_batch(wl, seed=500 + k, stochastic=stochastic)
@@ -133,7 +139,7 @@ def test_workspace_head_in_every_state(dev, stochastic):
         counter, tag = head_words(ws)
         assert counter == 0            # left ready for the next call
         tags.add(tag)
-    assert len(tags) == 1 and 0 not in tags
+    assert len(tags) == 1 and 0 not in next(iter(tags))
 
 
 @pytest.mark.parametrize("kernel", ["register", "bulk"])
