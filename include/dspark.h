@@ -185,7 +185,9 @@ int dspark_schedule_pack(const float* conf, int B, int gamma, const dspark_cost*
  * next request's rows (cu_seqlens[b+1] < cu_seqlens[b] + w_b - 1): each packed row is one
  * request's, although a request's last row may be shared. The exclusive scan of the windows
  * that dspark_pack writes meets both rules; with rows shared otherwise, row_prob of a shared
- * row holds either request's values.
+ * row holds either request's values. COMPACT needs cu_seqlens non-decreasing: where it
+ * decreases, the requests whose rows it reorders get undefined accept lengths and tokens
+ * (every row index is still checked: no fault).
  *
  * Greedy (stochastic == 0): g[b,i] = argmax_v target[row(b,i), v] (lowest v on ties; NaN
  *   unsupported). d_{i+1} is accepted iff d_{i+1} == g[b,i]; L = 1 + number of leading accepts;

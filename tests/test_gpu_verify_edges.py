@@ -3,7 +3,7 @@ calls of every size and mode, the workspace head in each of its states (garbage,
 call, zeroed, its first bytes overwritten), requests whose rows the buffer does not hold (a short buffer, or
 none at all: bad rows, nothing committed, (-1, -1) on the rows the buffer does hold), rows before
 cu_seqlens[0], requests whose windows reach into the next request's rows, fewer rows than
-requests, and batches of more than 4096 requests."""
+requests, random non-decreasing cu_seqlens, and batches of more than 4096 requests."""
 import numpy as np
 import pytest
 import torch
@@ -240,6 +240,45 @@ def test_fewer_rows_than_requests(dev, kernel, stochastic):
     for _ in range(2):          # the second call hands out the bulk kernel's tail by ticket
         gres = run(dev, ws, "compact", tgt, bt.tokens, cu, w, stochastic, drf, kernel, **kw)
         rres = ref("compact", tgt, bt.tokens, cu, w, stochastic, drf, **kw)
+        check(gres, rres, stochastic, 0)
+
+
+@pytest.mark.parametrize("case", range(48))
+def test_random_cu_seqlens_against_the_oracle(dev, case):
+    # non-decreasing cu_seqlens that need not be the scan of the windows: leading rows, gaps,
+    # requests sharing rows, totals past or short of the buffer, windows outside [1, gamma];
+    # every request verified, flagged or clamped as the oracle has it (compact mode)
+    rng = np.random.default_rng(31000 + case)
+    kernel = ["register", "bulk"][case % 2]
+    stochastic = bool((case // 2) % 2)
+    B = int(rng.integers(1, 49))
+    g = int(rng.integers(2 if stochastic else 1, 9))
+    V = int(rng.choice([1000, 1024, 2048, 4104]))
+    w = rng.integers(0, g + 2, size=B).astype(np.int32)
+    steps = rng.integers(0, g + 2, size=B)
+    cu = np.concatenate([[0], np.cumsum(steps)]).astype(np.int32) + int(rng.integers(0, 4))
+    rows = max(0, int(cu[B]) + int(rng.integers(-3, g + 1)))
+    tgt = (torch.randn((max(rows, 1), V), generator=torch.Generator().manual_seed(case)) * 2.0)
+    tgt = tgt.to(torch.bfloat16)[:rows]
+    tokens = rng.integers(0, V, size=(B, g)).astype(np.int32)
+    if rows:
+        best = tgt.float().argmax(dim=1).numpy()
+        for b in range(B):                      # accept some drafts where the rows exist
+            for i in range(g - 1):
+                r = int(cu[b]) + i
+                if r < rows and rng.uniform() < 0.7:
+                    tokens[b, i + 1] = best[r]
+    drf = None
+    kw = {}
+    if stochastic:
+        drf = (torch.randn((max(B * (g - 1), 1), V), generator=torch.Generator().manual_seed(
+            100 + case)) * 2.0).to(torch.bfloat16)[: B * (g - 1)]
+        kw = dict(temperature=float(rng.choice([0.7, 1.0])), seed=case, step=3)
+    ws = torch.empty(max(bd.dspark_verify_workspace_bytes(B, g, V, stochastic), 16),
+                     dtype=torch.uint8, device=dev)
+    for _ in range(2):          # the second call finds the head the first one left
+        gres = run(dev, ws, "compact", tgt, tokens, cu, w, stochastic, drf, kernel, **kw)
+        rres = ref("compact", tgt, tokens, cu, w, stochastic, drf, **kw)
         check(gres, rres, stochastic, 0)
 
 
