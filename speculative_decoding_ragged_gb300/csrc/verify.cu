@@ -451,7 +451,8 @@ verify_finalize_kernel(FinalArgs A)
 // exceeds u' * R; a residual summing to zero falls back to p; rounding that leaves no crossing
 // takes the last token with positive weight in the last candidate tile.
 template <int DT>
-__device__ void bonus_pick(const FinalArgs& A, int b, const BonusJob& job, int n_hist)
+__device__ void bonus_pick(const FinalArgs& A, int b, const BonusJob& job, int n_hist,
+                           const int* drafts)
 {
     constexpr int E = (DT == DSPARK_BF16) ? 2 : 4;
     constexpr int kWarps = kPickThreads / 32;
@@ -592,7 +593,7 @@ __device__ void bonus_pick(const FinalArgs& A, int b, const BonusJob& job, int n
         const int64_t row0 = static_cast<int64_t>(b) * A.gamma;
         const int Lc = static_cast<int>(job.slot - row0) + 1;
         int tok = -1;
-        if (lane < Lc - 1) tok = __ldg(A.tokens + row0 + lane + 1);
+        if (lane < Lc - 1) tok = drafts[lane];       // block token lane + 1, loaded before the wait
         else if (lane == Lc - 1) tok = chosen;
         const int sb = scatter_request(b, Lc, A.gamma, tok, lane, A.out_tokens, A.out_len,
                                        A.out_cap, n_hist);
@@ -622,6 +623,9 @@ bonus_final_kernel(FinalArgs A, int ctas_per_request)
     constexpr int E = (DT == DSPARK_BF16) ? 2 : 4;
     __shared__ float mp_s[DSPARK_MAX_GAMMA], zp_s[DSPARK_MAX_GAMMA];
     __shared__ float mq_s[DSPARK_MAX_GAMMA], zq_s[DSPARK_MAX_GAMMA];
+    __shared__ uint64_t ub_s[DSPARK_MAX_GAMMA];
+    __shared__ float u_s[DSPARK_MAX_GAMMA];
+    __shared__ int d_s[DSPARK_MAX_GAMMA];             // the drafts, for the fused scatter
     __shared__ BonusJob job_s;
     const int b = blockIdx.x / ctas_per_request;
     const int cta = blockIdx.x - b * ctas_per_request;
@@ -659,6 +663,17 @@ bonus_final_kernel(FinalArgs A, int ctas_per_request)
                                 (static_cast<int64_t>(b) * L + lane) * A.V * E, d_mine);
     }
     const int n_hist = (A.out_tokens != nullptr && warp == 0) ? A.out_len[b] : 0;
+    // the position's uniforms (Philox4x64-10 of request, position, step and seed, all call
+    // inputs): word 0 for the accept test, word 1 for a bonus drawn there; kept in shared
+    // memory by the lane that reads them back in the walk
+    if (warp == 0) d_s[lane] = d_mine;
+    if (warp == 0 && lane < nrows) {
+        uint64_t rnd[4];
+        philox4x64_10(static_cast<uint64_t>(b), static_cast<uint64_t>(lane), A.step, 0ull,
+                      A.seed, 0ull, rnd);
+        ub_s[lane] = rnd[1] >> 11;                    // u' = ub * 2^-53
+        u_s[lane] = static_cast<float>(rnd[0] >> 40) * 0x1p-24f;
+    }
     pdl_wait_and_trigger();
     reset_ws_head(A.head);
 
@@ -675,20 +690,17 @@ bonus_final_kernel(FinalArgs A, int ctas_per_request)
     if (warp == 0) {
         const bool writer = cta == 0;
         if (tested && !valid) bits |= DSPARK_STATUS_BAD_TOKEN;
-        uint64_t ub = 0;
         bool acc = false;
+        uint64_t ub = 0;
         if (lane < nrows) {
-            uint64_t rnd[4];
-            philox4x64_10(static_cast<uint64_t>(b), static_cast<uint64_t>(lane), A.step, 0ull,
-                          A.seed, 0ull, rnd);
-            ub = rnd[1] >> 11;                      // u' = ub * 2^-53
+            ub = ub_s[lane];
             float pp = -1.0f, qq = -1.0f;
             if (tested && valid) {
                 // fp32 (FP64 is scarce here): exponents relative to each row's maximum, and the
                 // ratio as one exp2 of their difference, so p/q neither under- nor overflows
                 const float ep = (lp - mp_s[lane]) * A.s;
                 const float eq = (lq - mq_s[lane]) * A.s;
-                const float u = static_cast<float>(rnd[0] >> 40) * 0x1p-24f;
+                const float u = u_s[lane];
                 if (lq == -INFINITY) {
                     acc = true;                     // q(d) = 0
                 } else {
@@ -794,7 +806,7 @@ bonus_final_kernel(FinalArgs A, int ctas_per_request)
     }
     __syncthreads();
     if (!last_s) return;
-    bonus_pick<DT>(A, b, job, n_hist);
+    bonus_pick<DT>(A, b, job, n_hist, d_s);
 }
 
 template <int DT, bool STOCH>
