@@ -259,27 +259,42 @@ __device__ __forceinline__ void combine_soft_rows(const FinalArgs& A, int64_t ba
                 }
             }
         }
+        // the batch's rows side by side, so that their shuffle trees overlap (each row's own
+        // operations keep their order: the same bits as one row at a time)
+        float m[RB], z[RB], M[RB], zz[RB];
 #pragma unroll
         for (int r = 0; r < RB; ++r) {
-            const int j = j0 + r * step;
-            if (j >= n) break;
-            float m = -INFINITY, z = 0.0f;
+            m[r] = -INFINITY;
+            z[r] = 0.0f;
 #pragma unroll
             for (int c = 0; c < CPL; ++c) {
                 if (p[r][c].m == -INFINITY) continue;
-                if (p[r][c].m > m) {
-                    z *= ex2_approx((m - p[r][c].m) * A.s);
-                    m = p[r][c].m;
+                if (p[r][c].m > m[r]) {
+                    z[r] *= ex2_approx((m[r] - p[r][c].m) * A.s);
+                    m[r] = p[r][c].m;
                 }
-                z += p[r][c].z * ex2_approx((p[r][c].m - m) * A.s);
+                z[r] += p[r][c].z * ex2_approx((p[r][c].m - m[r]) * A.s);
             }
-            float M = m;
-            for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-            float zz = m != -INFINITY ? z * ex2_approx((m - M) * A.s) : 0.0f;
-            for (int off = 16; off > 0; off >>= 1) zz += __shfl_xor_sync(0xffffffffu, zz, off);
-            if (lane == 0) {
-                if (j < nrows) { m_t[j] = M; z_t[j] = zz; }
-                else { m_d[j - nrows] = M; z_d[j - nrows] = zz; }
+            M[r] = m[r];
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+            for (int r = 0; r < RB; ++r) M[r] = fmaxf(M[r], __shfl_xor_sync(0xffffffffu, M[r], off));
+#pragma unroll
+        for (int r = 0; r < RB; ++r)
+            zz[r] = m[r] != -INFINITY ? z[r] * ex2_approx((m[r] - M[r]) * A.s) : 0.0f;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+            for (int r = 0; r < RB; ++r) zz[r] += __shfl_xor_sync(0xffffffffu, zz[r], off);
+        if (lane == 0) {
+#pragma unroll
+            for (int r = 0; r < RB; ++r) {
+                const int j = j0 + r * step;
+                if (j >= n) break;
+                if (j < nrows) { m_t[j] = M[r]; z_t[j] = zz[r]; }
+                else { m_d[j - nrows] = M[r]; z_d[j - nrows] = zz[r]; }
             }
         }
     }
@@ -290,8 +305,13 @@ __device__ __forceinline__ void combine_request_rows(const FinalArgs& A, int64_t
                                                      float* m_t, float* z_t, float* m_d,
                                                      float* z_d)
 {
+    // batches of rows as wide as the warps usually hold: few chunks per row come with large
+    // batches (B*gamma > 128 rows), whose requests give a warp two rows at gamma = 8; 33-64
+    // chunks come with at most 64 rows (batch-1 decoding: four rows per warp at gamma = 16).
+    // Shuffle trees of absent rows would only take issue slots, and each variant adds code
+    // that a call from cold caches must fetch.
     if (A.nc <= 32) {
-        combine_soft_rows<4, 1>(A, base, nrows, ndec, warp, warps, lane, m_t, z_t, m_d, z_d);
+        combine_soft_rows<2, 1>(A, base, nrows, ndec, warp, warps, lane, m_t, z_t, m_d, z_d);
     } else if (A.nc <= 64) {
         combine_soft_rows<4, 2>(A, base, nrows, ndec, warp, warps, lane, m_t, z_t, m_d, z_d);
     } else if (A.nc <= 128) {
