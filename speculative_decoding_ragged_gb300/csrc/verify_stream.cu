@@ -130,9 +130,10 @@ verify_stream_kernel(StreamArgs A)
 // launch from 178 to 170.5 us; a fifth, a third or all of the units by ticket landed within a
 // microsecond of that, a tenth or a twentieth gained less (172-174 us at high load). Each
 // CTA's first unit is fixed so that the head's tag, one L2 or DRAM round trip, is read while
-// that unit's copy is in flight instead of before it; where that unit is certainly a target
-// row its copy even starts before the PDL wait (same-box A/B: chained steps 0.3-0.6 us
-// shorter, large-vocab and high-load).
+// that unit's copy is in flight instead of before it. (Starting that copy before the PDL wait,
+// where the unit is certainly a target row, shortened the bench's chained steps by 0.3-0.6 us
+// only by overlapping the schedule-and-pack kernel, which a serving loop separates from verify
+// by the target forward; isolated launches did not move. Not kept.)
 // Measured on GB300 (whole steps of the large-vocab and high-load workloads): 4 consumer warps,
 // chunks of up to 12288 elements and a 96 KB ring (four stages of up to 24 KB, two CTAs per SM,
 // eight chunks in flight per SM) beat chunks of 2048-8192 elements in 32-80 KB rings (three or
@@ -166,13 +167,6 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
 {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-// Raises the barrier's expected transaction bytes without an arrival (the arrive comes later).
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
 }
 
@@ -261,8 +255,7 @@ verify_bulk_kernel(StreamArgs A, int stages, int stage_bytes)
     __shared__ __align__(8) uint64_t full_bar[kBulkMaxStages];
     __shared__ __align__(8) uint64_t empty_bar[kBulkMaxStages];
     __shared__ int64_t stage_job[kBulkMaxStages];     // the unit each stage holds (row job,
-    __shared__ int stage_c[kBulkMaxStages];           // chunk); job -1: no more units, -2: a
-                                                      // discarded early copy
+    __shared__ int stage_c[kBulkMaxStages];           // chunk), or job -1: no more units
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
@@ -273,29 +266,6 @@ verify_bulk_kernel(StreamArgs A, int stages, int stage_bytes)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    // The producer lane starts the copy of its first unit (unit blockIdx.x) before the wait
-    // when that unit is a target row whatever the previous kernels wrote: the logits are an
-    // input no kernel of this library writes, and rows below B (compact: every request has a
-    // row) or below B*gamma (static, cap-accept) are target rows of the buffer. The stage's
-    // slot and its arrive follow the wait, once cu_seqlens has confirmed the row.
-    int64_t spec_job = -1;
-    int spec_c = 0;
-    if (warp == kBulkConsumers && lane == 0) {
-        int64_t safe = (A.mode == DSPARK_COMPACT) ? static_cast<int64_t>(A.B)
-                                                  : static_cast<int64_t>(A.B) * A.gamma;
-        safe = min(min(safe, static_cast<int64_t>(A.target_rows)), A.rows_max);
-        const int job0 = static_cast<int>(blockIdx.x) / A.nc;
-        if (job0 < safe) {
-            spec_job = job0;
-            spec_c = static_cast<int>(blockIdx.x) - job0 * A.nc;
-            const int v0 = spec_c * A.C;
-            const int v1 = min(A.V, v0 + A.C);
-            const uint32_t bytes = static_cast<uint32_t>(v1 - v0) * E;
-            mbar_expect_tx(smem_addr(&full_bar[0]), bytes);
-            bulk_load(smem_addr(ring), static_cast<const char*>(A.target) +
-                      (static_cast<int64_t>(job0) * A.V + v0) * E, bytes, smem_addr(&full_bar[0]));
-        }
-    }
     pdl_wait_and_trigger();
     zero_next_counters(A);
     int64_t n_t;
@@ -340,20 +310,7 @@ verify_bulk_kernel(StreamArgs A, int stages, int stage_bytes)
         int s = 0;
         uint32_t ph = 0;                              // parity of this use of stage s
         int64_t k = 0;
-        bool more;
-        if (spec_job >= 0) {
-            // the early copy of unit blockIdx.x: publish it as that unit, or, where the windows
-            // made fewer rows than B, discard it (job -2) and stream the unit in order
-            const bool keep = spec_job < n_t;
-            stage_job[0] = keep ? spec_job : -2;
-            stage_c[0] = spec_c;
-            mbar_arrive(smem_addr(&full_bar[0]));
-            k = 1;
-            if (++s == stages) { s = 0; ph ^= 1u; }
-            more = keep ? advance() : u < U || advance();
-        } else {
-            more = u < U || advance();
-        }
+        bool more = u < U || advance();
         for (; more; ++k, more = advance()) {
             int64_t job;
             int c;
@@ -416,13 +373,8 @@ verify_bulk_kernel(StreamArgs A, int stages, int stage_bytes)
         }
         const int64_t job = stage_job[s];
         const int c = stage_c[s];
-        if (job == -1) break;                         // the producer's end marker
-        UnitSrc src;
-        if (job >= 0) {
-            src = unit_source<E>(A, job, c, n_t, A.cu, A.windows);
-        } else {                                      // an early copy the producer discarded
-            src.skip = true;
-        }
+        if (job < 0) break;                           // the producer's end marker
+        const UnitSrc src = unit_source<E>(A, job, c, n_t, A.cu, A.windows);
         float a = -INFINITY, bsum = 0.0f;
         int idx = 0x7FFFFFFF;
         if (!src.skip) {

@@ -219,9 +219,7 @@ def test_a_window_reaching_into_the_next_request(dev, kernel, stochastic):
 @pytest.mark.parametrize("kernel", ["register", "bulk"])
 @pytest.mark.parametrize("stochastic", [False, True])
 def test_fewer_rows_than_requests(dev, kernel, stochastic):
-    # cu_seqlens puts two requests on each row, so its total (32) is below B (64): the bulk
-    # kernel starts its first copy before the wait when that unit's row is below B, and must
-    # discard the copies of rows 32..63 (units that are no target rows after all); the
+    # cu_seqlens puts two requests on each row, so its total (32) is below B (64): the
     # even requests share their tested row with the next request (bad rows, as the oracle has
     # it), the odd ones share only their last row and are verified
     wl = (synth.WORKLOADS["stochastic"] if stochastic else synth.WORKLOADS["large_vocab_mixed"])
