@@ -395,7 +395,8 @@ int dspark_verify_noalloc(dspark_mode mode, int stochastic,
 const char* dspark_last_error(void);
 
 /* ABI version: 100 * major + minor (1.1: the dspark_graph_* capture and replay calls; 1.2: a
- * 256-byte head in the verify workspace). */
+ * 256-byte head in the verify workspace, and a stochastic workspace without per-request bonus
+ * jobs). */
 int dspark_version(void);
 
 #ifdef __cplusplus

@@ -50,8 +50,8 @@ __device__ __forceinline__ void philox4x64_10(uint64_t c0, uint64_t c1, uint64_t
     out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
 }
 
-// The bonus draw of one request, decided by the finaliser and carried out by the bonus kernel
-// (stochastic verify).
+// The bonus draw of one request (stochastic verify): decided by warp 0 of each bonus-kernel CTA
+// of the request and handed to the CTA's warps through shared memory.
 struct BonusJob {
     int64_t trow;   // target row of the bonus position
     int64_t drow;   // draft row of a residual draw; -1 for a draw from p
@@ -74,7 +74,6 @@ struct FinalArgs {
     int32_t* ceiling;
     float* row_prob;
     int32_t* status;
-    BonusJob* jobs;   // [B] (stochastic)
     float* tiles;     // [B][n_tiles][2]: residual and p weight sums per 256-token tile
     unsigned* done;   // [B]: tile CTAs finished per request (zeroed by the streaming kernel)
     WsHead* head;     // the workspace head, left ready for the next call
@@ -831,7 +830,7 @@ bonus_final_kernel(FinalArgs A, int ctas_per_request)
 
 template <int DT, bool STOCH>
 int run_verify(const VerifyCall& c, const Plan& plan, WsHead* head, void* part_t, void* part_d,
-               void* jobs, void* tiles, cudaStream_t stream)
+               unsigned* done, void* tiles, cudaStream_t stream)
 {
     const int L = c.gamma - 1;
     const double inv_t = STOCH ? 1.0 / static_cast<double>(c.temperature) : 1.0;
@@ -861,7 +860,7 @@ int run_verify(const VerifyCall& c, const Plan& plan, WsHead* head, void* part_t
     sa.rows_max = plan.rows_max;
     sa.s = s;
     // stochastic: the bonus kernel's per-request counters, zeroed by the streaming kernel
-    sa.zero = STOCH ? reinterpret_cast<unsigned*>(static_cast<BonusJob*>(jobs) + c.B) : nullptr;
+    sa.zero = STOCH ? done : nullptr;
     sa.n_zero = STOCH ? c.B : 0;
     sa.head = head;
 
@@ -893,8 +892,7 @@ int run_verify(const VerifyCall& c, const Plan& plan, WsHead* head, void* part_t
     fa.target_rows = c.target_rows;
     fa.rows_max = plan.rows_max;
     fa.s = s;
-    fa.jobs = static_cast<BonusJob*>(jobs);
-    fa.done = reinterpret_cast<unsigned*>(static_cast<BonusJob*>(jobs) + c.B);
+    fa.done = done;
     fa.tiles = static_cast<float*>(tiles);
     fa.head = head;
     fa.out_tokens = c.out_tokens;
@@ -926,10 +924,10 @@ int run_verify(const VerifyCall& c, const Plan& plan, WsHead* head, void* part_t
 }  // namespace
 
 // Workspace layout: the head (state handed from call to call); target-row partials; then,
-// stochastic only, draft-row partials, the bonus jobs [B] with their counters [B] and the bonus
+// stochastic only, draft-row partials, the bonus kernel's per-request counters [B] and the bonus
 // tile sums [B][n_tiles][2].
 struct WsLayout {
-    size_t part, jobs, tiles, total;
+    size_t part, done, tiles, total;
 };
 
 WsLayout ws_layout(int B, int gamma, int V, int stochastic)
@@ -943,9 +941,9 @@ WsLayout ws_layout(int B, int gamma, int V, int stochastic)
         l.total = kWsHeadBytes + l.part;
         return l;
     }
-    l.jobs = align_up((sizeof(BonusJob) + sizeof(unsigned)) * static_cast<size_t>(B), 256);
+    l.done = align_up(sizeof(unsigned) * static_cast<size_t>(B), 256);
     l.tiles = align_up(sizeof(float) * 2 * static_cast<size_t>(B) * ((V + 255) / 256), 256);
-    l.total = kWsHeadBytes + 2 * l.part + l.jobs + l.tiles;
+    l.total = kWsHeadBytes + 2 * l.part + l.done + l.tiles;
     return l;
 }
 
@@ -971,15 +969,15 @@ int launch_verify(const VerifyCall& c, cudaStream_t stream)
     char* ws = static_cast<char*>(c.ws) + kWsHeadBytes;
     void* part_t = ws;
     void* part_d = c.stochastic ? ws + lay.part : nullptr;
-    void* jobs = c.stochastic ? ws + 2 * lay.part : nullptr;
-    void* tiles = c.stochastic ? ws + 2 * lay.part + lay.jobs : nullptr;
+    unsigned* done = c.stochastic ? reinterpret_cast<unsigned*>(ws + 2 * lay.part) : nullptr;
+    void* tiles = c.stochastic ? ws + 2 * lay.part + lay.done : nullptr;
     if (c.dtype == DSPARK_BF16)
         return c.stochastic
-                   ? run_verify<DSPARK_BF16, true>(c, plan, head, part_t, part_d, jobs, tiles, stream)
-                   : run_verify<DSPARK_BF16, false>(c, plan, head, part_t, part_d, jobs, tiles, stream);
+                   ? run_verify<DSPARK_BF16, true>(c, plan, head, part_t, part_d, done, tiles, stream)
+                   : run_verify<DSPARK_BF16, false>(c, plan, head, part_t, part_d, done, tiles, stream);
     return c.stochastic
-               ? run_verify<DSPARK_F32, true>(c, plan, head, part_t, part_d, jobs, tiles, stream)
-               : run_verify<DSPARK_F32, false>(c, plan, head, part_t, part_d, jobs, tiles, stream);
+               ? run_verify<DSPARK_F32, true>(c, plan, head, part_t, part_d, done, tiles, stream)
+               : run_verify<DSPARK_F32, false>(c, plan, head, part_t, part_d, done, tiles, stream);
 }
 
 }  // namespace dspark

@@ -94,12 +94,12 @@ def test_workspace_size_is_a_function_of_sizes(lib):
     g = bd.dspark_verify_workspace_bytes(256, 8, 151936, False)
     s = bd.dspark_verify_workspace_bytes(256, 8, 151936, True)
     # a 256-byte head, then the target partials (8 B per chunk of each of the B*gamma rows);
-    # stochastic adds the draft partials (as many, 8 B each), a 48-byte bonus job and a 4-byte
-    # counter per request, and two fp32 sums per 256-token tile per request
+    # stochastic adds the draft partials (as many, 8 B each), a 4-byte counter per request and
+    # two fp32 sums per 256-token tile per request
     align = lambda x: (x + 255) // 256 * 256
     part = g - 256
     assert part > 0 and part % 256 == 0
-    assert s == 256 + 2 * part + align(52 * 256) + align(8 * 256 * ((151936 + 255) // 256))
+    assert s == 256 + 2 * part + align(4 * 256) + align(8 * 256 * ((151936 + 255) // 256))
     assert bd.dspark_verify_workspace_bytes(-1, 8, 10, False) == 0
     assert "bad sizes" in bd.last_error()
 
