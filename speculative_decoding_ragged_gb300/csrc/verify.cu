@@ -151,18 +151,6 @@ __device__ __forceinline__ void bonus_weights_of(const float (&xp)[8], const flo
     }
 }
 
-// The same weights, loading the logits first.
-template <int DT>
-__device__ __forceinline__ void bonus_weights(const char* trow, const char* drow, int v0, int V,
-                                              int vec, bool residual, float mp, float izp,
-                                              float mq, float izq, float s, float (&w)[8])
-{
-    float xp[8], xq[8];
-    load8<DT>(trow, v0, V, vec, xp);
-    if (residual) load8<DT>(drow, v0, V, vec, xq);
-    bonus_weights_of<DT>(xp, xq, v0, V, residual, mp, izp, mq, izq, s, w);
-}
-
 __device__ __forceinline__ float sum8(const float (&w)[8])
 {
     return ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
