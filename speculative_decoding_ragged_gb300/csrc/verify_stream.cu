@@ -91,10 +91,35 @@ verify_stream_kernel(StreamArgs A)
     const int64_t GW = static_cast<int64_t>(gridDim.x) * kStreamWarps;
     int64_t n_t;
     const int64_t U = unit_count<STOCH>(A, n_t, cu);
-    const int64_t u0 = gw * U / GW, u1 = (gw + 1) * U / GW;
 
-    int64_t job = u0 / A.nc;
-    int c = static_cast<int>(u0 - job * A.nc);
+    // At most one unit per warp: warp gw takes unit gw, so whole CTAs are busy and the rest
+    // exit at once. Else contiguous runs [gw U / GW, (gw + 1) U / GW), split in 32-bit
+    // arithmetic where GW * U fits (the chunk plan keeps U near 4096 units): three 64-bit
+    // divisions are long software sequences, most of a warp's work when it holds one unit.
+    int64_t u0, u1, job;
+    int c;
+    if (U <= GW) {
+        const uint32_t g = static_cast<uint32_t>(gw);
+        const uint32_t q = g / static_cast<uint32_t>(A.nc);
+        u0 = gw;
+        u1 = gw < U ? gw + 1 : gw;
+        job = q;
+        c = static_cast<int>(g - q * static_cast<uint32_t>(A.nc));
+    } else if (U * GW <= 0x7fffffff) {
+        const uint32_t g = static_cast<uint32_t>(gw), W = static_cast<uint32_t>(GW);
+        const uint32_t Uu = static_cast<uint32_t>(U);
+        const uint32_t a = g * Uu / W, e = (g + 1) * Uu / W;
+        const uint32_t q = a / static_cast<uint32_t>(A.nc);
+        u0 = a;
+        u1 = e;
+        job = q;
+        c = static_cast<int>(a - q * static_cast<uint32_t>(A.nc));
+    } else {
+        u0 = gw * U / GW;
+        u1 = (gw + 1) * U / GW;
+        job = u0 / A.nc;
+        c = static_cast<int>(u0 - job * A.nc);
+    }
     for (int64_t u = u0; u < u1; ++u) {
         const UnitSrc src = unit_source<E>(A, job, c, n_t, cu, windows);
         if (++c == A.nc) { c = 0; ++job; }
