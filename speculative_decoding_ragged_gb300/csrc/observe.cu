@@ -34,8 +34,15 @@ observe_kernel(const float* __restrict__ conf, const int32_t* __restrict__ accep
     // utilisation terms
     const int64_t e = static_cast<int64_t>(blockIdx.x) * kThreads + tid;
     if (e < static_cast<int64_t>(B) * gamma) {
-        const int b = static_cast<int>(e / gamma);
-        const int j = static_cast<int>(e - static_cast<int64_t>(b) * gamma);
+        int b, j;
+        if (static_cast<int64_t>(B) * gamma <= 0x7fffffff) {   // a 32-bit division where it fits
+            const int ei = static_cast<int>(e);
+            b = ei / gamma;
+            j = ei - b * gamma;
+        } else {
+            b = static_cast<int>(e / gamma);
+            j = static_cast<int>(e - static_cast<int64_t>(b) * gamma);
+        }
         int c = ceiling_len[b];
         if (c < 1 || c > gamma) {
             bits |= DSPARK_STATUS_BAD_LENGTH;
