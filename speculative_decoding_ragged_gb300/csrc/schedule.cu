@@ -843,6 +843,9 @@ schedule_small_kernel(const float* __restrict__ conf, int B, int L, double bias,
     // everything above reads call inputs that no kernel of this library writes; outputs and
     // the tiers (which a pack of this library may have written) wait for the previous kernel
     pdl_wait_and_trigger();
+    // the first 64 tiers, loaded now so that the round trip overlaps the scheduling below
+    const int tier_lo = (PACK && lane < pk.n_tiers) ? __ldg(pk.tiers + lane) : INT_MAX;
+    const int tier_hi = (PACK && lane + 32 < pk.n_tiers) ? __ldg(pk.tiers + lane + 32) : INT_MAX;
 
     // 1. survival key and rank word of the lane's candidate
     float sv = 1.0f;
@@ -938,7 +941,9 @@ schedule_small_kernel(const float* __restrict__ conf, int B, int L, double bias,
         }
         if (lane == 0) pk.cu[B] = M;
         int best = INT_MAX;
-        for (int t = lane; t < pk.n_tiers; t += 32) {
+        if (tier_lo >= M) best = tier_lo;
+        if (tier_hi >= M && tier_hi < best) best = tier_hi;
+        for (int t = 64 + lane; t < pk.n_tiers; t += 32) {
             const int tv = __ldg(pk.tiers + t);
             if (tv >= M && tv < best) best = tv;
         }
