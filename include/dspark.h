@@ -232,8 +232,9 @@ int dspark_schedule_pack(const float* conf, int B, int gamma, const dspark_cost*
  * streaming, see dspark_set_stream_kernel), then, greedy: one CTA per request that combines
  * the chunk results, walks and writes the outputs; stochastic: a bonus kernel spread over the
  * grid whose CTAs each combine their request's chunk results and run its accept tests, sum
- * the bonus row's weights over their tiles, and whose last CTA per request draws the bonus and
- * writes the outputs.
+ * the bonus row's weights over their tiles; CTA 0 of a request writes its accept length,
+ * drafts and ceiling, and the request's last CTA to finish draws the bonus token and, in
+ * dspark_verify_scatter, appends the request's tokens.
  * ------------------------------------------------------------------------------------- */
 int dspark_verify(dspark_mode mode, int stochastic,
                   const void* target_logits, int target_rows, const void* draft_logits,
