@@ -280,6 +280,28 @@ def test_random_cu_seqlens_against_the_oracle(dev, case):
         check(gres, rres, stochastic, 0)
 
 
+@pytest.mark.parametrize("kernel", ["register", "bulk"])
+@pytest.mark.parametrize("T", [0.02, 0.1, 5.0, 20.0])
+def test_extreme_temperatures(dev, kernel, T):
+    # a very sharp softmax (most exponentials underflow, p/q spans fp32's range) and a very
+    # flat one (the bonus draw's tile sums nearly uniform), compact and cap-accept
+    wl = synth.WORKLOADS["stochastic"].with_(B=24, V=8192, temperature=T, tiers=(192,))
+    bt = synth.make_batch(wl, seed=int(T * 100) + 3, stochastic=True)
+    B, g = bt.B, bt.gamma
+    w = oracle.schedule(bt.conf, bt.bias, bt.alpha, bt.theta)["windows"]
+    cu = np.concatenate([[0], np.cumsum(w)]).astype(np.int32)
+    kw = dict(temperature=T, seed=11, step=4)
+    ws = torch.empty(bd.dspark_verify_workspace_bytes(B, g, wl.V, True), dtype=torch.uint8,
+                     device=dev)
+    for mode in ("compact", "cap_accept"):
+        tgt = synth.gather_packed(bt.target, B, g, w) if mode == "compact" else bt.target
+        gres = run(dev, ws, mode, tgt, bt.tokens, cu if mode == "compact" else None, w, True,
+                   bt.draft, kernel, **kw)
+        rres = ref(mode, tgt, bt.tokens, cu if mode == "compact" else None, w, True, bt.draft,
+                   **kw)
+        check(gres, rres, True, tgt.shape[0])
+
+
 def test_register_kernel_with_more_units_than_a_32_bit_split_holds(dev):
     # stochastic compact at the largest batch with full windows: 8192 x 32 target rows and as
     # many draft jobs, one chunk each (V = 256), 524288 units for the register kernel's 4864
