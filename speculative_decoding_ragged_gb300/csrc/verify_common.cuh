@@ -77,7 +77,7 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // that finds either tag missing (a fresh or cleared workspace, or a former workspace whose
 // first bytes another tensor has since written) splits all of its units evenly instead: the
 // same partials, only the balance of the tail differs. Tickets add 2^32 to the first word, so
-// the low tag never changes while a kernel runs and every CTA reads the same verdict.
+// the low tag never changes while a kernel runs and every CTA reaches the same decision.
 struct WsHead {
     unsigned long long word;       // low 32 bits: kWsHeadTag32; high 32 bits: units handed out
     unsigned long long tag;        // kWsHeadTag64
