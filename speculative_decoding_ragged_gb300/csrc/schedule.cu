@@ -805,9 +805,11 @@ __global__ void schedule_trivial_kernel(int B, double bias, const double* __rest
 // ---- one warp for at most 32 candidates ---------------------------------------------------
 // The same outputs as schedule_kernel (and, with PACK, as the pack body) when n = B*(gamma-1)
 // <= 32: lane i holds candidate i; the warp sorts the candidates' rank words with a shuffle
-// bitonic network, scans their keys, evaluates the objective of every K exactly in fp64 (at
-// most 33 divisions, one or two per lane) and reduces with the same comparator, so no block
-// barrier is needed anywhere. A batch of one request lives here.
+// bitonic network (a single request's are in order already), scans their keys, evaluates the
+// objective of every K exactly in fp64 (one division per lane, side by side; lane 0 takes a
+// second only when n = 32: on this part one fp64 division costs about a third of a
+// microsecond) and reduces with the same comparator, so no block barrier is needed anywhere.
+// A batch of one request lives here.
 constexpr int kSmallMax = 32;
 
 template <bool PACK>
@@ -855,14 +857,18 @@ schedule_small_kernel(const float* __restrict__ conf, int B, int L, double bias,
     const uint32_t k32 = sv >= 1.0f ? 0xFFFFFFFFu : __float2uint_rn(__fmul_rn(sv, 4294967296.0f));
     uint64_t w = mine ? rank_word(k32, lane) : 0ull;   // 0 sorts after every candidate
 
-    // 2. bitonic sort of the 32 words, descending
+    // 2. bitonic sort of the 32 words, descending. One request's words are in order already:
+    // its survivals never grow along the block and its indices rise, so its keys fall or stay
+    // and its words fall, with the empty lanes' zeros after them.
+    if (B > 1) {
 #pragma unroll
-    for (int k = 2; k <= 32; k <<= 1) {
+        for (int k = 2; k <= 32; k <<= 1) {
 #pragma unroll
-        for (int j = k >> 1; j > 0; j >>= 1) {
-            const uint64_t o = __shfl_xor_sync(full, w, j);
-            const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
-            w = keep_max ? (w > o ? w : o) : (w < o ? w : o);
+            for (int j = k >> 1; j > 0; j >>= 1) {
+                const uint64_t o = __shfl_xor_sync(full, w, j);
+                const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
+                w = keep_max ? (w > o ? w : o) : (w < o ? w : o);
+            }
         }
     }
     const uint32_t kp = static_cast<uint32_t>(w >> 32);
@@ -876,18 +882,20 @@ schedule_small_kernel(const float* __restrict__ conf, int B, int L, double bias,
         if (lane >= off) S += v;
     }
 
-    // 4. exact objectives and the argmax (larger objective, then smaller K)
+    // 4. exact objectives and the argmax (larger objective, then smaller K). Lane i < n takes
+    // K = i + 1 and lane n, when there is one, K = 0, so that the divisions run side by side.
     const uint64_t base_E = static_cast<uint64_t>(B) << 32;
     uint64_t best_obj = 0;
     int best_k = -1;
-    if (lane < n) {
-        const double T = t0 + __longlong_as_double(th_k);
+    if (lane <= n) {
+        const bool k0 = lane == n;
+        const double T = t0 + __longlong_as_double(k0 ? th_0 : th_k);
         if (T > 0.0 && T < INFINITY) {
-            best_obj = __double_as_longlong(static_cast<double>(base_E + S) / T);
-            best_k = lane + 1;
+            best_obj = __double_as_longlong(static_cast<double>(k0 ? base_E : base_E + S) / T);
+            best_k = k0 ? 0 : lane + 1;
         }
     }
-    if (lane == 0) {
+    if (n == 32 && lane == 0) {
         const double T = t0 + __longlong_as_double(th_0);
         if (T > 0.0 && T < INFINITY) {
             const uint64_t o = __double_as_longlong(static_cast<double>(base_E) / T);
