@@ -16,12 +16,15 @@
 //      a bucket is too big (many equal keys), a stable merge of the runs instead. Larger n: a
 //      bitonic sort of 64-bit words key << 31 | (2^31 - 1 - index);
 //   3. block-wide inclusive scan of the keys (exact uint64 sums S(K));
-//   4. obj(K) = double(B*2^32 + S(K)) / T(K). FP64 throughput is scarce on this part, so an
-//      fp32 screen (theta read from its bits with integer operations, error < 1e-6 relative)
-//      finds the K within 1e-5 of the best and only those, plus any K the screen cannot
-//      judge (negative or extreme T), get the exact fp64 evaluation, gathered onto as few
-//      lanes as possible; the argmax compares the objectives' bit patterns as integers (they
-//      are positive) and takes the smallest K among equal objectives;
+//   4. obj(K) = double(B*2^32 + S(K)) / T(K), argmax K*, the smallest K among equal
+//      objectives. FP64 latency is long on this part, and K* is an output while the
+//      objective is not: a double-float screen (pairs of fp32 values, error below 2^-42
+//      relative, as 64-bit keys that order like the objective) gives each K a key, and one
+//      block reduction finds the best key, its K and the runner-up. K* is that K when every
+//      other key lies more than 2^-37 below and every K was judged; ties, near ties and cost
+//      tables the screen cannot judge (negative or out-of-range terms) take the exact fp64
+//      objectives of the K within the margin or not judged, and an argmax over those that
+//      compares the objectives' bit patterns as integers (they are positive);
 //   5. windows w_b = 1 + count of request b among the first K* candidates: with the ranks,
 //      the length of the prefix of its run ranked below K*.
 // Latency-bound (microseconds); the grid is one CTA by construction of the problem. Every
@@ -45,8 +48,10 @@ constexpr int kBuckets = 4096;           // 128 buckets per power of two of the 
 constexpr int kBucketsPerThread = kBuckets / kThreads;
 constexpr int kTiersPerThread = (DSPARK_MAX_TIERS + kThreads - 1) / kThreads;
 constexpr int kBucketMax = 64;           // larger buckets (many equal keys): merge instead
-constexpr float kScreen = 1.0f - 1e-5f;  // fp32 screen: candidates within 1e-5 of the best
-constexpr float kTmin = 1e-20f, kTmax = 1e20f;   // T range the fp32 screen judges
+// The screened best decides K* alone when every other key lies more than this below it:
+// 2^19 key units, at least 2^-37 of the objective, sixteen times the 2^-41 that two screened
+// values' errors (each below 2^-42 relative) can add up to.
+constexpr uint64_t kKeyMargin = 1ull << 19;
 
 // Objectives are positive doubles (or "none" = 0), whose bit patterns order like the values:
 // compare them as integers, the larger objective first, then the smaller K.
@@ -55,39 +60,111 @@ __device__ __forceinline__ bool better(uint64_t o1, int k1, uint64_t o2, int k2)
     return o1 > o2 || (o1 == o2 && static_cast<unsigned>(k1) < static_cast<unsigned>(k2));
 }
 
-// A non-negative finite double as fp32 by truncating its fields (relative error < 2^-23),
-// with integer operations only. ok = false for negative, infinite, NaN or too-large values.
-__device__ __forceinline__ float nonneg_double_to_float(uint64_t bits, bool& ok)
+// ---- the screen: obj(K) in double-float arithmetic (pairs of fp32 values) ----
+// The exact objective is an fp64 division, and FP64 latency on this part is long (one
+// division about 660 cycles). K* is an output but the objective is not, so a screen accurate
+// to 2^-40 relative decides K* whenever the best screened K beats every other by more than
+// twice that; only ties, near ties and cost tables the screen cannot judge take fp64.
+struct DF {
+    float h, l;     // value h + l, |l| <= ulp(h) / 2 once normalised
+};
+
+__device__ __forceinline__ DF fast_two_sum(float a, float b)   // |a| >= |b|: exact split
 {
-    const uint32_t hi = static_cast<uint32_t>(bits >> 32);
-    const int ex = static_cast<int>((hi >> 20) & 0x7FF);
-    if ((hi >> 31) != 0 && (bits << 1) != 0) { ok = false; return 0.0f; }   // negative
-    if (ex == 0x7FF) { ok = false; return 0.0f; }                            // inf, NaN
-    const int ef = ex - 1023 + 127;
-    if (ef >= 255) { ok = false; return 0.0f; }
-    if (ef <= 0) return 0.0f;                                                 // below fp32 range
-    const uint32_t mant = static_cast<uint32_t>(bits >> 29) & 0x7FFFFFu;
-    return __uint_as_float((static_cast<uint32_t>(ef) << 23) | mant);
+    const float s = __fadd_rn(a, b);
+    return {s, __fsub_rn(b, __fsub_rn(s, a))};
 }
 
-// fp32 approximation of an exact objective numerator E < 2^53 (two rounded halves).
-__device__ __forceinline__ float e_to_float(uint64_t E)
+__device__ __forceinline__ DF two_sum(float a, float b)        // any order: exact split
 {
-    return fmaf(__uint2float_rn(static_cast<uint32_t>(E >> 32)), 4294967296.0f,
-                __uint2float_rn(static_cast<uint32_t>(E)));
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    return {s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb))};
 }
 
-// The screen for one K: returns true if K must be evaluated exactly regardless of the
-// screen (the screen cannot judge T), else writes the approximate objective to f.
-__device__ __forceinline__ bool screen(uint64_t E, float t0f, bool t0_ok, uint64_t theta_bits,
-                                       float& f)
+// x (bits of a double) as h + l: h its top 24 significand bits, exactly, l the next 29
+// rounded once (relative error < 2^-47). False unless x is 0 or in [2^-60, 2^61).
+__device__ __forceinline__ bool split_double(uint64_t bits, DF& out)
 {
-    bool ok = t0_ok;
-    const float th = nonneg_double_to_float(theta_bits, ok);
-    const float T = t0f + th;
-    if (!ok || !(T >= kTmin && T <= kTmax)) return true;
-    f = __fdividef(e_to_float(E), T);
-    return false;
+    if (bits == 0) {
+        out = {0.0f, 0.0f};
+        return true;
+    }
+    const int e = static_cast<int>(bits >> 52);           // biased exponent, sign bit included
+    if (e < 1023 - 60 || e > 1023 + 60) return false;     // negative, tiny, huge, inf or NaN
+    const uint64_t m = (bits & ((1ull << 52) - 1)) | (1ull << 52);   // x = m 2^(e - 1075)
+    const float sh = __int_as_float((e - 1075 + 29 + 127) << 23);    // 2^(e - 1046)
+    const float sl = __int_as_float((e - 1075 + 127) << 23);         // 2^(e - 1075)
+    out = fast_two_sum(__fmul_rn(__uint2float_rn(static_cast<uint32_t>(m >> 29)), sh),
+                       __fmul_rn(__uint2float_rn(static_cast<uint32_t>(m & 0x1FFFFFFFu)), sl));
+    return true;
+}
+
+// An integer 1 <= E < 2^53 as h + l (relative error < 2^-47).
+__device__ __forceinline__ DF split_u53(uint64_t E)
+{
+    const int sh = 40 - __clzll(static_cast<long long>(E));   // bits below the top 24
+    if (sh <= 0) return {__uint2float_rn(static_cast<uint32_t>(E)), 0.0f};
+    const float h = __fmul_rn(__uint2float_rn(static_cast<uint32_t>(E >> sh)),
+                              __int_as_float((sh + 127) << 23));
+    return fast_two_sum(h, __uint2float_rn(static_cast<uint32_t>(E & ((1ull << sh) - 1))));
+}
+
+// A key that grows with the positive value h + l, continuously across h: h's bits above, then
+// l in units of 2^-32 ulp(h) added with its sign, so that one step of h is 2^32 units and a key
+// difference measures the value difference (a unit is 2^-56 to 2^-55 of the value).
+__device__ __forceinline__ uint64_t df_key(DF g)
+{
+    const uint32_t hb = __float_as_uint(g.h);
+    const int eh = static_cast<int>(hb >> 23) - 127;
+    const long long lu = __float2ll_rn(__fmul_rn(g.l, __int_as_float((127 + 55 - eh) << 23)));
+    return (static_cast<uint64_t>(hb) << 32) + static_cast<uint64_t>(lu);
+}
+
+// The screen key of obj(K) = E / (t0 + theta), theta given by its bits, t0 split once by the
+// caller (t0_ok false: not judged). Returns 0 when the screen cannot judge this K (t0 or theta
+// negative, outside [2^-60, 2^61), or T = 0); the exact fp64 path then decides it. Error
+// budget, relative: E and both cost terms 2^-47 each, their sum 2^-46, the quotient (fp32
+// estimate, exact residual by fma, fp32 correction) 2^-43, against the fp64 objective's own
+// two roundings 2^-52: below 2^-42 in all.
+__device__ __forceinline__ uint64_t screen_key(uint64_t E, DF t0d, bool t0_ok, uint64_t theta_bits)
+{
+    DF thd;
+    if (!t0_ok || !split_double(theta_bits, thd)) return 0;
+    const DF s = two_sum(t0d.h, thd.h);
+    const DF T = fast_two_sum(s.h, __fadd_rn(__fadd_rn(t0d.l, thd.l), s.l));
+    if (!(T.h > 0.0f)) return 0;
+    const DF e = split_u53(E);
+    const float q1 = __fdividef(e.h, T.h);
+    const float ph = __fmul_rn(q1, T.h);
+    float r = __fsub_rn(e.h, ph);                      // exact: ph is within 2x of e.h
+    r = __fsub_rn(r, __fmaf_rn(q1, T.h, -ph));         // the product's rounding error
+    r = __fadd_rn(r, e.l);
+    r = __fmaf_rn(-q1, T.l, r);
+    return df_key(fast_two_sum(q1, __fdividef(r, T.h)));
+}
+
+// The largest 64-bit value over the warp.
+__device__ __forceinline__ uint64_t warp_max_u64(uint64_t x)
+{
+    const uint32_t hi = __reduce_max_sync(0xffffffffu, static_cast<uint32_t>(x >> 32));
+    const uint32_t lo = __reduce_max_sync(0xffffffffu, static_cast<uint32_t>(x >> 32) == hi
+                                                           ? static_cast<uint32_t>(x) : 0u);
+    return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+// The best key of the warp (the smallest K among equal keys), every other key's maximum (the
+// runner-up; a tie with the best counts), and whether any K went unjudged; each lane brings
+// its own best (k1, K1), second k2 and flag. Key 0 means none; K1 = -1 with key 0.
+__device__ __forceinline__ void warp_top2(uint64_t& k1, int& K1, uint64_t& k2, bool& nj)
+{
+    const uint64_t m = warp_max_u64(k1);
+    const int mK = static_cast<int>(__reduce_min_sync(
+        0xffffffffu, k1 == m ? static_cast<uint32_t>(K1) : 0xFFFFFFFFu));
+    k2 = warp_max_u64((k1 == m && K1 == mK) ? k2 : k1);
+    k1 = m;
+    K1 = mK;
+    nj = __any_sync(0xffffffffu, nj);
 }
 
 // The sorted run of request b: fixed-point survival keys. MERGE: 32-bit keys and indices in
@@ -163,11 +240,13 @@ __device__ __noinline__ uint64_t exact_objective(uint64_t E, double t0, uint64_t
     return static_cast<uint64_t>(__double_as_longlong(u53_to_double(E) / T));
 }
 
-__device__ __forceinline__ uint32_t lanemask_lt()
+// The exact objective for the one-warp kernel: the bits of double(E) / (t0 + theta), or 0
+// when the step time is not positive and finite.
+__device__ __forceinline__ uint64_t small_objective(uint64_t E, double t0, uint64_t theta_bits)
 {
-    uint32_t m;
-    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-    return m;
+    const double T = t0 + __longlong_as_double(static_cast<long long>(theta_bits));
+    if (!(T > 0.0 && T < INFINITY)) return 0;
+    return static_cast<uint64_t>(__double_as_longlong(static_cast<double>(E) / T));
 }
 
 // Element i of a small register array, by selects (no local memory under a rolled loop).
@@ -179,13 +258,6 @@ __device__ __forceinline__ T get_n(const T (&a)[N], int i)
     for (int k = 1; k < N; ++k) v = i == k ? a[k] : v;
     return v;
 }
-template <typename T, int N>
-__device__ __forceinline__ void set_n(T (&a)[N], int i, T v)
-{
-#pragma unroll
-    for (int k = 0; k < N; ++k) a[k] = i == k ? v : a[k];
-}
-
 // Sum over the warps before this one of a per-warp total, read by every lane of the warp from
 // shared memory after the barrier that published the totals (no second barrier).
 template <typename T>
@@ -365,8 +437,9 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
     int* count = MERGE ? (idst + n) : reinterpret_cast<int*>(word + n_pad);
     __shared__ uint64_t warp_total[kWarps];
     __shared__ uint64_t red_obj[kWarps];
+    __shared__ uint64_t red_sec[kWarps];
     __shared__ int red_k[kWarps];
-    __shared__ float red_f[kWarps];
+    __shared__ int red_nj[kWarps];
     __shared__ double t0_s;
     __shared__ __align__(16) int bucket_cnt[MERGE ? kBuckets : 4];
     __shared__ __align__(16) int bucket_start[MERGE ? kBuckets : 4];
@@ -606,24 +679,26 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
     const uint64_t S_excl = incl - run + warps_before(warp_total, warp, lane);
     const uint64_t base_E = static_cast<uint64_t>(B) << 32;
     const double t0 = t0_s;
-    bool t0_ok = true;
-    const float t0f = nonneg_double_to_float(static_cast<uint64_t>(__double_as_longlong(t0)), t0_ok);
+    DF t0d;
+    const bool t0_ok = split_double(static_cast<uint64_t>(__double_as_longlong(t0)), t0d);
 
-    // 4a. fp32 screen over the K this thread owns. MERGE keeps each K's screen value for the
-    // exact pass (+inf where the screen cannot judge, so that K is always evaluated exactly)
-    float fb = -INFINITY;
-    float fv[kMergeItems];
-#pragma unroll
-    for (int k = 0; k < kMergeItems; ++k) fv[k] = 0.0f;
-    float f_k0 = -INFINITY;
-    float f_hi = -INFINITY;      // the largest of this thread's screen values (+inf included)
-    if (tid == 0) {
-        float f = 0.0f;
-        const bool no = screen(base_E, t0f, t0_ok, th0, f);
-        if (!no) fb = f;
-        f_k0 = no ? INFINITY : f;
-        f_hi = f_k0;              // a queued K = 0 makes warp 0 walk (and drain) as well
-    }
+    // 4a. screen keys of the K this thread owns (thread 0 also K = 0): the thread keeps its
+    // two largest keys and the first one's K, and notes any K the screen cannot judge
+    uint64_t key1 = 0, key2 = 0;
+    int K1 = -1;
+    bool unjudged = false;
+    auto take = [&](uint64_t key, int K) {
+        if (key == 0) {
+            unjudged = true;
+        } else if (key > key1) {
+            key2 = key1;
+            key1 = key;
+            K1 = K;
+        } else if (key > key2) {
+            key2 = key;
+        }
+    };
+    if (tid == 0) take(screen_key(base_E, t0d, t0_ok, th0), 0);
     {
         uint64_t S = S_excl;
 #pragma unroll 1
@@ -631,107 +706,71 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
             const int p = p0 + it;
             if (it >= items || p >= n) break;
             S += key_at(p);
-            float f = 0.0f;
-            const bool no = screen(base_E + S, t0f, t0_ok, theta_at(it, p), f);
-            if (!no) fb = fmaxf(fb, f);
-            f_hi = fmaxf(f_hi, no ? INFINITY : f);
-            if (MERGE) set_n(fv, it, no ? INFINITY : f);
+            take(screen_key(base_E + S, t0d, t0_ok, theta_at(it, p)), p + 1);
         }
     }
-    for (int off = 16; off > 0; off >>= 1) fb = fmaxf(fb, __shfl_xor_sync(full, fb, off));
-    if (lane == 0) red_f[warp] = fb;
+    // the block's best key with its K, the runner-up and the unjudged flag: per warp, then
+    // every warp combines the 32 warp results itself behind one barrier
+    uint64_t bk = key1, b2 = key2;
+    int bK = K1;
+    bool nj = unjudged;
+    warp_top2(bk, bK, b2, nj);
+    if (lane == 0) {
+        red_obj[warp] = bk;
+        red_sec[warp] = b2;
+        red_k[warp] = bK;
+        red_nj[warp] = nj ? 1 : 0;
+    }
     __syncthreads();
-    float f_best = lane < kWarps ? red_f[lane] : -INFINITY;
-    for (int off = 16; off > 0; off >>= 1) f_best = fmaxf(f_best, __shfl_xor_sync(full, f_best, off));
-    const float thr = f_best * kScreen;
+    bk = lane < kWarps ? red_obj[lane] : 0;
+    b2 = lane < kWarps ? red_sec[lane] : 0;
+    bK = lane < kWarps ? red_k[lane] : -1;
+    nj = lane < kWarps && red_nj[lane] != 0;
+    warp_top2(bk, bK, b2, nj);
+    const uint64_t thr = bk > kKeyMargin ? bk - kKeyMargin : 0;
 
-    // 4b. exact objectives of the candidates (near the screen's best, or not screenable). MERGE:
-    // each warp queues its candidates in 32 slots of the bucket tables (free after the sort), in
-    // ballot order, and evaluates a full queue 32 at a time, so that a warp with at most 32
-    // candidates runs its FP64 divisions in one pass. The larger kernel evaluates in place.
-    uint64_t best_obj = 0;        // bit pattern of a positive double; 0 = none
-    int best_k = -1;
-    auto consider = [&](uint64_t E, uint64_t tb, int k) {
-        const uint64_t obj = exact_objective(E, t0, tb);
-        if (obj != 0 && better(obj, k, best_obj, best_k)) {
-            best_obj = obj;
-            best_k = k;
-        }
-    };
-    uint64_t* slot_e = reinterpret_cast<uint64_t*>(bucket_start) + 64 * warp;   // MERGE only
-    uint64_t* slot_t = slot_e + 32;
-    int* slot_k = bucket_cnt + 32 * warp;
-    int queued = 0;               // uniform across the warp
-    if (warp == 0 && __any_sync(full, tid == 0 && f_k0 >= thr)) {
-        if (!MERGE) {
-            if (tid == 0) consider(base_E, th0, 0);
-        } else {
-            if (lane == 0) {
-                slot_e[0] = base_E;
-                slot_t[0] = th0;
-                slot_k[0] = 0;
+    // 4b. the screened best is K* when every other K lies beyond the margin and every K was
+    // judged. Else (ties, near ties, cost tables the screen cannot judge) the exact fp64
+    // objective of every K not judged or within the margin, and the argmax over those. The
+    // branch is uniform across the block.
+    int K_star = bK;
+    bool none = false;
+    if (nj || bK < 0 || b2 >= thr) {
+        uint64_t best_obj = 0;        // bit pattern of a positive double; 0 = none
+        int best_k = -1;
+        auto consider = [&](uint64_t E, uint64_t tb, int k) {
+            const uint64_t key = screen_key(E, t0d, t0_ok, tb);
+            if (key != 0 && key < thr) return;
+            const uint64_t obj = exact_objective(E, t0, tb);
+            if (obj != 0 && better(obj, k, best_obj, best_k)) {
+                best_obj = obj;
+                best_k = k;
             }
-            queued = 1;
-        }
-    }
-    // only warps with a candidate walk their items: at 32 warps the others' uniform work
-    // would take issue slots from the ones that divide
-    if (__any_sync(full, f_hi >= thr)) {
-        uint64_t S = S_excl;
+        };
+        if (tid == 0) consider(base_E, th0, 0);
+        if (unjudged || key1 >= thr) {
+            uint64_t S = S_excl;
 #pragma unroll 1
-        for (int it = 0; it <= kMaxItems; ++it) {
-            const bool done = it >= items || it == kMaxItems;   // uniform across the warp
-            const int p = p0 + it;
-            bool cand = false;
-            uint64_t tb = 0;
-            if (!done && p < n) {
+            for (int it = 0; it < kMaxItems; ++it) {
+                const int p = p0 + it;
+                if (it >= items || p >= n) break;
                 S += key_at(p);
-                tb = theta_at(it, p);
-                if (MERGE) {
-                    cand = get_n(fv, it) >= thr;
-                } else {
-                    float f = 0.0f;
-                    cand = screen(base_E + S, t0f, t0_ok, tb, f) || f >= thr;
-                }
+                consider(base_E + S, theta_at(it, p), p + 1);
             }
-            if (!MERGE) {
-                if (cand) consider(base_E + S, tb, p + 1);
-                if (done) break;
-                continue;
-            }
-            const unsigned cm = __ballot_sync(full, cand);
-            if (queued > 0 && (done || queued + __popc(cm) > 32)) {   // one drain site
-                __syncwarp();
-                if (lane < queued) consider(slot_e[lane], slot_t[lane], slot_k[lane]);
-                __syncwarp();
-                queued = 0;
-            }
-            if (done) break;
-            if (cand) {
-                const int r = queued + __popc(cm & lanemask_lt());
-                slot_e[r] = base_E + S;
-                slot_t[r] = tb;
-                slot_k[r] = p + 1;
-            }
-            queued += __popc(cm);
         }
-    }
-    // the best (objective, K) of a warp, then of the block (the second pass: every warp combines
-    // the 32 warp results itself); a reduction runs only where more than one lane holds a result
-    // (candidates are few and sit in one or two warps)
+        // the best (objective, K) of a warp, then of the block (every warp combines the 32
+        // warp results itself)
 #pragma unroll 1
-    for (int pass = 0; pass < 2; ++pass) {
-        if (pass == 1) {
-            if (lane == 0) {
-                red_obj[warp] = best_obj;
-                red_k[warp] = best_k;
+        for (int pass = 0; pass < 2; ++pass) {
+            if (pass == 1) {
+                if (lane == 0) {
+                    red_obj[warp] = best_obj;
+                    red_k[warp] = best_k;
+                }
+                __syncthreads();
+                best_obj = lane < kWarps ? red_obj[lane] : 0;
+                best_k = lane < kWarps ? red_k[lane] : -1;
             }
-            __syncthreads();
-            best_obj = lane < kWarps ? red_obj[lane] : 0;
-            best_k = lane < kWarps ? red_k[lane] : -1;
-        }
-        const unsigned vm = __ballot_sync(full, best_k >= 0);
-        if (__popc(vm) > 1) {
             for (int off = 16; off > 0; off >>= 1) {
                 const uint64_t o = __shfl_xor_sync(full, best_obj, off);
                 const int kk = __shfl_xor_sync(full, best_k, off);
@@ -740,14 +779,10 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
                     best_k = kk;
                 }
             }
-        } else if (vm != 0) {
-            const int src = __ffs(vm) - 1;
-            best_obj = __shfl_sync(full, best_obj, src);
-            best_k = __shfl_sync(full, best_k, src);
         }
+        none = best_k < 0;            // no K with a positive, finite step time
+        K_star = none ? 0 : best_k;
     }
-    const bool none = best_k < 0;   // no K with a positive, finite step time
-    const int K_star = none ? 0 : best_k;
     if (tid == 0) {
         if (none) raise_status(status, DSPARK_STATUS_BAD_COST);
         *k_star = K_star;
@@ -805,11 +840,10 @@ __global__ void schedule_trivial_kernel(int B, double bias, const double* __rest
 // ---- one warp for at most 32 candidates ---------------------------------------------------
 // The same outputs as schedule_kernel (and, with PACK, as the pack body) when n = B*(gamma-1)
 // <= 32: lane i holds candidate i; the warp sorts the candidates' rank words with a shuffle
-// bitonic network (a single request's are in order already), scans their keys, evaluates the
-// objective of every K exactly in fp64 (one division per lane, side by side; lane 0 takes a
-// second only when n = 32: on this part one fp64 division costs about a third of a
-// microsecond) and reduces with the same comparator, so no block barrier is needed anywhere.
-// A batch of one request lives here.
+// bitonic network (a single request's are in order already), scans their keys, screens every
+// K as the block kernel does (one K per lane, K = 0 on a free lane) and, when the screen does
+// not decide, evaluates the undecided K exactly in fp64 side by side and reduces with the same
+// comparator; no block barrier anywhere. A batch of one request lives here.
 constexpr int kSmallMax = 32;
 
 template <bool PACK>
@@ -882,44 +916,68 @@ schedule_small_kernel(const float* __restrict__ conf, int B, int L, double bias,
         if (lane >= off) S += v;
     }
 
-    // 4. exact objectives and the argmax (larger objective, then smaller K). Lane i < n takes
-    // K = i + 1 and lane n, when there is one, K = 0, so that the divisions run side by side.
+    // 4. screen keys: lane i < n takes K = i + 1 and lane n, when there is one, K = 0 (lane 0
+    // takes K = 0 besides K = 1 when n = 32). The warp's best screened K is K* when every
+    // other K lies beyond the margin and all were judged; else the exact fp64 objectives of
+    // the K not judged or within the margin decide, side by side, one division per lane.
     const uint64_t base_E = static_cast<uint64_t>(B) << 32;
-    uint64_t best_obj = 0;
-    int best_k = -1;
-    if (lane <= n) {
-        const bool k0 = lane == n;
-        const double T = t0 + __longlong_as_double(k0 ? th_0 : th_k);
-        if (T > 0.0 && T < INFINITY) {
-            best_obj = __double_as_longlong(static_cast<double>(k0 ? base_E : base_E + S) / T);
-            best_k = k0 ? 0 : lane + 1;
+    DF t0d;
+    const bool t0_ok = split_double(static_cast<uint64_t>(__double_as_longlong(t0)), t0d);
+    const bool own = lane <= n;
+    const bool extra0 = n == 32 && lane == 0;
+    const int K_own = lane == n ? 0 : lane + 1;
+    const uint64_t E_own = lane == n ? base_E : base_E + S;
+    const uint64_t th_own = lane == n ? th_0 : th_k;
+    const uint64_t key_own = own ? screen_key(E_own, t0d, t0_ok, th_own) : 0;
+    const uint64_t key_x = extra0 ? screen_key(base_E, t0d, t0_ok, th_0) : 0;
+    uint64_t bk = key_own, b2 = 0;
+    int bK = key_own != 0 ? K_own : -1;
+    bool nj = (own && key_own == 0) || (extra0 && key_x == 0);
+    if (key_x != 0) {                    // K = 0 first among equal keys
+        if (key_x >= bk) {
+            b2 = bk;
+            bk = key_x;
+            bK = 0;
+        } else {
+            b2 = key_x;
         }
     }
-    if (n == 32 && lane == 0) {
-        const double T = t0 + __longlong_as_double(th_0);
-        if (T > 0.0 && T < INFINITY) {
-            const uint64_t o = __double_as_longlong(static_cast<double>(base_E) / T);
-            if (better(o, 0, best_obj, best_k)) {
+    warp_top2(bk, bK, b2, nj);
+    const uint64_t thr = bk > kKeyMargin ? bk - kKeyMargin : 0;
+    int bits = 0;
+    int K_star = bK;
+    if (nj || bK < 0 || b2 >= thr) {     // uniform across the warp
+        uint64_t best_obj = 0;
+        int best_k = -1;
+        if (own && (key_own == 0 || key_own >= thr)) {
+            const uint64_t o = small_objective(E_own, t0, th_own);
+            if (o != 0) {
+                best_obj = o;
+                best_k = K_own;
+            }
+        }
+        if (extra0 && (key_x == 0 || key_x >= thr)) {
+            const uint64_t o = small_objective(base_E, t0, th_0);
+            if (o != 0 && better(o, 0, best_obj, best_k)) {
                 best_obj = o;
                 best_k = 0;
             }
         }
-    }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const uint64_t o = __shfl_xor_sync(full, best_obj, off);
-        const int kk = __shfl_xor_sync(full, best_k, off);
-        if (better(o, kk, best_obj, best_k)) {
-            best_obj = o;
-            best_k = kk;
+        for (int off = 16; off > 0; off >>= 1) {
+            const uint64_t o = __shfl_xor_sync(full, best_obj, off);
+            const int kk = __shfl_xor_sync(full, best_k, off);
+            if (better(o, kk, best_obj, best_k)) {
+                best_obj = o;
+                best_k = kk;
+            }
         }
+        if (best_k < 0) {
+            bits |= DSPARK_STATUS_BAD_COST;
+            best_k = 0;
+        }
+        K_star = best_k;
     }
-    int bits = 0;
-    if (best_k < 0) {
-        bits |= DSPARK_STATUS_BAD_COST;
-        best_k = 0;
-    }
-    const int K_star = best_k;
 
     // 5. windows: 1 + the request's candidates among the first K*
     const bool in = lane < K_star;

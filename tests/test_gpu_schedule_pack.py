@@ -84,6 +84,34 @@ def test_schedule_invalid_cost_and_empty(dev):
     assert g["status"] == 0x10 and (g["windows"] == 1).all()
 
 
+def tie_table(B, near=()):
+    """Every objective exactly B 2^31 (gamma = 2, confidences 0.5, bias 2, theta[B + K] = K / B,
+    B a power of two); each K in `near` one ulp above the rest (its theta lowered by 2^-51)."""
+    conf = np.full((B, 1), 0.5, np.float32)
+    theta = np.zeros(2 * B + 1)
+    theta[B:] = np.arange(B + 1) / B
+    for k in near:
+        theta[B + k] -= 2.0 ** -51
+    return conf, 2.0, np.zeros(B + 1), theta
+
+
+@pytest.mark.parametrize("B", [1, 16, 32, 64, 256, 4096, 8192])
+def test_schedule_exact_and_one_ulp_ties(dev, B):
+    """Objectives that tie exactly or differ by one ulp, which no screen can order: both
+    kernels (one warp up to 32 candidates, the block kernel's bucket and bitonic sorts) must
+    fall back to the exact objectives and agree with the oracle."""
+    rng = np.random.default_rng(B)
+    cases = [()] + [tuple(int(k) for k in rng.choice(np.arange(1, B + 1), size=m, replace=False))
+                    for m in (1, 2, 5) if m <= B]
+    for near in cases:
+        conf, bias, alpha, theta = tie_table(B, near)
+        g = gpu_schedule(dev, conf, bias, alpha, theta)
+        r = oracle.schedule(conf, bias, alpha, theta)
+        assert r["k_star"] == (min(near) if near else 0)
+        np.testing.assert_array_equal(g["windows"], r["windows"])
+        assert g["k_star"] == r["k_star"] and g["status"] == r["status"] == 0
+
+
 @pytest.mark.parametrize("B,gamma", [(64, 8), (256, 8), (600, 6), (2048, 9)])
 def test_schedule_k_star_at_and_near_zero(dev, B, gamma):
     """Steep cost tables put the argmax at K = 0 or among the first few K, where the block

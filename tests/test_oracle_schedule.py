@@ -114,6 +114,44 @@ def test_tie_rule_fills_lower_request_then_lower_position(oracle_mod):
     np.testing.assert_array_equal(out["windows"], [4, 3, 1])
 
 
+def tie_table(B, near=()):
+    """gamma = 2, every confidence 0.5 (key 2^31), bias 2, alpha 0, theta[B + K] = K / B with
+    B a power of two: E(K) = (2B + K) 2^31 and T(K) = (2B + K) / B are exact doubles, so every
+    objective is exactly B 2^31. Each K in `near` gets theta lowered by 2^-51 (one ulp of T),
+    which lifts its objective one ulp above the others."""
+    conf = np.full((B, 1), 0.5, np.float32)
+    theta = np.zeros(2 * B + 1)
+    K = np.arange(B + 1)
+    theta[B:] = K / B
+    for k in near:
+        theta[B + k] -= 2.0 ** -51
+    return conf, 2.0, np.zeros(B + 1), theta
+
+
+@pytest.mark.parametrize("B", [1, 16, 64])
+def test_equal_objectives_take_the_smallest_k(oracle_mod, B):
+    """Exact ties: every K has the same objective, so K* = 0 (the smallest K)."""
+    conf, bias, alpha, theta = tie_table(B)
+    out = oracle_mod.schedule(conf, bias, alpha, theta)
+    assert all(o == B * 2.0 ** 31 for o in out["obj"])
+    assert out["k_star"] == 0
+    np.testing.assert_array_equal(out["windows"], 1)
+
+
+def test_one_ulp_apart_objectives(oracle_mod):
+    """Near ties: a K whose step time is one ulp shorter wins by one ulp of the objective;
+    among two such K the smaller wins; the windows fill requests in order (equal keys)."""
+    B = 64
+    conf, bias, alpha, theta = tie_table(B, near=(37,))
+    out = oracle_mod.schedule(conf, bias, alpha, theta)
+    assert out["obj"][37] == np.nextafter(B * 2.0 ** 31, np.inf)
+    assert out["k_star"] == 37
+    np.testing.assert_array_equal(out["windows"], [2] * 37 + [1] * (B - 37))
+    conf, bias, alpha, theta = tie_table(B, near=(50, 21))
+    out = oracle_mod.schedule(conf, bias, alpha, theta)
+    assert out["k_star"] == 21
+
+
 def test_theta_zero_keeps_every_positive_survival(oracle_mod):
     rng = np.random.default_rng(5)
     B, gamma = 17, 8
