@@ -36,17 +36,19 @@
 namespace dspark {
 namespace {
 
-#ifndef DSPARK_SCHED_THREADS
-#define DSPARK_SCHED_THREADS 1024
-#endif
-constexpr int kThreads = DSPARK_SCHED_THREADS;   // the block kernel's CTA: 512 or 1024
-static_assert(kThreads == 512 || kThreads == 1024, "the block scheduler runs 512 or 1024 threads");
-constexpr int kWarps = kThreads / 32;
 constexpr int kMergeMax = 4096;          // ping-pong merge buffers up to this many words
-constexpr int kMergeItems = kMergeMax / kThreads;
 constexpr int kBuckets = 4096;           // 128 buckets per power of two of the key (keys 0, 1 share)
-constexpr int kBucketsPerThread = kBuckets / kThreads;
-constexpr int kTiersPerThread = (DSPARK_MAX_TIERS + kThreads - 1) / kThreads;
+constexpr int kSmallBlockMax = 256;      // up to this many candidates: a 256-thread block
+
+// The block kernel's shape: 1024 threads, or 256 for at most 256 candidates (fewer warps for
+// the same few items: every reduction, scan and loop bound of the block costs less).
+template <int NT>
+struct Shape {
+    static_assert(NT == 256 || NT == 1024, "the block scheduler runs 256 or 1024 threads");
+    static constexpr int kMergeItems = (NT == 256 ? kSmallBlockMax : kMergeMax) / NT;
+    static constexpr int kBucketsPerThread = kBuckets / NT;
+    static constexpr int kTiersPerThread = (DSPARK_MAX_TIERS + NT - 1) / NT;
+};
 constexpr int kBucketMax = 64;           // larger buckets (many equal keys): merge instead
 // The screened best decides K* alone when every other key lies more than this below it:
 // 2^19 key units, at least 2^-37 of the objective, sixteen times the 2^-41 that two screened
@@ -278,15 +280,17 @@ __device__ __forceinline__ T warps_before(const T* total, int warp, int lane)
 // padding. win(b) gives request b's window; owner holds M ints and may overlay what win reads
 // (every window is read before the block barrier), and win_s (B ints outside the owner map)
 // keeps each thread's windows for the pass after it.
-template <typename WinFn>
+template <int NT, typename WinFn>
 __device__ __forceinline__ void pack_after_schedule(WinFn win, int B, int gamma, int K_star,
                                                     PackArgs pk,
-                                                    const int (&tier_pre)[kTiersPerThread],
+                                                    const int (&tier_pre)[Shape<NT>::kTiersPerThread],
                                                     const int* tok_stage, int* owner,
                                                     int* tier_s, int* pack_total, int* win_s,
                                                     int32_t* __restrict__ windows,
                                                     int32_t* __restrict__ status)
 {
+    constexpr int kThreads = NT;
+    constexpr int kTiersPerThread = Shape<NT>::kTiersPerThread;
     // the output pointers as plain locals: no store below can be taken to change them
     int32_t* const cu = pk.cu;
     int32_t* const packed_ids = pk.packed_ids;
@@ -417,13 +421,18 @@ __device__ __forceinline__ void prefetch_inputs(int t, int nthreads, const float
 }
 
 // PACK: the same CTA then front-packs the windows it computed (dspark_schedule_pack).
-template <bool MERGE, bool PACK>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool MERGE, bool PACK, int NT>
+__global__ void __launch_bounds__(NT, 1)
 schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, double bias,
                 const double* __restrict__ alpha, const double* __restrict__ theta,
                 int32_t* __restrict__ windows, int32_t* __restrict__ k_star,
                 int32_t* __restrict__ status, PackArgs pk, int tok_stage_off)
 {
+    constexpr int kThreads = NT;
+    constexpr int kWarps = NT / 32;
+    constexpr int kMergeItems = Shape<NT>::kMergeItems;
+    constexpr int kBucketsPerThread = Shape<NT>::kBucketsPerThread;
+    constexpr int kTiersPerThread = Shape<NT>::kTiersPerThread;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     // MERGE: keys ksrc [n] (u32), indices isrc [n], then the ping-pong pair kdst, idst (the
     // bucket path uses that second half as n 64-bit rank words); else words [n_pad] (u64).
@@ -811,10 +820,10 @@ schedule_kernel(const float* __restrict__ conf, int B, int L, int n, int n_pad, 
         __shared__ int pack_total[kWarps];
         int* owner = reinterpret_cast<int*>(smem_raw);   // sort buffers: at least B + n ints
         if (MERGE)
-            pack_after_schedule(win_rank, B, L + 1, K_star, pk, tier_pre, tok_stage, owner,
+            pack_after_schedule<NT>(win_rank, B, L + 1, K_star, pk, tier_pre, tok_stage, owner,
                                 &tier_s, pack_total, count, windows, status);
         else
-            pack_after_schedule(win_count, B, L + 1, K_star, pk, tier_pre, tok_stage, owner,
+            pack_after_schedule<NT>(win_count, B, L + 1, K_star, pk, tier_pre, tok_stage, owner,
                                 &tier_s, pack_total, count, windows, status);
     } else {
         for (int b = tid; b < B; b += kThreads) windows[b] = MERGE ? win_rank(b) : win_count(b);
@@ -1068,17 +1077,20 @@ int launch_schedule_kernel(const char* what, const float* conf, int B, int L,
     int n_pad = 1;
     while (n_pad < n) n_pad <<= 1;
     const bool merge = n <= kMergeMax;
+    const bool small = n <= kSmallBlockMax;
     size_t smem = (merge ? 16 * static_cast<size_t>(n) : 8 * static_cast<size_t>(n_pad)) +
                   sizeof(int) * static_cast<size_t>(B);
     DeviceInfo dev;
     int rc = current_device(&dev);
     if (rc != DSPARK_OK) return rc;
+    // variants: 0 bitonic (1024 threads), 1 bucket or merge (1024), 2 bucket or merge (256)
+    const void* fns[3] = {reinterpret_cast<const void*>(schedule_kernel<false, PACK, 1024>),
+                          reinterpret_cast<const void*>(schedule_kernel<true, PACK, 1024>),
+                          reinterpret_cast<const void*>(schedule_kernel<true, PACK, 256>)};
     static thread_local int configured_device = -1;
-    static thread_local size_t max_dynamic[2] = {0, 0};
+    static thread_local size_t max_dynamic[3] = {0, 0, 0};
     if (configured_device != dev.device) {
-        const void* fns[2] = {reinterpret_cast<const void*>(schedule_kernel<false, PACK>),
-                              reinterpret_cast<const void*>(schedule_kernel<true, PACK>)};
-        for (int v = 0; v < 2; ++v) {
+        for (int v = 0; v < 3; ++v) {
             cudaFuncAttributes attr;
             if (cudaFuncGetAttributes(&attr, fns[v]) != cudaSuccess)
                 return check_launch("schedule (attributes)");
@@ -1089,26 +1101,31 @@ int launch_schedule_kernel(const char* what, const float* conf, int B, int L,
         }
         configured_device = dev.device;
     }
-    if (smem > max_dynamic[merge ? 1 : 0])
+    const int v = !merge ? 0 : small ? 2 : 1;
+    if (smem > max_dynamic[v])
         return fail(DSPARK_ERR_UNSUPPORTED, "%s: %zu bytes of shared memory needed, the device "
-                    "allows %zu", what, smem, max_dynamic[merge ? 1 : 0]);
+                    "allows %zu", what, smem, max_dynamic[v]);
     // the pack's tokens staged behind the scheduler's arrays when they fit (16-byte aligned)
     int stage_off = -1;
     if (PACK && reinterpret_cast<uintptr_t>(pk.tokens) % 16 == 0) {
         const size_t off = align_to(smem, 16);
         const size_t need = off + sizeof(int) * static_cast<size_t>(B) * (L + 1);
-        if (need <= max_dynamic[merge ? 1 : 0]) {
+        if (need <= max_dynamic[v]) {
             stage_off = static_cast<int>(off);
             smem = need;
         }
     }
-    if (merge)
-        return launch_pdl(what, schedule_kernel<true, PACK>, dim3(1), dim3(kThreads), smem,
+    if (v == 2)
+        return launch_pdl(what, schedule_kernel<true, PACK, 256>, dim3(1), dim3(256), smem,
                           stream, conf, B, L, n, n_pad, cost->bias, cost->alpha, cost->theta,
                           windows, k_star, status, pk, stage_off);
-    return launch_pdl(what, schedule_kernel<false, PACK>, dim3(1), dim3(kThreads), smem, stream,
-                      conf, B, L, n, n_pad, cost->bias, cost->alpha, cost->theta, windows,
-                      k_star, status, pk, stage_off);
+    if (v == 1)
+        return launch_pdl(what, schedule_kernel<true, PACK, 1024>, dim3(1), dim3(1024), smem,
+                          stream, conf, B, L, n, n_pad, cost->bias, cost->alpha, cost->theta,
+                          windows, k_star, status, pk, stage_off);
+    return launch_pdl(what, schedule_kernel<false, PACK, 1024>, dim3(1), dim3(1024), smem,
+                      stream, conf, B, L, n, n_pad, cost->bias, cost->alpha, cost->theta,
+                      windows, k_star, status, pk, stage_off);
 }
 
 }  // namespace
