@@ -38,7 +38,9 @@ def tables(rng, B, gamma, kind):
 SIZES = [(1, 1), (1, 2), (4, 4), (3, 32), (7, 8), (100, 5), (256, 8), (512, 8), (1000, 17),
          (2048, 9), (8192, 2), (8192, 3), (5, 1), (1023, 2), (1025, 3),
          # the one-warp kernel's range (n <= 32) and just past it
-         (32, 2), (16, 3), (2, 17), (11, 3), (1, 32), (1, 16), (33, 2), (3, 12)]
+         (32, 2), (16, 3), (2, 17), (11, 3), (1, 32), (1, 16), (33, 2), (3, 12),
+         # the 256-thread block (n <= 256) at its edge and the 1024-thread block just past it
+         (128, 3), (8, 32), (257, 2), (52, 6)]
 
 
 @pytest.mark.parametrize("B,gamma", SIZES)
