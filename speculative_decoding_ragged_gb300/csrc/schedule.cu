@@ -65,8 +65,9 @@ __device__ __forceinline__ bool better(uint64_t o1, int k1, uint64_t o2, int k2)
 // ---- the screen: obj(K) in double-float arithmetic (pairs of fp32 values) ----
 // The exact objective is an fp64 division, and FP64 latency on this part is long (one
 // division about 660 cycles). K* is an output but the objective is not, so a screen accurate
-// to 2^-40 relative decides K* whenever the best screened K beats every other by more than
-// twice that; only ties, near ties and cost tables the screen cannot judge take fp64.
+// to 2^-42 relative decides K* whenever the best screened K beats every other by the margin
+// kKeyMargin (at least 2^-37); only ties, near ties and cost tables the screen cannot judge
+// take fp64.
 struct DF {
     float h, l;     // value h + l, |l| <= ulp(h) / 2 once normalised
 };
