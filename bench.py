@@ -117,6 +117,13 @@ def sum_over_ranks(x, world):
     return float(t.item())
 
 
+def whole_job(ms_local, rows_local, world):
+    """The job's time (the slowest rank's), rows (every rank's) and rows/s over all ranks."""
+    ms = max_over_ranks(ms_local, world)
+    rows = sum_over_ranks(rows_local, world)
+    return ms, rows, rows / (ms * 1e-3)
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -500,11 +507,8 @@ def run_native(args, rank, world, local):
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    ms = t_start.elapsed_time(t_end)
-    ms = max_over_ranks(ms, world)
-    rows = sum(batches[i % nb]["M"] for i in range(K))
-    rows = sum_over_ranks(rows, world)
-    value = rows / (ms * 1e-3)
+    ms, rows, value = whole_job(t_start.elapsed_time(t_end),
+                                sum(batches[i % nb]["M"] for i in range(K)), world)
 
     # end to end through the C ABI with host buffers: every step copies its confidences,
     # tokens and packed logits from pinned host memory and reads its results back, inside the
