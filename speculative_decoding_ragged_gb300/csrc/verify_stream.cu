@@ -222,13 +222,25 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
     }
 }
 
+// An L2 policy that marks lines for eviction first: the logits are read once, so they should
+// not push out of L2 what the step's other kernels use again (their code, the small inputs
+// and outputs, the partials).
+__device__ __forceinline__ uint64_t evict_first_policy()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 // Global -> shared copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) by the
-// TMA engine; completion is counted on `bar`.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
+// TMA engine under the L2 policy `pol`; completion is counted on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                          uint64_t pol)
 {
     asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(pol)
         : "memory");
 }
 
@@ -332,6 +344,7 @@ verify_bulk_kernel(StreamArgs A, int stages, int stage_bytes)
         };
         bool ok = true;
         DraftCursor cur;
+        const uint64_t pol = evict_first_policy();
         int s = 0;
         uint32_t ph = 0;                              // parity of this use of stage s
         int64_t k = 0;
@@ -363,7 +376,7 @@ verify_bulk_kernel(StreamArgs A, int stages, int stage_bytes)
                 const uint32_t bytes = static_cast<uint32_t>(v1 - v0) * E;
                 mbar_arrive_expect_tx(full, bytes);
                 bulk_load(smem_addr(ring + static_cast<size_t>(s) * stage_bytes),
-                          row + static_cast<int64_t>(v0) * E, bytes, full);
+                          row + static_cast<int64_t>(v0) * E, bytes, full, pol);
             }
             if (++s == stages) { s = 0; ph ^= 1u; }
         }
