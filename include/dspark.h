@@ -219,8 +219,8 @@ int dspark_schedule_pack(const float* conf, int B, int gamma, const dspark_cost*
  *   request (always -1 in greedy mode).
  * workspace: device scratch of at least dspark_verify_workspace_bytes(B, gamma, V, stochastic)
  *   bytes, 16-byte aligned, owned by the caller; no clearing needed. Its first 256 bytes carry
- *   state from one call to the next: the bulk-copy streaming kernel hands out the second half
- *   of its work from a counter there (bytes 4-7), and each call leaves that counter at zero,
+ *   state from one call to the next: the bulk-copy streaming kernel hands out most of its
+ *   work from a counter there (bytes 4-7), and each call leaves that counter at zero,
  *   between a 32-bit tag (bytes 0-3) and a 64-bit tag (bytes 8-15), for the next call. A call
  *   that finds either tag missing (a fresh or zeroed workspace, or one whose first bytes were
  *   written since) splits its work evenly instead, with identical results. Between two calls

@@ -135,14 +135,15 @@ verify_stream_kernel(StreamArgs A)
 
 // ---- bulk-copy streaming -----------------------------------------------------------------
 // A persistent grid (a few CTAs per SM). CTA i streams unit i first; of the remaining units
-// the first half is split into one contiguous run per CTA and the second half is handed out one
-// unit at a time from the counter in the workspace head (an atomic ticket, fetched while the
-// previous copy lands), so CTAs on SMs that stream faster take more of the tail. Without a
-// valid head every remaining unit is in the runs. Warp kBulkConsumers is the producer: its
-// lane 0, for its k-th unit, waits until stage
-// k % S is free, records the unit in the stage's slot, arms the stage's "full" mbarrier with
-// the unit's byte count (the arrive publishes the slot) and starts one cp.async.bulk of the
-// whole chunk into the stage; after its last unit it posts one end marker per consumer.
+// the first quarter is split into one contiguous run per CTA and the other three quarters are
+// handed out one unit at a time from the counter in the workspace head (an atomic ticket,
+// fetched while the previous copy lands), so CTAs on SMs that stream faster, or that started
+// later (a step's scheduler holds one SM's registers until it ends), take more of the tail.
+// Without a valid head every remaining unit is in the runs. Warp kBulkConsumers is the
+// producer: its lane 0, for its k-th unit, waits until stage k % S is free, records the unit
+// in the stage's slot, arms the stage's "full" mbarrier with the unit's byte count (the arrive
+// publishes the slot) and starts one cp.async.bulk of the whole chunk into the stage; after
+// its last unit it posts one end marker per consumer.
 // Consumer warp k % kBulkConsumers waits on the full barrier, reads the slot, folds the staged
 // chunk with the same per-lane order as the register kernel, releases the stage on its "empty"
 // barrier and writes the unit's partial. Every wait is bounded (about a second of SM clock from
@@ -153,7 +154,9 @@ verify_stream_kernel(StreamArgs A)
 // ended between 40.9 and 46.4 us, since SMs stream at rates a few per cent apart. Handing out
 // the second half by ticket took the launch from 51.1 to 49.6 us and the high-load cap-accept
 // launch from 178 to 170.5 us; a fifth, a third or all of the units by ticket landed within a
-// microsecond of that, a tenth or a twentieth gained less (172-174 us at high load). Each
+// microsecond of that, a tenth or a twentieth gained less (172-174 us at high load); three
+// quarters by ticket then shortened the whole large-vocab step by 0.15-0.2 us, all of them
+// lengthened it by 0.25 us. Each
 // CTA's first unit is fixed so that the head's tag, one L2 or DRAM round trip, is read while
 // that unit's copy is in flight instead of before it. (Starting that copy before the PDL wait,
 // where the unit is certainly a target row, shortened the bench's chained steps by 0.3-0.6 us
@@ -312,8 +315,9 @@ verify_bulk_kernel(StreamArgs A, int stages, int stage_bytes)
         if (lane != 0) return;
         // Units: first unit blockIdx.x, whatever the head says, so the first copy is in flight
         // before the head's tag arrives; then of the rest [G, U) a contiguous run per CTA over
-        // the first half and tickets for the second half when the head is valid, else runs over
-        // all of it. No kernel writes the head while this one runs: every CTA reads one tag.
+        // the first quarter and tickets for the other three quarters when the head is valid,
+        // else runs over all of it. No kernel writes the head while this one runs: every CTA
+        // reads one tag.
         const int64_t G = gridDim.x;
         unsigned long long head_w, head_t;            // compared only when first needed
         ws_head_read(A.head, head_w, head_t);
@@ -326,7 +330,7 @@ verify_bulk_kernel(StreamArgs A, int stages, int stage_bytes)
             if (phase == 0) {
                 tickets = ws_head_tags_ok(head_w, head_t);
                 const int64_t R = U > G ? U - G : 0;
-                S = tickets ? R - R / 2 : R;
+                S = tickets ? R / 4 : R;
                 u = G + static_cast<int64_t>(blockIdx.x) * S / G;
                 u1 = G + static_cast<int64_t>(blockIdx.x + 1) * S / G;
                 if (tickets) tk = ws_head_ticket(A.head);  // used after the run
