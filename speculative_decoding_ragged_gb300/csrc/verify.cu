@@ -8,10 +8,12 @@
 //
 // Kernels of one call:
 // 1. the streaming kernel (verify_stream.cu): one partial per (row, chunk) unit;
-// 2. greedy: verify_finalize_kernel — one CTA per request: combines the chunk partials of its
-//    rows, tests each draft against its row's argmax, walks to the first rejection, writes
-//    accept_len / committed / ceiling (and, fused, appends the committed tokens to the
-//    request's history);
+// 2. greedy: verify_finalize_kernel — a CTA per request, or per two or four requests when one
+//    per request would occupy every SM (the next step's scheduler, one CTA holding a whole SM's
+//    registers, then starts on a free SM while this kernel works): combines the chunk partials
+//    of each request's rows, tests each draft against its row's argmax, walks to the first
+//    rejection, writes accept_len / committed / ceiling (and, fused, appends the committed
+//    tokens to the request's history);
 //    stochastic: bonus_final_kernel — spread over the grid: every CTA of a request combines its
 //    rows' partials and runs the accept tests (Philox4x64-10 uniforms), sums the bonus row's
 //    weights over its tiles, and the last CTA of the request draws the bonus token.
@@ -361,19 +363,25 @@ __device__ __forceinline__ void bad_rows_outputs(const FinalArgs& A, int b, int6
     }
 }
 
-// Greedy verify's finaliser: one CTA per request combines the argmax partials of its rows (one
-// warp per row), then warp 0 runs the accept tests, walks to the first rejection and writes the
-// request's outputs (and, fused, appends its tokens to the history).
-template <int DT, int FT>
-__global__ void __launch_bounds__(FT)
+// Greedy verify's finaliser: FT threads per request (RPC requests per CTA) combine the argmax
+// partials of the request's rows (one warp per row), then the request's warp 0 runs the accept
+// tests, walks to the first rejection and writes the request's outputs (and, fused, appends its
+// tokens to the history).
+template <int DT, int FT, int RPC>
+__global__ void __launch_bounds__(FT * RPC)
 verify_finalize_kernel(FinalArgs A)
 {
-    constexpr int kFinalThreads = FT;
+    constexpr int kFinalThreads = FT;                 // threads per request
     constexpr int kFinalWarps = FT / 32;
-    __shared__ int g_s[DSPARK_MAX_GAMMA];
+    __shared__ int g_ss[RPC][DSPARK_MAX_GAMMA];
 
-    const int b = blockIdx.x;
-    const int tid = threadIdx.x;
+    // RPC requests per CTA, FT threads each; a request index past B (the last CTA) idles but
+    // meets the block barrier
+    const int r = RPC == 1 ? 0 : static_cast<int>(threadIdx.x) / FT;
+    const bool live = static_cast<int>(blockIdx.x) * RPC + r < A.B;
+    const int b = live ? static_cast<int>(blockIdx.x) * RPC + r : 0;
+    int* const g_s = g_ss[r];
+    const int tid = static_cast<int>(threadIdx.x) - r * FT;
     const int lane = tid & 31;
     const int warp = tid >> 5;
     const int gamma = A.gamma;
@@ -403,23 +411,23 @@ verify_finalize_kernel(FinalArgs A)
     reset_ws_head(A.head);
     int32_t* out = A.committed + static_cast<int64_t>(b) * gamma;
 
-    if (!rows_ok) {
-        bad_rows_outputs(A, b, base, nrows, tid, kFinalThreads, bits, n_hist);
-        return;
-    }
+    if (live && !rows_ok) bad_rows_outputs(A, b, base, nrows, tid, kFinalThreads, bits, n_hist);
+    const bool work = live && rows_ok;
     const int ndec = nrows - 1;   // accept tests this mode runs
 
     // 1. per-row argmax from the chunk partials, one warp per row
-    for (int t = warp; t < nrows; t += kFinalWarps) {
-        const int g = combine_arg(static_cast<const ArgPart*>(A.part_t) + (base + t) * A.nc,
-                                  A.nc, lane);
-        if (lane == 0) g_s[t] = g;
+    if (work) {
+        for (int t = warp; t < nrows; t += kFinalWarps) {
+            const int g = combine_arg(static_cast<const ArgPart*>(A.part_t) + (base + t) * A.nc,
+                                      A.nc, lane);
+            if (lane == 0) g_s[t] = g;
+        }
     }
     __syncthreads();
 
     // 2. warp 0: accept tests (lane i tests draft d_{i+1} against row i's argmax), the walk to
     //    the first rejection, the outputs and the fused scatter
-    if (warp == 0) {
+    if (work && warp == 0) {
         const bool tested = lane < ndec;
         const bool valid = d_mine >= 0 && d_mine < A.V;
         if (tested && !valid) bits |= DSPARK_STATUS_BAD_TOKEN;
@@ -889,10 +897,23 @@ int run_verify(const VerifyCall& c, const Plan& plan, WsHead* head, void* part_t
     fa.n_tiles = (c.V + 255) / 256;
     if (!STOCH) {
         if (c.B <= kFinalSmallBatch)
-            return launch_pdl("verify (finalize)", verify_finalize_kernel<DT, kFinalThreadsSmall>,
+            return launch_pdl("verify (finalize)", verify_finalize_kernel<DT, kFinalThreadsSmall, 1>,
                               dim3(c.B), dim3(kFinalThreadsSmall), 0, stream, fa);
-        return launch_pdl("verify (finalize)", verify_finalize_kernel<DT, kFinalThreadsLarge>,
-                          dim3(c.B), dim3(kFinalThreadsLarge), 0, stream, fa);
+        // two or four requests per CTA when one per CTA would put a CTA on every SM: the next
+        // step's scheduler (one CTA holding a whole SM's registers) can then start on a free SM
+        // while the finaliser works
+        DeviceInfo dev;
+        rc = current_device(&dev);
+        if (rc != DSPARK_OK) return rc;
+        const int room = dev.sm_count - dev.sm_count / 8;
+        if (c.B <= room)
+            return launch_pdl("verify (finalize)", verify_finalize_kernel<DT, kFinalThreadsLarge, 1>,
+                              dim3(c.B), dim3(kFinalThreadsLarge), 0, stream, fa);
+        if (c.B <= 2 * room)
+            return launch_pdl("verify (finalize)", verify_finalize_kernel<DT, kFinalThreadsLarge, 2>,
+                              dim3((c.B + 1) / 2), dim3(2 * kFinalThreadsLarge), 0, stream, fa);
+        return launch_pdl("verify (finalize)", verify_finalize_kernel<DT, kFinalThreadsLarge, 4>,
+                          dim3((c.B + 3) / 4), dim3(4 * kFinalThreadsLarge), 0, stream, fa);
     }
     // one tile per warp while the batch's bonus rows would not cover the SMs, four otherwise
     DeviceInfo dev;
