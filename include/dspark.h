@@ -229,8 +229,9 @@ int dspark_schedule_pack(const float* conf, int B, int gamma, const dspark_cost*
  *   not overlap on the GPU.
  * Limits: 0 <= B, 1 <= gamma <= DSPARK_MAX_GAMMA, V >= 1, temperature > 0 (stochastic).
  * Kernels: a persistent streaming kernel over fixed row chunks (register or TMA bulk-copy
- * streaming, see dspark_set_stream_kernel), then, greedy: one CTA per request that combines
- * the chunk results, walks and writes the outputs; stochastic: a bonus kernel spread over the
+ * streaming, see dspark_set_stream_kernel), then, greedy: a finaliser (256 threads or more per
+ * request, one to four requests per CTA) that combines the chunk results, walks and writes
+ * the outputs; stochastic: a bonus kernel spread over the
  * grid whose CTAs each combine their request's chunk results and run its accept tests, sum
  * the bonus row's weights over their tiles; CTA 0 of a request writes its accept length,
  * drafts and ceiling, and the request's last CTA to finish draws the bonus token and, in
