@@ -51,11 +51,15 @@ def test_fused_step_matches_the_oracle(dev, case):
 
 @pytest.mark.parametrize("B,gamma,stochastic", [(1024, 5, False), (2049, 3, True),
                                                 (4096, 4, False), (8192, 2, True),
-                                                (4000, 5, False)])
+                                                (4000, 5, False),
+                                                # greedy finaliser CTAs of two or four
+                                                # requests with idle slots in the last one
+                                                (201, 4, False), (299, 3, False),
+                                                (513, 2, False)])
 def test_fused_step_large_batches(dev, B, gamma, stochastic):
     """Batches up to the limit (more requests than threads in the scheduler and the pack, the
-    bitonic scheduler past 4096 candidates), with a small vocabulary so that the oracle stays
-    quick."""
+    bitonic scheduler past 4096 candidates), and greedy batches whose size the finaliser's
+    requests per CTA do not divide, with a small vocabulary so that the oracle stays quick."""
     rng = np.random.default_rng(B + gamma)
     tiers = sorted(set(int(t) for t in rng.integers(B, B * gamma + 1, size=6)))
     _check_fused_step(dev, B, rng, B, gamma, 512, "bf16", stochastic, "compact", 1.0, tiers,
