@@ -61,7 +61,7 @@ extern "C" {
 /* ---- return codes ---------------------------------------------------------------------- */
 #define DSPARK_OK                  0
 #define DSPARK_ERR_INVALID_ARG   (-1)  /* null pointer, bad size, bad enum, short workspace */
-#define DSPARK_ERR_UNSUPPORTED   (-2)  /* valid request beyond this build's limits           */
+#define DSPARK_ERR_UNSUPPORTED   (-2)  /* valid request beyond the library's limits          */
 #define DSPARK_ERR_CUDA          (-3)  /* the CUDA runtime refused a query or a launch       */
 
 /* ---- device status bits (OR-ed into the caller's int32 status word) -------------------- */
@@ -76,7 +76,7 @@ extern "C" {
 #define DSPARK_STATUS_STALL         0x100 /* a bounded in-kernel wait gave up: this call's verify
                                              results are invalid (not expected in operation)   */
 
-/* ---- limits of this build ------------------------------------------------------------- */
+/* ---- limits of the library ----------------------------------------------------------- */
 #define DSPARK_MAX_GAMMA        32     /* block width                                         */
 #define DSPARK_MAX_CANDIDATES   16384  /* B*(gamma-1): the scheduler sorts them in one CTA    */
 #define DSPARK_MAX_BATCH        8192   /* B for schedule and pack (single-CTA scans)          */
@@ -284,7 +284,7 @@ int dspark_verify_scatter(dspark_mode mode, int stochastic,
 /* ---------------------------------------------------------------------------------------
  * dspark_set_stream_kernel — which kernel streams the logits inside dspark_verify and
  * dspark_verify_scatter, for every later call in this process:
- *   DSPARK_STREAM_AUTO (0, the default): this build's choice;
+ *   DSPARK_STREAM_AUTO (0, the default): the library's choice;
  *   DSPARK_STREAM_REGISTER (1): warps stream 16-byte loads into registers;
  *   DSPARK_STREAM_BULK (2): a producer warp per CTA moves whole chunks into shared memory with
  *     the TMA bulk-copy engine (cp.async.bulk, mbarrier completion) and four warps fold them;

@@ -8,9 +8,8 @@ all-reduce(MAX) of that int32 tier per step, done in place on meta[1] where the 
 so the host never reads M or the tier. The rank then re-packs with the agreed tier as its only
 tier (dspark_pack pads rows M..tier), so every rank replays the same graph shape.
 
-Every call of this build runs on one GPU, so the collective runs over whatever process group
-the caller provides: gloo on CPU tensors in the multi-rank tests, NCCL on device tensors in a
-multi-GPU job.
+The collective runs over whatever process group the caller provides: gloo on CPU tensors in
+the multi-rank tests, NCCL on device tensors in a multi-GPU job.
 """
 from __future__ import annotations
 

@@ -1,7 +1,7 @@
 """bench.py on more than one rank, on CPU ranks over gloo (world size 2): the whole-job
 aggregation (the slowest rank's time, every rank's rows, rows/s over all of them), the barrier,
 and the reference arm launched by torchrun, where rank 0 alone runs and prints its JSON line
-and the other rank exits 0 without work. The GPU arm's timed region runs only on a GPU machine;
+and the other rank exits 0 without work. The GPU arm's timed region needs a GPU;
 what it hands to this aggregation is what is tested here."""
 import json
 import os

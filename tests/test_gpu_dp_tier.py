@@ -1,7 +1,7 @@
 """DP tier agreement on the device ("DSpark in SGLang", A2 ragged verify over full CUDA graphs:
 every DP rank replays the largest tier any rank needs). The fused schedule-and-pack writes
-meta = {M, tier} on the GPU; TierSync all-reduces meta[1] in place over an NCCL group (one rank
-here: every call of this build gets one GPU) and hands the agreed tier, still on the device, to
+meta = {M, tier} on the GPU; TierSync all-reduces meta[1] in place over an NCCL group (of one
+rank: the test runs on a single GPU) and hands the agreed tier, still on the device, to
 the re-pack as its only tier. The re-pack must equal the oracle's pack with that tier."""
 import numpy as np
 import pytest
